@@ -1,0 +1,246 @@
+"""Plain Python restatement of the iteration-level scheduler and block pool.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).  The native scheduler in
+the product library must emit exactly the same metadata, step by step, for the
+same request trace.  This file is written for readability, not speed.
+
+Sources and the reading taken where they differ:
+
+* Block pool: a preallocated set of physical block ids and a free list used as
+  a stack (pop from the end, push freed ids back on the end) -- "Project 17",
+  Step 4 "Implement the paged KV cache" (BlockPool), and the free-list-as-stack
+  of "Build a pure-Python continuous batching LLM serving engine", Step 2.
+  Allocation of n blocks is all-or-nothing; failure is reported, never a crash.
+* Step order -- retire, admit, run one iteration -- from "Project 17" Step 2
+  (Scheduler.step) and "Continuous Batching" §4 (Engine.Step).
+* Admission is first-come-first-served and stops at the first request that does
+  not fit ("Continuous Batching" §4: break on allocation failure), with
+  optimistic allocation: blocks for the tokens known now, grown as the
+  sequence grows (§5 "Admission policy").  A recomputed request needs blocks
+  for prompt + generated tokens, not the prompt alone.
+* Per-step token budget max_num_batched_tokens and prefill chunks of at most
+  `chunk` tokens riding with decodes (§5 "Mixed batching").
+* Preemption by recompute: free the victim's blocks, push it to the FRONT of
+  the waiting queue, re-prefill prompt + generated later (§4 preempt, §5
+  "Preemption").  Victim: the most recently admitted running request (LIFO,
+  §5 "Victim selection"); if that is the request that needs the block, it
+  preempts itself (matching §4, where the request that needs the block is
+  the one re-queued).
+* Retire on EOS (a pre-drawn output length here), on max_tokens, or when the
+  total length reaches max_model_len (tiny-vllm part 7 "Termination and
+  returning blocks"); blocks are freed immediately (§1 lifecycle diagram).
+* Context length of a scheduled sequence counts its tokens appended this step
+  (tiny-vllm part 7 "Uploading the active arrays to the GPU").
+
+Emitted per step: prefill chunks (more than one new token) first, then decode
+sequences (exactly one new token), each group in scheduling order.
+"""
+from collections import deque
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+
+
+class OutOfBlocks(Exception):
+    pass
+
+
+class BlockPool:
+    def __init__(self, num_blocks: int, initial_order=None):
+        self.num_blocks = num_blocks
+        if initial_order is None:
+            self.free_list = list(range(num_blocks))
+        else:
+            self.free_list = [int(x) for x in initial_order]
+            assert sorted(self.free_list) == list(range(num_blocks))
+        self.fail_at = None      # fault injection: fail the n-th alloc call (1-based)
+        self.alloc_calls = 0
+
+    def free_count(self) -> int:
+        return len(self.free_list)
+
+    def alloc(self, n: int) -> List[int]:
+        self.alloc_calls += 1
+        if self.fail_at is not None and self.alloc_calls == self.fail_at:
+            raise OutOfBlocks("injected")
+        if n > len(self.free_list):
+            raise OutOfBlocks("need %d, free %d" % (n, len(self.free_list)))
+        return [self.free_list.pop() for _ in range(n)]
+
+    def free(self, ids) -> None:
+        for i in ids:
+            self.free_list.append(int(i))
+
+
+@dataclass
+class Request:
+    rid: int
+    prompt_len: int
+    max_tokens: int
+    eos_after: int                 # output length at which the request emits EOS
+    generated: int = 0
+    num_computed: int = 0          # tokens whose K/V are in the cache
+    blocks: List[int] = field(default_factory=list)
+    state: str = "waiting"         # waiting | running | finished
+    arrival_step: int = 0
+    finish_step: int = -1
+    preemptions: int = 0
+
+    @property
+    def length(self) -> int:
+        return self.prompt_len + self.generated
+
+
+@dataclass
+class StepMeta:
+    seq_rids: np.ndarray           # int64 [S]
+    q_lens: np.ndarray             # int32 [S]
+    context_lens: np.ndarray       # int32 [S]
+    cu_seqlens: np.ndarray         # int32 [S+1]
+    block_tables: np.ndarray       # int32 [S, max_blocks], -1 padded
+    slot_mapping: np.ndarray       # int64 [T]
+    token_rids: np.ndarray         # int64 [T]
+    token_pos: np.ndarray          # int32 [T]
+    num_prefill: int
+
+
+def cdiv(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+class Scheduler:
+    def __init__(self, num_blocks: int, block_size: int = 16, max_batch: int = 256,
+                 max_num_batched_tokens: int = 8192, chunk: int = 512, max_model_len: int = 8192,
+                 initial_order=None):
+        self.bs = block_size
+        self.pool = BlockPool(num_blocks, initial_order)
+        self.max_batch = max_batch
+        self.budget = max_num_batched_tokens
+        self.chunk = chunk
+        self.max_model_len = max_model_len
+        self.max_blocks = cdiv(max_model_len, block_size)
+        self.waiting = deque()
+        self.running: List[Request] = []
+        self.finished: List[Request] = []
+        self.step_no = 0
+        self.n_preemptions = 0
+        self.sum_running = 0
+
+    def add(self, rid: int, prompt_len: int, max_tokens: int, eos_after: int) -> None:
+        # A request that needs more blocks than the pool holds is accepted but
+        # never admitted (it stays at the head of the queue).
+        if prompt_len < 1 or prompt_len >= self.max_model_len or max_tokens < 1 or eos_after < 1:
+            raise ValueError("bad request")
+        self.waiting.append(Request(rid, prompt_len, max_tokens, eos_after, arrival_step=self.step_no))
+
+    def _preempt(self, r: Request) -> None:
+        self.pool.free(r.blocks)
+        r.blocks = []
+        r.num_computed = 0
+        r.state = "waiting"
+        r.preemptions += 1
+        self.running.remove(r)
+        self.waiting.appendleft(r)
+        self.n_preemptions += 1
+
+    def _try_alloc(self, n: int):
+        try:
+            return self.pool.alloc(n)
+        except OutOfBlocks:
+            return None
+
+    def step(self) -> Optional[StepMeta]:
+        budget = self.budget
+        scheduled = []
+        # running requests first, in admission order
+        i = 0
+        while i < len(self.running) and budget > 0:
+            r = self.running[i]
+            q = min(r.length - r.num_computed, self.chunk, budget)
+            need = cdiv(r.num_computed + q, self.bs) - len(r.blocks)
+            got = [] if need <= 0 else self._try_alloc(need)
+            preempted_self = False
+            while got is None:
+                victim = self.running[-1]
+                self._preempt(victim)
+                if victim is r:
+                    preempted_self = True
+                    break
+                got = self._try_alloc(need)
+            if preempted_self:
+                continue
+            r.blocks.extend(got)
+            scheduled.append((r, q))
+            budget -= q
+            i += 1
+        # admit waiting requests, first come first served
+        while self.waiting and len(self.running) < self.max_batch and budget > 0:
+            r = self.waiting[0]
+            got = self._try_alloc(cdiv(r.length, self.bs))
+            if got is None:
+                break
+            self.waiting.popleft()
+            r.blocks = got
+            r.state = "running"
+            self.running.append(r)
+            q = min(r.length, self.chunk, budget)
+            scheduled.append((r, q))
+            budget -= q
+        self.sum_running += len(self.running)
+        meta = self._emit(scheduled) if scheduled else None
+        # the iteration ran: advance, emit a token where the context caught up, retire
+        for r, q in scheduled:
+            r.num_computed += q
+            if r.num_computed == r.length:
+                r.generated += 1
+                if (r.generated >= r.eos_after or r.generated >= r.max_tokens
+                        or r.length >= self.max_model_len):
+                    self.pool.free(r.blocks)
+                    r.blocks = []
+                    r.state = "finished"
+                    r.finish_step = self.step_no
+                    self.running.remove(r)
+                    self.finished.append(r)
+        self.step_no += 1
+        return meta
+
+    def _emit(self, scheduled) -> StepMeta:
+        order = [x for x in scheduled if x[1] > 1] + [x for x in scheduled if x[1] == 1]
+        S = len(order)
+        q_lens = np.array([q for _, q in order], dtype=np.int32)
+        cu = np.zeros(S + 1, dtype=np.int32)
+        cu[1:] = np.cumsum(q_lens)
+        tables = np.full((S, self.max_blocks), -1, dtype=np.int32)
+        ctx = np.zeros(S, dtype=np.int32)
+        T = int(cu[-1])
+        slots = np.zeros(T, dtype=np.int64)
+        trid = np.zeros(T, dtype=np.int64)
+        tpos = np.zeros(T, dtype=np.int32)
+        for s, (r, q) in enumerate(order):
+            ctx[s] = r.num_computed + q
+            tables[s, : len(r.blocks)] = r.blocks
+            for j in range(q):
+                pos = r.num_computed + j
+                t = cu[s] + j
+                slots[t] = r.blocks[pos // self.bs] * self.bs + pos % self.bs
+                trid[t] = r.rid
+                tpos[t] = pos
+        return StepMeta(seq_rids=np.array([r.rid for r, _ in order], dtype=np.int64), q_lens=q_lens,
+                        context_lens=ctx, cu_seqlens=cu, block_tables=tables, slot_mapping=slots,
+                        token_rids=trid, token_pos=tpos,
+                        num_prefill=sum(1 for _, q in order if q > 1))
+
+    def idle(self) -> bool:
+        return not self.running and not self.waiting
+
+    def stats(self) -> dict:
+        return {
+            "steps": self.step_no,
+            "free_blocks": self.pool.free_count(),
+            "running": len(self.running),
+            "waiting": len(self.waiting),
+            "finished": len(self.finished),
+            "preemptions": self.n_preemptions,
+            "sum_running": self.sum_running,
+        }

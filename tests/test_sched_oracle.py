@@ -1,0 +1,164 @@
+"""The Python scheduler restatement against hand-worked traces and invariants."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle.sched import Scheduler
+import sched_golden
+
+
+def replay(sched, path):
+    config, requests, steps = sched_golden.load(path)
+    for r in requests:
+        sched.add(r["rid"], r["prompt"], r["max_tokens"], r["eos_after"])
+    for n in sorted(steps):
+        exp = steps[n]
+        meta = sched.step()
+        if exp["none"]:
+            assert meta is None, "step %d: expected nothing scheduled" % n
+        else:
+            assert meta is not None, "step %d: nothing scheduled" % n
+            assert len(meta.seq_rids) == len(exp["seqs"]), "step %d" % n
+            for s, e in enumerate(exp["seqs"]):
+                assert meta.seq_rids[s] == e["rid"], "step %d seq %d rid" % (n, s)
+                assert meta.q_lens[s] == e["q"], "step %d seq %d q" % (n, s)
+                assert meta.context_lens[s] == e["ctx"], "step %d seq %d ctx" % (n, s)
+                row = meta.block_tables[s]
+                assert row[: len(e["table"])].tolist() == e["table"], "step %d seq %d table" % (n, s)
+                assert np.all(row[len(e["table"]):] == -1)
+                got = meta.slot_mapping[meta.cu_seqlens[s]: meta.cu_seqlens[s + 1]].tolist()
+                assert got == e["slots"], "step %d seq %d slots" % (n, s)
+        st = sched.stats()
+        for k, v in exp["after"].items():
+            key = {"free": "free_blocks"}.get(k, k)
+            assert st[key] == v, "step %d after: %s = %d, expected %d" % (n, k, st[key], v)
+
+
+@pytest.mark.parametrize("path", sched_golden.all_traces(), ids=os.path.basename)
+def test_python_scheduler_reproduces_hand_worked_trace(path):
+    config, _, _ = sched_golden.load(path)
+    sched = Scheduler(config["num_blocks"], config["block_size"], config["max_batch"], config["budget"],
+                      config["chunk"], config["max_model_len"])
+    replay(sched, path)
+
+
+def random_trace(seed, n=60, NB=64, max_batch=8, budget=96, chunk=32, mml=256):
+    rng = np.random.default_rng(seed)
+    sched = Scheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=rng.permutation(NB))
+    arrivals = []
+    for rid in range(n):
+        arrivals.append((int(rng.integers(0, 40)), rid, int(rng.integers(1, 120)),
+                         int(rng.integers(1, 80)), int(rng.geometric(1 / 20))))
+    arrivals.sort()
+    return sched, arrivals
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_invariants_hold_on_random_traces(seed):
+    """free + owned == pool; no block owned twice; a scheduled sequence owns
+    ceil(ctx/16) or more blocks and at most ceil(known_tokens/16); waste in the
+    last block <= 15 tokens; the pool is whole again when idle."""
+    sched, arrivals = random_trace(seed)
+    NB = sched.pool.num_blocks
+    i = 0
+    for step in range(3000):
+        while i < len(arrivals) and arrivals[i][0] <= step:
+            _, rid, p, mt, eos = arrivals[i]
+            sched.add(rid, p, mt, eos)
+            i += 1
+        meta = sched.step()
+        owned = [b for r in sched.running for b in r.blocks]
+        assert len(owned) == len(set(owned))
+        assert len(owned) + sched.pool.free_count() == NB
+        assert not set(owned) & set(sched.pool.free_list)
+        for r in sched.running:
+            known = r.num_computed
+            assert len(r.blocks) * 16 - known <= 15 + 16 * (-(-(r.length - known) // 16)) + 15
+        if meta is not None:
+            for s in range(len(meta.seq_rids)):
+                ctx = int(meta.context_lens[s])
+                nb = int((meta.block_tables[s] >= 0).sum())
+                assert nb >= -(-ctx // 16)
+                assert meta.q_lens[s] >= 1
+        if i == len(arrivals) and sched.idle():
+            break
+    assert sched.idle()
+    assert sched.pool.free_count() == NB
+    assert len(sched.finished) == len(arrivals)
+    for r in sched.finished:
+        assert r.generated == min(r.eos_after, r.max_tokens, sched.max_model_len - r.prompt_len)
+
+
+def test_waste_per_decoding_sequence_is_at_most_block_size_minus_one():
+    """"Project 17" states at most 12 tokens of waste per sequence with 16-token
+    pages; the bound that holds is block_size - 1 = 15."""
+    sched = Scheduler(256, 16, 16, 4096, 4096, 1024)
+    for rid in range(16):
+        sched.add(rid, 1 + 7 * rid, 500, 10 + 13 * rid)
+    worst = 0
+    while not sched.idle():
+        sched.step()
+        for r in sched.running:
+            if r.num_computed == r.length - 1:      # decode phase: cache holds all but the newest token
+                waste = len(r.blocks) * 16 - r.num_computed
+                assert 0 <= waste <= 15
+                worst = max(worst, waste)
+    assert worst == 15
+
+
+def test_generates_exactly_max_tokens():
+    """Basic generation (cf. "Build a pure-Python ... engine", Running and Testing)."""
+    sched = Scheduler(64, 16, 2, 8192, 512, 8192)
+    sched.add(7, 11, 16, 10**6)
+    while not sched.idle():
+        sched.step()
+    assert sched.finished[0].generated == 16
+
+
+def test_tiny_pool_keeps_requests_pending():
+    """A 2-block pool cannot admit 3-block prompts: they stay pending, and the
+    pool is untouched (no leak)."""
+    sched = Scheduler(2, 16, 4, 8192, 512, 8192)
+    for rid in range(10):
+        sched.add(rid, 40, 128, 128)
+    for _ in range(5):
+        assert sched.step() is None
+    st = sched.stats()
+    assert st["waiting"] == 10 and st["running"] == 0 and st["free_blocks"] == 2
+
+
+def test_short_requests_complete_beside_a_long_one():
+    """With a 4-block pool, a long request and several short ones: the short
+    ones complete (preemption by recompute lets them through)."""
+    sched = Scheduler(4, 16, 4, 8192, 512, 64)
+    sched.add(0, 20, 1000, 1000)
+    for rid in range(1, 6):
+        sched.add(rid, 5, 4, 4)
+    for _ in range(400):
+        sched.step()
+        if sched.idle():
+            break
+    done = {r.rid for r in sched.finished}
+    assert {1, 2, 3, 4, 5} <= done
+    assert sched.idle() and sched.pool.free_count() == 4
+
+
+def test_injected_alloc_failure_preempts_lifo_and_recompute_reaches_same_state():
+    sched = Scheduler(64, 16, 4, 8192, 512, 8192)
+    for rid in range(3):
+        sched.add(rid, 16, 40, 40)
+    sched.step()                     # all three admitted (3 alloc calls)
+    sched.pool.fail_at = sched.pool.alloc_calls + 1    # the next growth alloc fails
+    meta = sched.step()
+    assert sched.n_preemptions == 1
+    # the newest request (rid 2) was the victim; blocks were free again for its
+    # re-admission in the same step, as a recompute prefill of prompt + 1 token
+    victim = [r for r in sched.running if r.rid == 2][0]
+    assert victim.preemptions == 1
+    assert meta.seq_rids.tolist() == [2, 0, 1]
+    assert meta.q_lens.tolist() == [17, 1, 1]
+    while not sched.idle():
+        sched.step()
+    assert [r.generated for r in sorted(sched.finished, key=lambda r: r.rid)] == [40, 40, 40]
+    assert sched.pool.free_count() == 64
