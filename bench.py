@@ -1,0 +1,366 @@
+"""Benchmark: one engine step of paged decode attention on the Llama-3-8B-shaped
+workload (256 sequences, 32 query / 8 KV heads, head_dim 128, 16-token blocks,
+lognormal contexts with median 1024 clipped to 32..8192, bf16, 64k-block pool).
+
+A step = append of the 256 new tokens' K/V by slot mapping, then paged decode
+attention over every sequence's whole context (split-KV kernel + merge).
+Prints ONE JSON line (rank 0).  `--impl reference` times the FP64 CPU oracle
+on a bounded sample of the same workload instead.
+
+Metric: algorithmic bytes of the step / step time, where the bytes are every
+attended token's K and V once per KV head, Q in, O out, the block-table
+entries in use, the context lengths, plus the append's reads and writes.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention KV GB/s (% of ~8 TB/s HBM) and attended tokens/s"
+WORKLOAD = "llama8b-decode"
+
+
+def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
+    ctx = np.asarray(ctx, np.int64)
+    S = ctx.shape[0]
+    kv = int(ctx.sum()) * 2 * Hkv * d * esize
+    return kv + S * Hq * d * esize * 2 + int(((ctx + bs - 1) // bs).sum()) * 4 + 4 * S
+
+
+def append_bytes(T, Hkv, d, esize=2):
+    # read k, v and slot; write the cache rows
+    return T * (2 * Hkv * d * esize * 2 + 8)
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, ws):
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def to_dev_bits(a, dtype):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16))
+    return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).cuda()
+
+
+def cpu_oracle_sample(st, budget_s):
+    """Time the oracle on the first k sequences of the step, k sized to ~budget_s."""
+    import oracle
+    q, bt, cl = st.q, st.block_tables, st.context_lens
+    kc, vc = st.k_cache, st.v_cache
+    # calibrate on one short sequence
+    order = list(range(st.S))
+    t0 = time.perf_counter()
+    oracle.decode(q[:1], kc, vc, bt[:1], cl[:1], st.dtype)
+    per_tok = (time.perf_counter() - t0) / max(1, int(cl[0]))
+    k, acc = 0, 0.0
+    while k < st.S and acc + per_tok * int(cl[k]) <= budget_s:
+        acc += per_tok * int(cl[k])
+        k += 1
+    k = max(k, 1)
+    t0 = time.perf_counter()
+    oracle.decode(q[:k], kc, vc, bt[:k], cl[:k], st.dtype)
+    dt = time.perf_counter() - t0
+    nbytes = decode_bytes(cl[:k], st.Hq, st.Hkv, st.d)
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d sequences of the step (%d attended tokens), decode only, %.1f s"
+                      % (k, st.S, int(cl[:k].sum()), dt),
+            "seconds": dt, "tokens_per_s": float(cl[:k].sum()) / dt}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup(args)
+    if rank != 0:
+        return
+    from synth import make_step
+    st = make_step("llama8b")
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_oracle_sample(st, args.ref_budget)
+        if i >= args.warmup:
+            vals.append(r)
+    v = statistics.median([r["value"] for r in vals])
+    ms = statistics.median([r["seconds"] for r in vals]) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "seqs": st.S, "q_heads": st.Hq, "kv_heads": st.Hkv, "head_dim": st.d,
+                       "block_size": st.bs, "sample": vals[-1]["sample"]},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": vals[-1]["sample"]},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_e2e(args, ws, st, q, kn, vn, slots, bt, cl, out, kc, vc, work, status, stream, scale, step_bytes, K):
+    """Same step through the public API with inputs in pinned host memory:
+    every step copies its inputs host->device and its output device->host."""
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_kn, h_vn = pin(q), pin(kn), pin(vn)
+    h_slots, h_bt, h_cl = pin(slots), pin(bt), pin(cl)
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+    d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_bt, h_cl))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        for dst, src in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_slots, h_slots), (d_bt, h_bt), (d_cl, h_cl)):
+            dst.copy_(src, non_blocking=True)
+        pkv.kv_append(d_kn, d_vn, d_slots, kc, vc, dev_status=status, stream=stream)
+        pkv.paged_decode_attention(out, d_q, kc, vc, d_bt, d_cl, scale=scale, workspace=work, dev_status=status,
+                                   stream=stream)
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / K
+    e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
+    return e2e_value, e2e_ms, h2d, d2h
+
+
+
+def run_pkv(args):
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    from synth import SEEDS, make_step
+
+    ws, rank, local = dist_setup(args)
+    dev_index = local if ws > 1 else 0
+    # weak scaling: each rank runs its own 256-sequence step (its own seed)
+    over = {}
+    if args.seqs:
+        over["S"] = args.seqs
+    if args.pool:
+        over["NB"] = args.pool
+    st = make_step("llama8b", seed=SEEDS["llama8b"] + rank, **over)
+    S, Hq, Hkv, d = st.S, st.Hq, st.Hkv, st.d
+    q = to_dev_bits(st.q, st.dtype)
+    kn, vn = to_dev_bits(st.k_new, st.dtype), to_dev_bits(st.v_new, st.dtype)
+    kc, vc = to_dev_bits(st.k_cache, st.dtype), to_dev_bits(st.v_cache, st.dtype)
+    slots = torch.from_numpy(st.slot_mapping).cuda()
+    bt = torch.from_numpy(st.block_tables).cuda()
+    cl = torch.from_numpy(st.context_lens).cuda()
+    out = torch.empty((S, Hq, d), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = pkv.decode_workspace_size(S, Hq, Hkv, d)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(d)
+
+    def step():
+        pkv.kv_append(kn, vn, slots, kc, vc, dev_status=status, stream=stream)
+        pkv.paged_decode_attention(out, q, kc, vc, bt, cl, scale=scale, workspace=work, dev_status=status,
+                                   stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(ws)
+    with ClockSampler(dev_index) as clk:
+        torch.cuda.synchronize()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            pkv.kv_append(kn, vn, slots, kc, vc, dev_status=status, stream=stream)
+            ev[k][1].record(stream)
+            pkv.paged_decode_attention(out, q, kc, vc, bt, cl, scale=scale, workspace=work, dev_status=status,
+                                       stream=stream)
+            ev[k][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws)
+    ms_step = total_ms / K
+    dec_ms = statistics.mean(ev[k][1].elapsed_time(ev[k][2]) for k in range(K))
+    app_ms = statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for k in range(K))
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d during the benchmark" % int(status.item()))
+
+    dbytes = decode_bytes(st.context_lens, Hq, Hkv, d)
+    abytes = append_bytes(st.T, Hkv, d)
+    step_bytes = dbytes + abytes
+    value = step_bytes * ws / (ms_step * 1e-3) / 1e9
+    attended = float(st.context_lens.sum())
+
+    # ---- end to end through the public API with host buffers ----
+    if args.no_e2e:
+        e2e_value, e2e_ms, h2d, d2h = None, None, 0, 0
+    else:
+        e2e_value, e2e_ms, h2d, d2h = run_e2e(args, ws, st, q, kn, vn, slots, bt, cl, out, kc, vc, work, status,
+                                              stream, scale, step_bytes, K)
+    if rank != 0:
+        return
+    peak, peak_kind = load_peaks()
+    achieved = dbytes / (dec_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "seqs_per_gpu": S, "q_heads": Hq, "kv_heads": Hkv, "head_dim": d,
+                   "block_size": st.bs, "pool_blocks": st.NB, "mean_context": round(float(st.context_lens.mean()), 1),
+                   "step": "kv_append(256 tokens) + paged_decode_attention", "l2": "inputs larger than L2 "
+                   "(%.2f GB of KV per step vs 129 MB L2), no flush" % (dbytes / 1e9), "parallelism": "dp%d" % ws},
+        "attended_tokens_per_s": round(attended * ws / (ms_step * 1e-3), 1),
+        "pct_of_8tbs": round(100 * value / 8000.0, 2),
+        "kernels_ms": {"kv_append": round(app_ms, 4), "paged_decode_attention": round(dec_ms, 4)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_kind,
+                     "kernel": "paged_decode_attention (split-KV + merge), bytes %d per launch" % dbytes},
+        "e2e": None if e2e_value is None else {
+            "value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and ws == 1:
+        cb = cpu_oracle_sample(st, args.cpu_budget)
+        cb.pop("seconds")
+        cb.pop("tokens_per_s")
+        line["cpu_baseline"] = cb
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--seqs", type=int, default=0, help="override the sequence count (profiling cases)")
+    ap.add_argument("--pool", type=int, default=0, help="override the pool size in blocks (profiling cases)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # each reference step is a bounded oracle sample; keep the whole run to a few minutes
+        args.ref_budget = min(args.ref_budget, 150.0 / (args.steps + args.warmup))
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,291 @@
+/*
+ * pkv.h -- C ABI of libpkv.so: attention for one continuous-batching engine
+ * step over a paged KV cache, on one GB300 (sm_103a), plus the host-side block
+ * pool and iteration-level scheduler that build the step's metadata.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Plain C types only.  Device pointers are owned by the caller (this
+ *   library never allocates or frees device memory on these paths); host
+ *   pointers are owned by whoever the function says.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   Every device entry point only enqueues work on that stream and returns;
+ *   results are ready when the stream reaches that point.
+ * - Return value: PKV_OK (0) or a negative PKV_ERR_* code.  Arguments are
+ *   validated on the host before any launch; on an error nothing is enqueued.
+ *   PKV_ERR_CUDA means a CUDA call failed; pkv_last_cuda_error() names it.
+ * - Contents of index arrays (block ids, context lengths, slots) are the
+ *   caller's contract.  The kernels still never read or write outside the
+ *   buffers whose sizes they are given: an out-of-range block id reads zeros
+ *   and sets PKV_DEV_BAD_BLOCK_ID in *dev_status, a context length beyond the
+ *   table is clamped and sets PKV_DEV_BAD_CONTEXT, an out-of-range slot is
+ *   skipped and sets PKV_DEV_BAD_SLOT.  dev_status (device int, may be NULL)
+ *   is OR-ed, never cleared, by the library.  Nothing traps.
+ * - Dtypes: PKV_DTYPE_F16 or PKV_DTYPE_BF16 for Q/K/V; outputs may also be
+ *   PKV_DTYPE_F32.  Accumulation and softmax are fp32; a 16-bit output is
+ *   rounded once, to nearest even, at the final store.
+ *
+ * Cache layout (both k_cache and v_cache): [num_blocks][num_kv_heads]
+ * [block_size][head_dim], row-major, 16-byte aligned.  One (block, KV head)
+ * tile is a contiguous block_size x head_dim run.  Physical block b of a
+ * sequence holds its logical tokens 16*j .. 16*j+15 where block_tables row
+ * entry j == b ("Project 17: Production Serving: Continuous Batching and
+ * PagedAttention", section "PagedAttention, the thing you build for memory":
+ * fixed-size pages, a per-sequence page table from logical to physical page).
+ * Entries past ceil(context_len / block_size) are never read and may hold -1
+ * (tiny-vllm part 7, "Termination and returning blocks": -1 = unassigned).
+ *
+ * Supported instantiations: head_dim 64 or 128, block_size 16, grouped-query
+ * ratio num_q_heads / num_kv_heads between 1 and 16.  Query head h reads KV
+ * head h / (num_q_heads / num_kv_heads).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------- */
+#define PKV_OK 0
+#define PKV_ERR_INVALID_ARG (-1)   /* null/misaligned pointer, inconsistent sizes */
+#define PKV_ERR_UNSUPPORTED (-2)   /* dtype, head_dim, block_size or group size not built */
+#define PKV_ERR_WORKSPACE (-3)     /* workspace too small or misaligned */
+#define PKV_ERR_CUDA (-4)          /* a CUDA runtime/driver call failed */
+#define PKV_ERR_OUT_OF_BLOCKS (-5) /* block pool exhausted (host allocator) */
+#define PKV_ERR_NO_DEVICE (-6)     /* no CUDA device is current / visible */
+
+/* ---- dtypes ---------------------------------------------------------------- */
+#define PKV_DTYPE_F16 0
+#define PKV_DTYPE_BF16 1
+#define PKV_DTYPE_F32 2
+
+/* ---- device status bits (OR-ed into *dev_status) ---------------------------- */
+#define PKV_DEV_BAD_BLOCK_ID 1  /* a block-table entry in use was outside [0, num_blocks) */
+#define PKV_DEV_BAD_CONTEXT 2   /* a context length < 0 or > max_blocks_per_seq*block_size */
+#define PKV_DEV_WAIT_TIMEOUT 4  /* a bounded wait for a tile gave up; outputs are invalid */
+#define PKV_DEV_BAD_SLOT 8      /* a slot_mapping entry pointed outside the pool */
+#define PKV_DEV_BAD_CHUNK 16    /* a prefill chunk had q_len > context_len or q_len < 0 */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *pkv_status_string(int status);
+
+/* Name of the last CUDA error seen by this thread inside the library
+ * ("no error" if none).  Static/thread-local string, never NULL. */
+const char *pkv_last_cuda_error(void);
+
+/* Library version string, e.g. "pkv 0.1 sm_103a". */
+const char *pkv_version(void);
+
+/*
+ * pkv_kv_append -- write this step's new keys and values into the paged cache.
+ *
+ * Defined by "Project 17", Step 4 "Implement the paged KV cache" (append
+ * stores a token's K and V at (page, slot in page)), with the slot of each new
+ * token given by slot_mapping, part of the per-step metadata of "Continuous
+ * Batching" (infra.pidoku.co.in) §6 "Under the hood"; it runs before
+ * attention (tiny-vllm part 7, "Uploading the active arrays to the GPU").
+ *
+ *   k, v           device, [num_tokens][num_kv_heads][head_dim], dtype, 16-B aligned
+ *   slot_mapping   device int64 [num_tokens]; slot = block * block_size + offset;
+ *                  a negative slot means "padding, write nothing"
+ *   k_cache, v_cache  device caches (layout above), modified in place
+ * For every token t with slot_mapping[t] >= 0 and every KV head h, the bytes
+ * of k[t][h][:] and v[t][h][:] are copied unchanged to
+ * cache[slot / block_size][h][slot % block_size][:].  Bit-exact.  Slots must be
+ * unique within one call (duplicates leave one of the writers' rows).
+ * num_tokens == 0 is a no-op.
+ */
+int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int num_tokens,
+                  void *k_cache, void *v_cache, int num_blocks, int block_size, int num_kv_heads,
+                  int head_dim, int dtype, int *dev_status, void *stream);
+
+/*
+ * Bytes of device workspace pkv_paged_decode_attention needs on the current
+ * device for these head counts and head_dim (independent of the contexts).
+ * Returns 0 if no device is current.
+ */
+size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
+
+/*
+ * pkv_paged_decode_attention -- one query token per sequence attends its whole
+ * paged context.
+ *
+ * Defined by "Project 17", Step 6 "Implement attention over paged storage":
+ * walk the page table, score each stored key against the query scaled by
+ * 1/sqrt(head_dim), softmax over the sequence, weighted sum of the stored
+ * values -- taken per query head, with grouped KV heads.  For sequence s and
+ * query head h (g = h / (Hq/Hkv)):
+ *     out[s][h][:] = sum_{t < ctx_s} softmax_t(scale * q[s][h] . K_t) V_t,
+ *     K_t, V_t = cache[block_tables[s][t / 16]][g][t % 16][:]
+ * where ctx_s = context_lens[s] counts the token(s) appended this step
+ * (tiny-vllm part 7: K/V are written first, then attention reads length + 1).
+ * ctx_s == 0 gives an all-zero row.
+ *
+ *   out            device, [num_seqs][num_q_heads][head_dim], out_dtype (dtype or F32)
+ *   q              device, [num_seqs][num_q_heads][head_dim], dtype, 4-B aligned
+ *   k_cache, v_cache  device caches, 16-B aligned, num_blocks blocks
+ *   block_tables   device int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   device int32 [num_seqs]
+ *   scale          score scale (pass 1/sqrt(head_dim) for the standard one)
+ *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 16-B aligned;
+ *                  scratch for split-context partial results, contents on entry
+ *                  ignored.  Owned by the caller; must not be used by another
+ *                  call that may run concurrently.
+ *   dev_status     device int or NULL (see conventions)
+ * The KV range of every (sequence, KV head) pair is split across warps so
+ * every SM gets the same number of blocks; split ranges are combined by a
+ * log-sum-exp merge in a second small kernel on the same stream.
+ */
+int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                               const int32_t *block_tables, int max_blocks_per_seq,
+                               const int32_t *context_lens, int num_seqs, int num_blocks,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               float scale, int dtype, int out_dtype, void *workspace,
+                               size_t workspace_bytes, int *dev_status, void *stream);
+
+/*
+ * pkv_paged_prefill_attention -- chunked prefill: a chunk of new query tokens
+ * per sequence attends the sequence's prior context plus the chunk, causally.
+ *
+ * Defined by "Continuous Batching" §5 "Mixed batching (prefill + decode in one
+ * step)": prompts are split into chunks that ride with the decode step, and
+ * variable-length kernels take the ragged shape through cu_seqlens (§6).  For
+ * chunk c with q_len = cu_seqlens[c+1] - cu_seqlens[c] and ctx = context_lens[c]
+ * (which counts the chunk), query row i sits at position p = ctx - q_len + i and
+ *     out[cu[c]+i][h][:] = sum_{t <= p} softmax_t(scale * q[cu[c]+i][h] . K_t) V_t
+ * with K_t, V_t gathered through block_tables[c] as in decode.
+ *
+ *   out, q         device, [total_q][num_q_heads][head_dim]
+ *   cu_seqlens     device int32 [num_seqs + 1], cu[0] = 0, non-decreasing
+ *   max_q_len      host int, >= every chunk's q_len (sizes the grid)
+ *   total_q        host int, == cu_seqlens[num_seqs]
+ *   other arguments as in decode.  No workspace is needed.
+ * A chunk with q_len > ctx is skipped and sets PKV_DEV_BAD_CHUNK.
+ */
+int pkv_paged_prefill_attention(void *out, const void *q, const int32_t *cu_seqlens, int num_seqs,
+                                int max_q_len, int total_q, const void *k_cache,
+                                const void *v_cache, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens,
+                                int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, float scale, int dtype, int out_dtype,
+                                int *dev_status, void *stream);
+
+/* ---- host block pool ----------------------------------------------------------
+ * A preallocated set of physical block ids with a free list used as a stack
+ * ("Project 17", Step 4: BlockPool.alloc pops from the end of the free list,
+ * free appends; "Build a pure-Python continuous batching LLM serving engine",
+ * Step 2: the free list is a stack).  Pure host code, no GPU needed.
+ */
+typedef struct pkv_pool pkv_pool;
+
+/* initial_order: NULL for [0, 1, ..., num_blocks-1] (so block num_blocks-1 is
+ * popped first), or a permutation of [0, num_blocks) to start from (copied).
+ * Returns NULL on invalid arguments or allocation failure. */
+pkv_pool *pkv_pool_create(int num_blocks, const int32_t *initial_order);
+void pkv_pool_destroy(pkv_pool *pool);
+/* All-or-nothing: pops n ids into out_ids (host array of >= n) in pop order,
+ * or returns PKV_ERR_OUT_OF_BLOCKS and changes nothing ("Project 17" Step 4
+ * raises OutOfPagesError; "Continuous Batching" §4 returns an error). */
+int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *out_ids);
+/* Pushes ids back in the given order.  PKV_ERR_INVALID_ARG if an id is out of
+ * range or already free (nothing is changed then). */
+int pkv_pool_free(pkv_pool *pool, const int32_t *ids, int n);
+int pkv_pool_free_count(const pkv_pool *pool);
+/* Copies the free list (bottom to top) into out (host, >= free_count ints). */
+int pkv_pool_free_list(const pkv_pool *pool, int32_t *out);
+/* Fault injection for tests: the nth alloc call from now (1 = the next one)
+ * fails with PKV_ERR_OUT_OF_BLOCKS; 0 disarms. */
+int pkv_pool_inject_failure(pkv_pool *pool, int64_t nth);
+
+/* ---- host iteration-level scheduler --------------------------------------------
+ * Builds each step's metadata for the kernels above and nothing else:
+ * retire -> run the running requests -> admit, once per engine step
+ * ("Project 17" Step 2, "Continuous Batching" §4 Engine.Step):
+ *   - running requests are scheduled first, in admission order: a decode gets
+ *     1 token, a request still prefilling gets min(remaining, chunk) tokens,
+ *     all within max_num_batched_tokens per step (§5 "Mixed batching");
+ *   - before a request runs, it gets blocks for all tokens it will hold after
+ *     this step; if the pool is empty, the most recently admitted running
+ *     request is preempted (blocks freed, moved to the FRONT of the waiting
+ *     queue, recomputed later from prompt + generated tokens), repeatedly; if
+ *     that is the request itself it is preempted (§4 preempt, §5 Preemption,
+ *     "Victim selection": LIFO);
+ *   - waiting requests are admitted first-come-first-served while the batch
+ *     has room, the budget is not spent and blocks for all their known tokens
+ *     can be allocated; admission stops at the first that does not fit (§4);
+ *   - after the iteration, a request whose cache caught up emits one token;
+ *     it retires on its pre-drawn EOS step, on max_tokens or when its length
+ *     reaches max_model_len, and its blocks are freed at once (§1 lifecycle,
+ *     tiny-vllm part 7 "Termination and returning blocks").
+ * Emitted sequences: prefill chunks (q_len > 1) first, then decodes
+ * (q_len == 1), each group in scheduling order.  Pure host code.
+ */
+typedef struct pkv_sched pkv_sched;
+
+typedef struct pkv_sched_config {
+    int num_blocks;             /* physical blocks in the pool */
+    int block_size;             /* tokens per block (16) */
+    int max_batch;              /* max running requests */
+    int max_num_batched_tokens; /* token budget per step */
+    int chunk;                  /* max prefill tokens per request per step */
+    int max_model_len;          /* max prompt + generated tokens */
+    const int32_t *initial_order; /* NULL or a permutation of [0, num_blocks) (copied) */
+} pkv_sched_config;
+
+/* Arrays are owned by the scheduler and valid until the next pkv_sched_step
+ * or pkv_sched_destroy on the same scheduler. */
+typedef struct pkv_step_meta {
+    int num_seqs;       /* sequences scheduled this step */
+    int num_prefill;    /* the first num_prefill sequences are prefill chunks */
+    int num_tokens;     /* new tokens this step (sum of q_lens) */
+    int max_blocks;     /* row length of block_tables = ceil(max_model_len / block_size) */
+    const int64_t *seq_rids;      /* [num_seqs] request ids */
+    const int32_t *q_lens;        /* [num_seqs] new tokens per sequence */
+    const int32_t *context_lens;  /* [num_seqs] tokens attended, including the new ones */
+    const int32_t *cu_seqlens;    /* [num_seqs + 1] prefix sums of q_lens */
+    const int32_t *block_tables;  /* [num_seqs][max_blocks], -1 padded */
+    const int64_t *slot_mapping;  /* [num_tokens] cache slot of every new token */
+    const int64_t *token_rids;    /* [num_tokens] request id of every new token */
+    const int32_t *token_pos;     /* [num_tokens] position of every new token in its request */
+} pkv_step_meta;
+
+typedef struct pkv_sched_stats {
+    int64_t steps;          /* pkv_sched_step calls */
+    int64_t preemptions;    /* preemption events */
+    int64_t admitted;       /* admissions (a recomputed request counts again) */
+    int64_t finished;       /* retired requests */
+    int64_t sum_running;    /* sum over steps of running requests (average batch) */
+    int64_t tokens;         /* scheduled tokens, all steps */
+    int64_t prefill_tokens; /* of which in prefill chunks */
+    int running;
+    int waiting;
+    int free_blocks;
+    double host_ms;         /* wall time spent inside pkv_sched_step */
+} pkv_sched_stats;
+
+pkv_sched *pkv_sched_create(const pkv_sched_config *config);
+void pkv_sched_destroy(pkv_sched *sched);
+/* Queue a request.  eos_after >= 1 is the output length at which it emits
+ * EOS.  PKV_ERR_INVALID_ARG for prompt_len < 1, prompt_len >= max_model_len,
+ * max_tokens < 1, eos_after < 1 or a duplicate rid.  A request needing more
+ * blocks than the pool holds is accepted but never admitted. */
+int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int max_tokens, int eos_after);
+/* One engine step.  Returns the number of scheduled sequences (0 = nothing to
+ * run; *out then has num_seqs = 0), or a negative status. */
+int pkv_sched_step(pkv_sched *sched, pkv_step_meta *out);
+int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out);
+/* Fault injection for tests: forwarded to the scheduler's pool. */
+int pkv_sched_inject_alloc_failure(pkv_sched *sched, int64_t nth);
+/* Request state: 0 waiting, 1 running, 2 finished, -1 unknown rid.
+ * generated (may be NULL) receives its output-token count. */
+int pkv_sched_request_state(const pkv_sched *sched, int64_t rid, int *generated);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,72 @@
+// K1: append this step's new K/V rows into the paged cache by slot mapping.
+//
+// "Project 17: Production Serving: Continuous Batching and PagedAttention",
+// Step 4 "Implement the paged KV cache": a token's key and value go to
+// (physical page, slot in page).  The slot of every new token comes from the
+// step's slot_mapping ("Continuous Batching" §6 "Under the hood").  A pure
+// bit copy: each thread moves one 16-byte vector of K and the matching vector
+// of V; a warp covers two (token, head) rows of head_dim 128, so reads and
+// writes are whole 256-byte rows.
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                                                        const int64_t *__restrict__ slot_mapping, int num_tokens,
+                                                        uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                                                        int num_blocks, int block_size, int num_kv_heads,
+                                                        int vec_per_row, int *dev_status) {
+    const int64_t items = (int64_t)num_tokens * num_kv_heads * vec_per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
+        const int64_t row = i / vec_per_row;           // (token, head)
+        const int vec = (int)(i - row * vec_per_row);
+        const int t = (int)(row / num_kv_heads);
+        const int h = (int)(row - (int64_t)t * num_kv_heads);
+        const int64_t slot = __ldg(slot_mapping + t);
+        if (slot < 0) continue;
+        const int64_t block = slot / block_size;
+        const int off = (int)(slot - block * block_size);
+        if (block >= num_blocks) {
+            if (vec == 0 && h == 0) set_status(dev_status, PKV_DEV_BAD_SLOT);
+            continue;
+        }
+        const int64_t dst = ((block * num_kv_heads + h) * block_size + off) * vec_per_row + vec;
+        k_cache[dst] = __ldg(k + i);
+        v_cache[dst] = __ldg(v + i);
+    }
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int num_tokens,
+                             void *k_cache, void *v_cache, int num_blocks, int block_size, int num_kv_heads,
+                             int head_dim, int dtype, int *dev_status, void *stream) {
+    using namespace pkv;
+    if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (block_size != 16 || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = current_sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    const int vec_per_row = head_dim * 2 / 16;
+    const int64_t items = (int64_t)num_tokens * num_kv_heads * vec_per_row;
+    const int threads = 256;
+    int64_t blocks = (items + threads - 1) / threads;
+    if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+    kv_append_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_blocks, block_size, num_kv_heads,
+        vec_per_row, dev_status);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}

@@ -1,0 +1,622 @@
+// K2 + K3: paged decode attention with a split KV range and a log-sum-exp merge.
+//
+// What is computed: "Project 17: Production Serving: Continuous Batching and
+// PagedAttention", Step 6 "Implement attention over paged storage" -- walk a
+// sequence's page table, score every stored key against the query scaled by
+// 1/sqrt(head_dim), softmax over the sequence, weighted sum of the stored
+// values -- per query head, with query head h reading KV head h / G.
+//
+// How (GB300):
+//  * Work = the flat list of (sequence, KV head, block) triples, cut into equal
+//    contiguous ranges, one per warp of a persistent grid (one CTA of 8 warps
+//    per SM).  Every warp streams the same number of 16-token blocks, whatever
+//    the context-length mix; a (sequence, head) range that crosses a warp
+//    boundary is finished by the merge kernel from per-warp partials (m, l, acc).
+//  * Each warp runs its own ring of STAGES shared-memory slots.  Lane 0 issues
+//    2-D TMA loads (128-byte swizzle) of the K and V tiles of a block -- the
+//    block id comes from the block table -- and the warp waits on the slot's
+//    mbarrier (bounded wait, error bit on timeout).
+//  * The GQA group is one MMA row tile: S = Q(16 padded heads x d) . K^T
+//    (d x 16 tokens) with mma.m16n8k16 (K fragments by ldmatrix from the
+//    swizzled tile), online softmax in fp32 with warp shuffles over the four
+//    lanes of a row, then O^T(d x heads) += V^T . P^T (V fragments by
+//    ldmatrix.trans).  P is fed to the MMA as a 16-bit pair (rounded value +
+//    rounding residual), so the weights keep ~16 significant bits.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a tile that has not landed in 2 s never will
+constexpr int kDecodeWarps = 8;
+
+struct DecodeParams {
+    void *out;
+    const void *q;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    float *part;        // [2 * total_warps][record] partial results
+    int *seq_start;     // [S + 1]: exclusive prefix sum of blocks per sequence
+    int *dev_status;
+    int S, max_blocks, num_blocks, Hq, Hkv, G;
+    float scale_log2;   // scale * log2(e): scores are kept in base-2 units
+    int out_dtype;
+    int total_warps;
+};
+
+template <int D, int NT>
+struct DecodeShape {
+    static constexpr int HALVES = D / 64;              // 64-element (128-byte) column halves
+    static constexpr int HALF_BYTES = 64 * 16 * 2;     // one 16-row half tile
+    static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
+    static constexpr int STAGES = D == 128 ? 3 : 6;
+    static constexpr int HP = 8 * NT;                   // heads held by a partial record
+    static constexpr int REC = 2 * HP + HP * D;         // m[HP], l[HP], acc[HP][D]
+    static constexpr int RING_BYTES = kDecodeWarps * STAGES * STAGE_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + kDecodeWarps * STAGES * 8 + 256;
+};
+
+__device__ __forceinline__ int blocks_of(const int32_t *context_lens, int s, int max_blocks, int *dev_status,
+                                         int *ctx_out) {
+    int c = __ldg(context_lens + s);
+    if (c < 0) {
+        set_status(dev_status, PKV_DEV_BAD_CONTEXT);
+        c = 0;
+    }
+    if (c > max_blocks * 16) {
+        set_status(dev_status, PKV_DEV_BAD_CONTEXT);
+        c = max_blocks * 16;
+    }
+    if (ctx_out) *ctx_out = c;
+    return (c + 15) >> 4;
+}
+
+// Inclusive block-wide scan of v over kDecodeWarps warps; *total gets the sum.
+__device__ __forceinline__ int64_t block_scan(int64_t v, int64_t *sh, int64_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int64_t n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    if (lane == 31) sh[warp] = v;
+    __syncthreads();
+    int64_t add = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+        int64_t x = sh[w];
+        if (w < warp) add += x;
+        tot += x;
+    }
+    __syncthreads();
+    *total = tot;
+    return v + add;
+}
+
+__device__ __forceinline__ int64_t range_lo(int64_t w, int64_t total, int64_t nw) { return w * total / nw; }
+
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
+    paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv) {
+    using Sh = DecodeShape<D, NT>;
+    constexpr int STAGES = Sh::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ring = smem;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sh::RING_BYTES);
+    int64_t *sh_scan = reinterpret_cast<int64_t *>(bars + kDecodeWarps * STAGES);
+    int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);
+    int *plan_off = plan_s + kDecodeWarps;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Hkv = p.Hkv;
+
+    // ---- plan: total blocks, this CTA's warp ranges, per-sequence offsets ----
+    int64_t local = 0;
+    for (int s = tid; s < p.S; s += blockDim.x) local += blocks_of(p.context_lens, s, p.max_blocks, p.dev_status, nullptr);
+    int64_t total_nblk;
+    block_scan(local, sh_scan, &total_nblk);
+    const int64_t total = total_nblk * Hkv;
+    const int64_t nw = p.total_warps;
+    if (tid < kDecodeWarps) plan_s[tid] = -1;
+    __syncthreads();
+    int64_t carry = 0;
+    for (int base = 0; base < p.S; base += blockDim.x) {
+        const int s = base + tid;
+        const int nb = s < p.S ? blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) : 0;
+        int64_t tile_total;
+        const int64_t excl = carry + block_scan(nb, sh_scan, &tile_total) - nb;
+        if (blockIdx.x == 0 && s < p.S) p.seq_start[s] = (int)excl;
+        if (nb > 0) {
+#pragma unroll
+            for (int w = 0; w < kDecodeWarps; ++w) {
+                const int64_t lo = range_lo((int64_t)blockIdx.x * kDecodeWarps + w, total, nw);
+                if (lo >= excl * Hkv && lo < (excl + nb) * Hkv) {
+                    plan_s[w] = s;
+                    plan_off[w] = (int)(lo - excl * Hkv);
+                }
+            }
+        }
+        carry += tile_total;
+    }
+    if (blockIdx.x == 0 && tid == 0) p.seq_start[p.S] = (int)total_nblk;
+    __syncthreads();
+
+    const int64_t wg = (int64_t)blockIdx.x * kDecodeWarps + warp;
+    const int n = (int)(range_lo(wg + 1, total, nw) - range_lo(wg, total, nw));
+    if (n <= 0 || plan_s[warp] < 0) return;
+
+    // ---- this warp's ring ----
+    uint8_t *wring = ring + warp * STAGES * Sh::STAGE_BYTES;
+    uint64_t *wbar = bars + warp * STAGES;
+    if (lane == 0) {
+        for (int st = 0; st < STAGES; ++st) mbar_init(&wbar[st], 1);
+        fence_mbar_init();
+        if (warp == 0) {
+            prefetch_tensormap(&tk);
+            prefetch_tensormap(&tv);
+        }
+    }
+    __syncwarp();
+    const uint64_t policy = l2_policy_evict_first();
+
+    // consumer and producer cursors over (sequence, head, block)
+    int cs = plan_s[warp], c_ctx;
+    int c_nb = blocks_of(p.context_lens, cs, p.max_blocks, nullptr, &c_ctx);
+    int ch = plan_off[warp] / c_nb, cj = plan_off[warp] % c_nb;
+    int ps = cs, p_nb = c_nb, ph = ch, pj = cj;
+    bool started_mid = cj != 0;
+
+    auto next_seq = [&](int s, int &nb_out, int *ctx_out) {
+        int nb;
+        do {
+            ++s;
+            nb = blocks_of(p.context_lens, s, p.max_blocks, nullptr, ctx_out);
+        } while (nb == 0);
+        nb_out = nb;
+        return s;
+    };
+    auto table_entry = [&]() { return __ldg(p.block_tables + (int64_t)ps * p.max_blocks + pj); };
+    auto advance_producer = [&]() {
+        if (++pj == p_nb) {
+            pj = 0;
+            if (++ph == Hkv) {
+                ph = 0;
+                ps = next_seq(ps, p_nb, nullptr);
+            }
+        }
+    };
+    auto issue = [&](int stage, int blk) {
+        if (lane == 0) {
+            int row = (blk * Hkv + ph) * 16;
+            if (blk < 0 || blk >= p.num_blocks) {
+                set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                row = p.num_blocks * Hkv * 16;   // past the end: the load fills zeros
+            }
+            uint64_t *bar = &wbar[stage];
+            mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES);
+            uint8_t *kdst = wring + stage * Sh::STAGE_BYTES;
+            uint8_t *vdst = kdst + Sh::TILE_BYTES;
+#pragma unroll
+            for (int hf = 0; hf < Sh::HALVES; ++hf) {
+                tma_load_2d(kdst + hf * Sh::HALF_BYTES, &tk, hf * 64, row, bar, policy);
+                tma_load_2d(vdst + hf * Sh::HALF_BYTES, &tv, hf * 64, row, bar, policy);
+            }
+        }
+    };
+
+    // prologue: fill the ring
+    int pending = table_entry();
+    const int pro = n < STAGES ? n : STAGES;
+    for (int k = 0; k < pro; ++k) {
+        issue(k, pending);
+        if (k + 1 < n) {
+            advance_producer();
+            pending = table_entry();
+        }
+    }
+
+    const int g = lane >> 2, t4 = lane & 3;
+    const int mi = lane >> 3;
+    const int ld_row = ((mi >> 1) << 3) + (lane & 7);          // token row this lane addresses
+    const int ld_sw = ld_row & 7;                               // 128-byte swizzle phase of that row
+    const uint32_t ring_addr = smem_addr(wring);
+
+    uint32_t qa[D / 16][4];
+    float acc[D / 16][NT][4];
+    float m_run[NT], l_run[NT];
+    bool seg_fresh = true;
+
+    const int G = p.G;
+    for (int i = 0; i < n; ++i) {
+        if (seg_fresh) {
+            // query fragments of (cs, ch): rows = heads of the group (padded to 16)
+            const uint32_t *qbase = reinterpret_cast<const uint32_t *>(
+                static_cast<const T *>(p.q) + ((int64_t)cs * p.Hq + (int64_t)ch * G) * D);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const int c0 = (kk * 16 + 2 * t4) >> 1;
+                qa[kk][0] = g < G ? __ldg(qbase + g * (D / 2) + c0) : 0u;
+                qa[kk][2] = g < G ? __ldg(qbase + g * (D / 2) + c0 + 4) : 0u;
+                qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0) : 0u;
+                qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0 + 4) : 0u;
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[mt][pn][e] = 0.f;
+#pragma unroll
+            for (int pn = 0; pn < NT; ++pn) {
+                m_run[pn] = -INFINITY;
+                l_run[pn] = 0.f;
+            }
+            seg_fresh = false;
+        }
+
+        const int stage = i % STAGES;
+        const bool landed = mbar_wait(&wbar[stage], (uint32_t)((i / STAGES) & 1), kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, landed)) {
+            set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+            // let the copies this warp still has in flight land before leaving
+            for (int k = i + 1; k < n && k < i + STAGES; ++k)
+                mbar_wait(&wbar[k % STAGES], (uint32_t)((k / STAGES) & 1), kWaitLimitNs / 8);
+            return;
+        }
+        const uint32_t kbase = ring_addr + stage * Sh::STAGE_BYTES;
+        const uint32_t vbase = kbase + Sh::TILE_BYTES;
+
+        // ---- S = Q K^T over the 16 tokens of this block ----
+        float sacc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int chunk = ((kk & 3) << 1) + (mi & 1);
+            const uint32_t addr = kbase + (kk >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
+            uint32_t b00, b01, b10, b11;
+            ldsm_x4(addr, b00, b01, b10, b11);
+            mma_16816<T>(sacc[0], qa[kk], b00, b01);
+            mma_16816<T>(sacc[1], qa[kk], b10, b11);
+        }
+
+        // ---- mask, online softmax (base 2) ----
+        const int lim = c_ctx - cj * 16;   // valid tokens in this block (>= 16: all)
+        float pr[2][4];
+        float alpha[NT];
+#pragma unroll
+        for (int pn = 0; pn < NT; ++pn) {
+            float x[2][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = nt * 8 + 2 * t4 + e;
+                    x[nt][e] = tok < lim ? sacc[nt][pn * 2 + e] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, x[nt][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run[pn], mx);
+            alpha[pn] = exp2_approx(m_run[pn] - m_new);
+            m_run[pn] = m_new;
+            float rs = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    pr[nt][pn * 2 + e] = exp2_approx(x[nt][e] - m_new);
+                    rs += pr[nt][pn * 2 + e];
+                }
+            l_run[pn] = l_run[pn] * alpha[pn] + rs;
+        }
+
+        // rows beyond the context may hold anything: zero them in V so that
+        // 0-weight x garbage cannot reach the accumulator
+        if (lim < 16) {
+            const int bad_rows = 16 - lim;
+            for (int idx = lane; idx < bad_rows * 8 * Sh::HALVES; idx += 32) {
+                const int hf = idx / (bad_rows * 8);
+                const int rem = idx - hf * bad_rows * 8;
+                const int row = lim + (rem >> 3);
+                uint4 *dst = reinterpret_cast<uint4 *>(wring + stage * Sh::STAGE_BYTES + Sh::TILE_BYTES +
+                                                       hf * Sh::HALF_BYTES + row * 128 + ((rem & 7) << 4));
+                *dst = make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // ---- rescale the accumulator, O^T += V^T P^T ----
+#pragma unroll
+        for (int pn = 0; pn < NT; ++pn) {
+            const float a_lo = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4);
+            const float a_hi = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4 + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                acc[mt][pn][0] *= a_lo;
+                acc[mt][pn][1] *= a_hi;
+                acc[mt][pn][2] *= a_lo;
+                acc[mt][pn][3] *= a_hi;
+            }
+        }
+        uint32_t pb0[NT][2], pb1[NT][2];
+#pragma unroll
+        for (int pn = 0; pn < NT; ++pn) {
+            pack2_split<T>(pr[0][pn * 2], pr[0][pn * 2 + 1], pb0[pn][0], pb0[pn][1]);
+            pack2_split<T>(pr[1][pn * 2], pr[1][pn * 2 + 1], pb1[pn][0], pb1[pn][1]);
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            const int chunk = ((mt & 3) << 1) + (mi & 1);
+            const uint32_t addr = vbase + (mt >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
+            uint32_t a[4];
+            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
+#pragma unroll
+            for (int pn = 0; pn < NT; ++pn) {
+                mma_16816<T>(acc[mt][pn], a, pb0[pn][0], pb1[pn][0]);
+                mma_16816<T>(acc[mt][pn], a, pb0[pn][1], pb1[pn][1]);
+            }
+        }
+
+        // release the slot to the TMA engine and refill it
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (i + STAGES < n) {
+            issue(stage, pending);
+            if (i + STAGES + 1 < n) {
+                advance_producer();
+                pending = table_entry();
+            }
+        }
+
+        // ---- end of a (sequence, head) range in this warp ----
+        const bool seg_done = cj == c_nb - 1;
+        if (seg_done || i == n - 1) {
+            float lsum[NT];
+#pragma unroll
+            for (int pn = 0; pn < NT; ++pn) {
+                lsum[pn] = l_run[pn];
+                lsum[pn] += __shfl_xor_sync(0xffffffffu, lsum[pn], 1);
+                lsum[pn] += __shfl_xor_sync(0xffffffffu, lsum[pn], 2);
+            }
+            const int head0 = ch * G;
+            if (!started_mid && seg_done) {
+                // whole range in this warp: normalise and store
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn) {
+                    const float inv_lo = 1.f / __shfl_sync(0xffffffffu, lsum[pn], 8 * t4);
+                    const float inv_hi = 1.f / __shfl_sync(0xffffffffu, lsum[pn], 8 * t4 + 4);
+                    const int ha = pn * 8 + 2 * t4, hb = ha + 1;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const int d0 = mt * 16 + g;
+                        if (ha < G) {
+                            const int64_t o = ((int64_t)cs * p.Hq + head0 + ha) * D;
+                            store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][0] * inv_lo);
+                            store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][2] * inv_lo);
+                        }
+                        if (hb < G) {
+                            const int64_t o = ((int64_t)cs * p.Hq + head0 + hb) * D;
+                            store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][1] * inv_hi);
+                            store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][3] * inv_hi);
+                        }
+                    }
+                }
+            } else {
+                // part of a range shared with other warps: leave (m, l, acc)
+                float *rec = p.part + (size_t)(wg * 2 + (started_mid ? 0 : 1)) * Sh::REC;
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn) {
+                    if (t4 == 0) {
+                        rec[pn * 8 + g] = m_run[pn];
+                        rec[Sh::HP + pn * 8 + g] = lsum[pn];
+                    }
+                    float *racc = rec + 2 * Sh::HP;
+                    const int ha = pn * 8 + 2 * t4, hb = ha + 1;
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        const int d0 = mt * 16 + g;
+                        racc[ha * D + d0] = acc[mt][pn][0];
+                        racc[hb * D + d0] = acc[mt][pn][1];
+                        racc[ha * D + d0 + 8] = acc[mt][pn][2];
+                        racc[hb * D + d0 + 8] = acc[mt][pn][3];
+                    }
+                }
+            }
+            started_mid = false;
+            seg_fresh = true;
+        }
+        // advance the consumer cursor
+        if (i + 1 < n) {
+            if (++cj == c_nb) {
+                cj = 0;
+                if (++ch == Hkv) {
+                    ch = 0;
+                    cs = next_seq(cs, c_nb, &c_ctx);
+                }
+            }
+        }
+    }
+}
+
+// Combines the partials of (sequence, KV head) ranges that crossed a warp
+// boundary, and writes zeros for sequences with an empty context.  One warp
+// per (sequence, KV head).
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
+    using Sh = DecodeShape<D, NT>;
+    const int lane = threadIdx.x & 31;
+    const int idx = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (idx >= p.S * p.Hkv) return;
+    const int s = idx / p.Hkv, h = idx - s * p.Hkv;
+    const int G = p.G;
+    const int nb = blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr);
+    constexpr int PER = D / 32;
+    if (nb == 0) {
+        for (int hh = 0; hh < G; ++hh) {
+            const int64_t o = ((int64_t)s * p.Hq + h * G + hh) * D;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) store_out<T>(p.out, p.out_dtype, o + lane + 32 * k, 0.f);
+        }
+        return;
+    }
+    const int64_t total = (int64_t)p.seq_start[p.S] * p.Hkv;
+    const int64_t nw = p.total_warps;
+    const int64_t seg_lo = (int64_t)p.seq_start[s] * p.Hkv + (int64_t)h * nb;
+    const int64_t seg_hi = seg_lo + nb - 1;
+    // warp holding flat position x: the largest w with range_lo(w) <= x
+    auto owner = [&](int64_t x) { return ((x + 1) * nw + total - 1) / total - 1; };
+    const int64_t w0 = owner(seg_lo), w1 = owner(seg_hi);
+    if (w0 == w1) return;   // finished by its warp
+    for (int hh = 0; hh < G; ++hh) {
+        float M = -INFINITY;
+        for (int64_t w = w0; w <= w1; ++w) {
+            if (range_lo(w + 1, total, nw) == range_lo(w, total, nw)) continue;   // warp with no blocks
+            const float *rec = p.part + (size_t)(w * 2 + (w == w0 ? 1 : 0)) * Sh::REC;
+            M = fmaxf(M, rec[hh]);
+        }
+        float L = 0.f;
+        float o[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) o[k] = 0.f;
+        for (int64_t w = w0; w <= w1; ++w) {
+            if (range_lo(w + 1, total, nw) == range_lo(w, total, nw)) continue;
+            const float *rec = p.part + (size_t)(w * 2 + (w == w0 ? 1 : 0)) * Sh::REC;
+            const float sc = exp2_approx(rec[hh] - M);
+            L += sc * rec[Sh::HP + hh];
+            const float *racc = rec + 2 * Sh::HP + hh * D;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) o[k] += sc * racc[lane + 32 * k];
+        }
+        const float inv = 1.f / L;
+        const int64_t ob = ((int64_t)s * p.Hq + h * G + hh) * D;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) store_out<T>(p.out, p.out_dtype, ob + lane + 32 * k, o[k] * inv);
+    }
+}
+
+template <typename T, int D, int NT>
+static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
+                         cudaStream_t stream) {
+    using Sh = DecodeShape<D, NT>;
+    static bool attr_set = false;   // per instantiation; idempotent if raced
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        attr_set = true;
+    }
+    paged_decode_kernel<T, D, NT><<<grid, kDecodeWarps * 32, Sh::SMEM_BYTES, stream>>>(prm, tk, tv);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int merge_blocks = (prm.S * prm.Hkv + 7) / 8;
+    decode_merge_kernel<T, D, NT><<<merge_blocks, 256, 0, stream>>>(prm);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+static size_t decode_record_floats(int G, int head_dim) {
+    const int HP = G > 8 ? 16 : 8;
+    return (size_t)(2 * HP + HP * head_dim);
+}
+
+static size_t workspace_bytes_for(int S, int G, int head_dim, int total_warps) {
+    size_t head = ((size_t)(S + 1) * sizeof(int) + 255) & ~size_t(255);
+    return head + (size_t)2 * total_warps * decode_record_floats(G, head_dim) * sizeof(float);
+}
+
+}  // namespace pkv
+
+extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+    using namespace pkv;
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+    int sms = 0;
+    if (current_sm_count(&sms) != PKV_OK) return 0;
+    return workspace_bytes_for(num_seqs, num_q_heads / num_kv_heads, head_dim, sms * kDecodeWarps);
+}
+
+extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *context_lens, int num_seqs, int num_blocks,
+                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          float scale, int dtype, int out_dtype, void *workspace,
+                                          size_t workspace_bytes, int *dev_status, void *stream) {
+    using namespace pkv;
+    if (num_seqs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    const int G = num_q_heads / num_kv_heads;
+    if (G > 16 || block_size != 16 || (head_dim != 64 && head_dim != 128)) return PKV_ERR_UNSUPPORTED;
+    if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
+    if (out_dtype != dtype && out_dtype != PKV_DTYPE_F32) return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    if ((int64_t)num_blocks * num_kv_heads * block_size >= (int64_t)1 << 31) return PKV_ERR_UNSUPPORTED;
+    if ((int64_t)num_seqs * max_blocks_per_seq >= (int64_t)1 << 31) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(out, 4) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return PKV_ERR_WORKSPACE;
+    int sms = 0;
+    int rc = current_sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    // enough warps for the largest possible total, at most one CTA per SM
+    const int64_t upper = (int64_t)num_seqs * num_kv_heads * max_blocks_per_seq;
+    int grid = (int)((upper + kDecodeWarps - 1) / kDecodeWarps);
+    if (grid > sms) grid = sms;
+    if (grid < 1) grid = 1;
+    const int total_warps = grid * kDecodeWarps;
+    if (workspace_bytes < workspace_bytes_for(num_seqs, G, head_dim, total_warps)) return PKV_ERR_WORKSPACE;
+
+    CUtensorMap tk, tv;
+    rc = encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    if (rc != PKV_OK) return rc;
+    rc = encode_cache_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
+    if (rc != PKV_OK) return rc;
+
+    DecodeParams prm;
+    prm.out = out;
+    prm.q = q;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.seq_start = static_cast<int *>(workspace);
+    prm.part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                         (((size_t)(num_seqs + 1) * sizeof(int) + 255) & ~size_t(255)));
+    prm.dev_status = dev_status;
+    prm.S = num_seqs;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.Hq = num_q_heads;
+    prm.Hkv = num_kv_heads;
+    prm.G = G;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.out_dtype = out_dtype;
+    prm.total_warps = total_warps;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const bool wide = G > 8;
+    if (dtype == PKV_DTYPE_BF16) {
+        if (head_dim == 128)
+            return wide ? launch_decode<__nv_bfloat16, 128, 2>(prm, tk, tv, grid, st)
+                        : launch_decode<__nv_bfloat16, 128, 1>(prm, tk, tv, grid, st);
+        return wide ? launch_decode<__nv_bfloat16, 64, 2>(prm, tk, tv, grid, st)
+                    : launch_decode<__nv_bfloat16, 64, 1>(prm, tk, tv, grid, st);
+    }
+    if (head_dim == 128)
+        return wide ? launch_decode<__half, 128, 2>(prm, tk, tv, grid, st)
+                    : launch_decode<__half, 128, 1>(prm, tk, tv, grid, st);
+    return wide ? launch_decode<__half, 64, 2>(prm, tk, tv, grid, st)
+                : launch_decode<__half, 64, 1>(prm, tk, tv, grid, st);
+}

@@ -1,0 +1,29 @@
+// Host-side helpers shared by the launchers: CUDA error capture, device
+// properties, and TMA descriptor encoding for the paged caches.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Records the CUDA error name for pkv_last_cuda_error() and returns PKV_ERR_CUDA.
+int cuda_fail(cudaError_t err);
+int cuda_fail_driver(int cu_result, const char *what);
+
+// SM count of the current device (cached per device).  PKV_OK or an error.
+int current_sm_count(int *num_sms);
+
+// Encodes a 2-D TMA descriptor over a paged cache viewed as
+// [num_blocks * num_kv_heads * block_size rows][head_dim elements] of 16-bit
+// elements, with a box of 64 elements x block_size rows and 128-byte swizzle.
+// Out-of-range rows read as zeros.
+int encode_cache_map(CUtensorMap *map, const void *base, int num_blocks, int num_kv_heads,
+                     int block_size, int head_dim);
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace pkv

@@ -1,0 +1,78 @@
+"""Helpers for the GPU parity tests: move synth arrays to the device, run the
+C-ABI calls, and compare with the oracle under the stated tolerance.
+
+Tolerance (from the 2e-3 max-abs target on fp32-accumulated outputs):
+  * fp32 output: |gpu - oracle| <= 2e-3 everywhere;
+  * 16-bit output: |gpu - oracle| <= max(2e-3, ulp(oracle)/2 + 1e-4), because a
+    correctly rounded bf16 value near 1 is already 2^-8 = 3.9e-3 away at worst.
+"""
+import numpy as np
+import torch
+
+import oracle
+
+ATOL = 2e-3
+TORCH_DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
+MANT_BITS = {"fp16": 10, "bf16": 7}
+
+
+def dev_bits(bits, dtype):
+    """uint16 bit patterns -> CUDA tensor of the 16-bit dtype (same bits)."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(TORCH_DT[dtype]).cuda()
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host_bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def out_to_f64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def half_ulp(x, dtype):
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.maximum(ax, 1e-30)))
+    if dtype == "fp16":
+        e = np.maximum(e, -14)
+    return np.exp2(e - MANT_BITS[dtype] - 1)
+
+
+def assert_close(gpu, ref, out_dtype, dtype=None, what=""):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape
+    assert np.all(np.isfinite(gpu)), "%s: non-finite output" % what
+    err = np.abs(gpu - ref)
+    if out_dtype == "fp32":
+        bound = np.full_like(ref, ATOL)
+    else:
+        bound = np.maximum(ATOL, half_ulp(ref, out_dtype) + 1e-4)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError("%s: %d elements over tolerance; worst at %s: gpu %.6g ref %.6g err %.3g bound %.3g"
+                             % (what, bad.sum(), i, gpu[i], ref[i], err[i], bound[i]))
+    return float(err.max())
+
+
+class DeviceStep:
+    """A synth.Step resident on the GPU."""
+
+    def __init__(self, st):
+        self.st = st
+        dt = st.dtype
+        self.q = dev_bits(st.q, dt)
+        self.k_new = dev_bits(st.k_new, dt)
+        self.v_new = dev_bits(st.v_new, dt)
+        self.k_cache = dev_bits(st.k_cache, dt)
+        self.v_cache = dev_bits(st.v_cache, dt)
+        self.slot_mapping = dev(st.slot_mapping)
+        self.block_tables = dev(st.block_tables)
+        self.context_lens = dev(st.context_lens)
+        self.cu_seqlens = dev(st.cu_seqlens)
+        self.status = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -1,0 +1,73 @@
+"""libpkv.so loads on a machine without a GPU and exports every symbol that
+include/pkv.h declares; host-only entry points work there; device entry points
+reject bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_cache_tables_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["pkv_kv_append", "pkv_paged_decode_attention", "pkv_paged_prefill_attention",
+                     "pkv_decode_workspace_size", "pkv_status_string", "pkv_sched_step", "pkv_pool_alloc"]:
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported():
+    L = _binding.lib()
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    L = _binding.lib()
+    assert L.pkv_status_string(0) == b"PKV_OK"
+    assert L.pkv_status_string(-3) == b"PKV_ERR_WORKSPACE"
+    assert L.pkv_status_string(12345) == b"PKV_ERR_UNKNOWN"
+    assert b"sm_103a" in L.pkv_version()
+
+
+def test_device_entry_points_validate_before_launch():
+    L = _binding.lib()
+    P = ctypes.c_void_p
+    fake = P(1 << 20)       # never dereferenced: validation fails first
+    # unsupported head_dim
+    assert L.pkv_kv_append(fake, fake, fake, 4, fake, fake, 8, 16, 2, 96, 1, None, None) == -2
+    # block_size other than 16
+    assert L.pkv_kv_append(fake, fake, fake, 4, fake, fake, 8, 8, 2, 64, 1, None, None) == -2
+    # zero tokens is a no-op
+    assert L.pkv_kv_append(None, None, None, 0, None, None, 8, 16, 2, 64, 1, None, None) == 0
+    # Hq not a multiple of Hkv
+    assert L.pkv_paged_decode_attention(fake, fake, fake, fake, fake, 4, fake, 2, 8, 6, 4, 64, 16, 0.125, 1, 1,
+                                        fake, 1 << 20, None, None) == -1
+    # group of 32 query heads per KV head is not built
+    assert L.pkv_paged_decode_attention(fake, fake, fake, fake, fake, 4, fake, 2, 8, 32, 1, 64, 16, 0.125, 1, 1,
+                                        fake, 1 << 20, None, None) == -2
+    # fp32 inputs are not a supported dtype
+    assert L.pkv_paged_decode_attention(fake, fake, fake, fake, fake, 4, fake, 2, 8, 8, 8, 64, 16, 0.125, 2, 2,
+                                        fake, 1 << 20, None, None) == -2
+    # NaN scale
+    assert L.pkv_paged_decode_attention(fake, fake, fake, fake, fake, 4, fake, 2, 8, 8, 8, 64, 16, float("nan"), 1, 1,
+                                        fake, 1 << 20, None, None) == -1
+    # zero sequences is a no-op
+    assert L.pkv_paged_decode_attention(None, None, None, None, None, 4, None, 0, 8, 8, 8, 64, 16, 0.125, 1, 1,
+                                        None, 0, None, None) == 0
+
+
+def test_workspace_size_without_a_device_is_zero():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert _binding.decode_workspace_size(4, 32, 8, 128) == 0

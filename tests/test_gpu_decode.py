@@ -1,0 +1,207 @@
+"""GPU parity of pkv_paged_decode_attention (K2 + K3) against the FP64 oracle.
+
+Small workloads are compared element by element in full; the Llama-3-8B-shaped
+step (256 sequences, lognormal contexts) runs at full size in the launch
+configuration the benchmark uses and is compared on a sample of sequences
+that includes the longest and shortest contexts.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import DeviceStep, assert_close, dev, dev_bits, host_bits, out_to_f64
+from paged_kv_cache_tables_gb300 import decode_workspace_size, kv_append, paged_decode_attention
+from synth import NAN_BITS, build_step, make_step, rne_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(ds, q, block_tables, context_lens, out_dtype, scale=None):
+    st = ds.st
+    S = q.shape[0]
+    odt = torch.float32 if out_dtype == "fp32" else q.dtype
+    out = torch.full((S, st.Hq, st.d), float("nan"), dtype=odt, device="cuda")
+    paged_decode_attention(out, q, ds.k_cache, ds.v_cache, block_tables, context_lens, scale=scale,
+                           dev_status=ds.status)
+    torch.cuda.synchronize()
+    return out
+
+
+def append_then_decode(st, out_dtype, append=True):
+    ds = DeviceStep(st)
+    if append:
+        kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
+    q_d, bt_d, cl_d = st.decode_part()
+    p = st.n_prefill
+    t0 = int(st.cu_seqlens[p])
+    out = run_decode(ds, ds.q[t0:], ds.block_tables[p:], ds.context_lens[p:], out_dtype)
+    kc, vc = st.k_cache, st.v_cache
+    if append:
+        kc, vc = kc.copy(), vc.copy()
+        oracle.append(st.k_new, st.v_new, st.slot_mapping, kc, vc, st.bs)
+    return ds, out, (q_d, kc, vc, bt_d, cl_d)
+
+
+@pytest.mark.parametrize("out_dtype", ["fp32", "same"])
+@pytest.mark.parametrize("name,kw", [("tiny", {}), ("llama1b", {"S": 64})])
+def test_decode_small_workloads_full_compare(cuda_lib, name, kw, out_dtype):
+    st = make_step(name, **kw)
+    od = "fp32" if out_dtype == "fp32" else st.dtype
+    ds, out, (q, kc, vc, bt, cl) = append_then_decode(st, od)
+    ref = oracle.decode(q, kc, vc, bt, cl, st.dtype)
+    err = assert_close(out_to_f64(out), ref, od, what=name)
+    assert int(ds.status.item()) == 0
+    print("%s %s max-abs %.3g" % (name, od, err))
+
+
+def test_decode_llama8b_full_size_sampled(cuda_lib):
+    st = make_step("llama8b")
+    ds, out32, (q, kc, vc, bt, cl) = append_then_decode(st, "fp32")
+    out16 = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "bf16")
+    ctx = st.context_lens
+    pick = sorted(set([int(np.argmax(ctx)), int(np.argmin(ctx))] + list(range(0, 256, 37))))
+    ref = oracle.decode(q[pick], kc, vc, bt[pick], cl[pick], st.dtype)
+    e32 = assert_close(out_to_f64(out32)[pick], ref, "fp32", what="llama8b fp32")
+    e16 = assert_close(out_to_f64(out16)[pick], ref, "bf16", what="llama8b bf16")
+    assert np.all(np.isfinite(out_to_f64(out32)))
+    assert int(ds.status.item()) == 0
+    print("llama8b sampled max-abs fp32 %.3g bf16 %.3g" % (e32, e16))
+
+
+def test_decode_part_of_mixed_step_with_nan_tails(cuda_lib):
+    st = make_step("mixed", n_chunks=2, chunk=64, n_decode=40, NB=8192)
+    ds, out, (q, kc, vc, bt, cl) = append_then_decode(st, "fp32")
+    ref = oracle.decode(q, kc, vc, bt, cl, st.dtype)
+    assert_close(out_to_f64(out), ref, "fp32", what="mixed decode")
+
+
+def custom_step(ctx, Hq, Hkv, d, dtype, seed=0, NB=None):
+    ctx = np.asarray(ctx, np.int64)
+    rng = np.random.default_rng(seed)
+    nb = int(((ctx + 15) // 16).sum())
+    NB = NB or nb + 7
+    # q_lens = 0: every position below the context is already stored; one
+    # query row per sequence is drawn separately
+    st = build_step("custom", rng, ctx=ctx, q_lens=np.zeros_like(ctx), Hq=Hq, Hkv=Hkv, d=d, NB=NB, dtype=dtype,
+                    pool_order=rng.permutation(NB))
+    st.q = rne_bits(rng.standard_normal((len(ctx), Hq, d), dtype=np.float32), dtype)
+    return st
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,dtype", [
+    (4, 4, 64, "fp16"), (32, 8, 64, "bf16"), (32, 8, 128, "bf16"), (32, 8, 128, "fp16"),
+    (64, 8, 128, "bf16"), (32, 2, 128, "bf16"), (16, 1, 64, "fp16"), (12, 4, 128, "bf16"),
+])
+def test_decode_edge_contexts_and_group_sizes(cuda_lib, Hq, Hkv, d, dtype):
+    ctx = [1, 15, 16, 17, 32, 33, 0, 250, 1000]
+    st = custom_step(ctx, Hq, Hkv, d, dtype, seed=Hq * d)
+    ds = DeviceStep(st)
+    out = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "fp32")
+    ref = oracle.decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, dtype)
+    assert_close(out_to_f64(out), ref, "fp32", what="edges %d/%d d%d %s" % (Hq, Hkv, d, dtype))
+    # context 0 gives exact zeros
+    assert torch.all(out[6] == 0)
+    assert int(ds.status.item()) == 0
+
+
+def test_decode_one_long_sequence_split_across_many_warps(cuda_lib):
+    st = custom_step([8192], 32, 8, 128, "bf16", seed=5)
+    ds = DeviceStep(st)
+    out = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "fp32")
+    ref = oracle.decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, "bf16")
+    assert_close(out_to_f64(out), ref, "fp32", what="8192 split")
+
+
+def test_decode_many_sequences_plan_spans_several_scan_tiles(cuda_lib):
+    rng = np.random.default_rng(2)
+    ctx = rng.integers(0, 70, size=1100)
+    st = custom_step(ctx, 8, 2, 64, "bf16", seed=3)
+    ds = DeviceStep(st)
+    out = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "fp32")
+    ref = oracle.decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, "bf16")
+    assert_close(out_to_f64(out), ref, "fp32", what="S=1100")
+
+
+def test_decode_explicit_scale(cuda_lib):
+    st = custom_step([40, 300], 8, 8, 64, "fp16", seed=9)
+    ds = DeviceStep(st)
+    out = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "fp32", scale=0.05)
+    ref = oracle.decode(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, "fp16", scale=0.05)
+    assert_close(out_to_f64(out), ref, "fp32", what="scale")
+
+
+def test_decode_block_permutation_gives_identical_bits(cuda_lib):
+    st = make_step("llama1b", S=16)
+    ds = DeviceStep(st)
+    out_a = run_decode(ds, ds.q, ds.block_tables, ds.context_lens - 1, "fp32")
+    perm = np.random.default_rng(4).permutation(st.NB)
+    kc = np.empty_like(st.k_cache)
+    vc = np.empty_like(st.v_cache)
+    kc[perm] = st.k_cache
+    vc[perm] = st.v_cache
+    tables = np.where(st.block_tables >= 0, perm[np.maximum(st.block_tables, 0)], -1).astype(np.int32)
+    ds.k_cache = dev_bits(kc, st.dtype)
+    ds.v_cache = dev_bits(vc, st.dtype)
+    out_b = run_decode(ds, ds.q, dev(tables), ds.context_lens - 1, "fp32")
+    assert torch.equal(out_a, out_b)
+
+
+def test_decode_sequence_alone_equals_sequence_in_batch(cuda_lib):
+    st = make_step("llama1b", S=64)
+    ds = DeviceStep(st)
+    full = run_decode(ds, ds.q, ds.block_tables, ds.context_lens - 1, "fp32")
+    for s in [0, 17, 63]:
+        alone = run_decode(ds, ds.q[s:s + 1], ds.block_tables[s:s + 1], ds.context_lens[s:s + 1] - 1, "fp32")
+        np.testing.assert_allclose(out_to_f64(alone[0]), out_to_f64(full[s]), rtol=0, atol=1e-5)
+
+
+def test_decode_flags_bad_block_ids_and_contexts_without_faulting(cuda_lib):
+    st = custom_step([40, 40], 8, 8, 64, "bf16", seed=1)
+    ds = DeviceStep(st)
+    bt = st.block_tables.copy()
+    bt[0, 1] = st.NB + 1000          # past the pool: reads zeros, flags
+    cl = st.context_lens.copy()
+    cl[1] = 10_000                   # beyond the table: clamped, flags
+    run_decode(ds, ds.q, dev(bt), dev(cl), "fp32")
+    flags = int(ds.status.item())
+    assert flags & 1 and flags & 2
+
+
+def test_decode_one_hot_closed_form_is_exact(cuda_lib):
+    """q = 256 e_r, a single K row with 256 in dim r: the output is exactly the
+    selected V row (fp32 output), whatever the split."""
+    rng = np.random.default_rng(8)
+    Hq, Hkv, d, dtype = 32, 8, 128, "bf16"
+    G = Hq // Hkv
+    ctx = np.array([3000, 17, 700], np.int64)
+    st = custom_step(ctx, Hq, Hkv, d, dtype, seed=8)
+    one = rne_bits(np.float32([256.0]), dtype)[0]
+    kc = st.k_cache.copy()
+    for s in range(len(ctx)):
+        for t in range(int(ctx[s])):
+            kc[st.block_tables[s, t // 16], :, t % 16, :] = 0
+    q = np.zeros_like(st.q)
+    expect = np.zeros((len(ctx), Hq, d))
+    for s in range(len(ctx)):
+        for h in range(Hq):
+            g, r = h // G, h % G
+            q[s, h, r] = one
+            t = int(rng.integers(0, ctx[s]))
+            while np.any(kc[st.block_tables[s, t // 16], g, t % 16, :G] != 0):
+                t = int(rng.integers(0, ctx[s]))
+            kc[st.block_tables[s, t // 16], g, t % 16, r] = one
+            expect[s, h] = oracle.to_double(st.v_cache[st.block_tables[s, t // 16], g, t % 16], dtype)
+    ds = DeviceStep(st)
+    ds.k_cache = dev_bits(kc, dtype)
+    ds.q = dev_bits(q, dtype)
+    out = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "fp32")
+    assert np.array_equal(out_to_f64(out), expect)
+
+
+def test_workspace_size_is_independent_of_contexts(cuda_lib):
+    a = decode_workspace_size(256, 32, 8, 128)
+    assert a > 0 and a == decode_workspace_size(256, 32, 8, 128)
+    assert decode_workspace_size(256, 64, 8, 128) > a   # 16-head records for G > 8

@@ -1,0 +1,137 @@
+"""The native scheduler and pool (libpkv.so, host only) against the hand-worked
+traces and, step by step, against the Python restatement in oracle/sched.py."""
+import os
+
+import numpy as np
+import pytest
+
+import sched_golden
+from oracle.sched import Scheduler as PyScheduler
+from paged_kv_cache_tables_gb300 import BlockPool, PkvError, Scheduler
+
+
+class _Adapter:
+    """Presents the native scheduler with the oracle's step()/stats() shape."""
+
+    def __init__(self, **kw):
+        self.s = Scheduler(**kw)
+
+    def add(self, *a):
+        self.s.add(*a)
+
+    def step(self):
+        m = self.s.step()
+        if m is None:
+            return None
+
+        class M:
+            pass
+        out = M()
+        for k, v in m.items():
+            setattr(out, k, v)
+        return out
+
+    def stats(self):
+        st = self.s.stats()
+        st["finished"] = st["finished"]
+        return st
+
+
+@pytest.mark.parametrize("path", sched_golden.all_traces(), ids=os.path.basename)
+def test_native_scheduler_reproduces_hand_worked_trace(path):
+    from test_sched_oracle import replay
+    c, _, _ = sched_golden.load(path)
+    replay(_Adapter(num_blocks=c["num_blocks"], block_size=c["block_size"], max_batch=c["max_batch"],
+                    max_num_batched_tokens=c["budget"], chunk=c["chunk"], max_model_len=c["max_model_len"]), path)
+
+
+def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fail_every=0):
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(NB)
+    py = PyScheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order)
+    nat = Scheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order)
+    arrivals = sorted((int(rng.integers(0, 60)), rid, int(rng.integers(1, 200)), int(rng.integers(1, 120)),
+                       int(rng.geometric(1 / 30))) for rid in range(n))
+    i = 0
+    for step in range(5000):
+        while i < len(arrivals) and arrivals[i][0] <= step:
+            _, rid, p, mt, eos = arrivals[i]
+            py.add(rid, p, mt, eos)
+            nat.add(rid, p, mt, eos)
+            i += 1
+        if fail_every and step % fail_every == 3:
+            py.pool.fail_at = py.pool.alloc_calls + 1
+            nat.inject_alloc_failure(1)
+        a = py.step()
+        b = nat.step()
+        assert (a is None) == (b is None), "step %d" % step
+        if a is not None:
+            for k in ["seq_rids", "q_lens", "context_lens", "cu_seqlens", "block_tables", "slot_mapping",
+                      "token_rids", "token_pos"]:
+                assert np.array_equal(getattr(a, k), b[k]), "step %d field %s" % (step, k)
+            assert a.num_prefill == b["num_prefill"]
+        sa, sb = py.stats(), nat.stats()
+        for k in ["free_blocks", "running", "waiting", "finished", "preemptions", "sum_running"]:
+            assert sa[k] == sb[k], "step %d stat %s" % (step, k)
+        if i == len(arrivals) and py.idle():
+            break
+    assert py.idle() and nat.stats()["free_blocks"] == NB
+    return py
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_native_matches_python_restatement_step_by_step(seed):
+    run_both(seed)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_native_matches_python_under_memory_pressure_and_injected_failures(seed):
+    py = run_both(100 + seed, NB=40, fail_every=7)
+    assert py.n_preemptions > 0
+
+
+def test_pool_stack_order_and_all_or_nothing():
+    p = BlockPool(4)
+    assert p.alloc(2) == [3, 2]
+    with pytest.raises(PkvError):
+        p.alloc(3)
+    assert p.free_count() == 2          # failed alloc changed nothing
+    p.free([2])
+    assert p.free_list() == [0, 1, 2]
+    with pytest.raises(PkvError):
+        p.free([2])                     # double free rejected
+    with pytest.raises(PkvError):
+        p.free([9])                     # out of range rejected
+    p.inject_failure(1)
+    with pytest.raises(PkvError):
+        p.alloc(1)
+    assert p.alloc(1) == [2]
+
+
+def test_pool_rejects_bad_initial_order():
+    with pytest.raises(ValueError):
+        BlockPool(3, [0, 0, 1])
+
+
+def test_scheduler_rejects_bad_requests():
+    s = Scheduler(16, max_model_len=64)
+    with pytest.raises(PkvError):
+        s.add(1, 0, 4, 4)
+    with pytest.raises(PkvError):
+        s.add(1, 64, 4, 4)
+    s.add(1, 10, 4, 4)
+    with pytest.raises(PkvError):
+        s.add(1, 10, 4, 4)              # duplicate rid
+
+
+def test_request_state_and_host_time():
+    s = Scheduler(64, max_model_len=256)
+    s.add(5, 20, 3, 100)
+    assert s.request_state(5) == (0, 0)
+    s.step()
+    assert s.request_state(5) == (1, 1)
+    while s.step() is not None:
+        pass
+    assert s.request_state(5) == (2, 3)
+    assert s.request_state(99)[0] == -1
+    assert s.stats()["host_ms"] >= 0.0
