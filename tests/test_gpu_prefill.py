@@ -1,0 +1,131 @@
+"""GPU parity of pkv_paged_prefill_attention (K4) against the FP64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_helpers import DeviceStep, assert_close, dev, dev_bits, out_to_f64
+from paged_kv_cache_tables_gb300 import kv_append, paged_decode_attention, paged_prefill_attention
+from synth import build_step, make_step, rne_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def chunk_step(priors, q_lens, Hq, Hkv, d, dtype, seed=0):
+    priors = np.asarray(priors, np.int64)
+    q_lens = np.asarray(q_lens, np.int64)
+    rng = np.random.default_rng(seed)
+    ctx = priors + q_lens
+    nb = int(((ctx + 15) // 16).sum())
+    NB = nb + 9
+    st = build_step("chunks", rng, ctx=ctx, q_lens=q_lens, Hq=Hq, Hkv=Hkv, d=d, NB=NB, dtype=dtype,
+                    pool_order=rng.permutation(NB), n_prefill=len(ctx))
+    return st
+
+
+def run_prefill(ds, out_dtype, q=None, cu=None, bt=None, cl=None, max_q_len=None):
+    st = ds.st
+    q = ds.q if q is None else q
+    cu = ds.cu_seqlens if cu is None else cu
+    bt = ds.block_tables if bt is None else bt
+    cl = ds.context_lens if cl is None else cl
+    odt = torch.float32 if out_dtype == "fp32" else q.dtype
+    out = torch.full((q.shape[0], st.Hq, st.d), float("nan"), dtype=odt, device="cuda")
+    mq = int(st.q_lens.max()) if max_q_len is None else max_q_len
+    paged_prefill_attention(out, q, cu, mq, ds.k_cache, ds.v_cache, bt, cl, dev_status=ds.status)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_after_append(st):
+    kc, vc = st.k_cache.copy(), st.v_cache.copy()
+    oracle.append(st.k_new, st.v_new, st.slot_mapping, kc, vc, st.bs)
+    return kc, vc
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,dtype", [
+    (4, 4, 64, "fp16"), (32, 8, 128, "bf16"), (32, 8, 64, "bf16"), (16, 2, 128, "fp16"), (12, 4, 128, "bf16"),
+    (16, 1, 64, "bf16"),
+])
+def test_prefill_small_chunks_full_compare(cuda_lib, Hq, Hkv, d, dtype):
+    priors = [0, 0, 5, 16, 100, 37]
+    q_lens = [1, 40, 17, 33, 70, 129]
+    st = chunk_step(priors, q_lens, Hq, Hkv, d, dtype, seed=Hq + d)
+    ds = DeviceStep(st)
+    kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
+    out = run_prefill(ds, "fp32")
+    kc, vc = oracle_after_append(st)
+    ref = oracle.prefill(st.q, st.cu_seqlens, kc, vc, st.block_tables, st.context_lens, dtype)
+    assert_close(out_to_f64(out), ref, "fp32", what="prefill %d/%d d%d %s" % (Hq, Hkv, d, dtype))
+    out16 = run_prefill(ds, dtype)
+    assert_close(out_to_f64(out16), ref, dtype, what="prefill 16-bit out")
+    assert int(ds.status.item()) == 0
+
+
+def test_prefill_with_one_query_row_equals_decode(cuda_lib):
+    st = make_step("llama1b", S=24)
+    ds = DeviceStep(st)
+    kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache)
+    cu = torch.arange(st.S + 1, dtype=torch.int32, device="cuda")
+    pre = torch.empty((st.S, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    paged_prefill_attention(pre, ds.q, cu, 1, ds.k_cache, ds.v_cache, ds.block_tables, ds.context_lens)
+    dec = torch.empty_like(pre)
+    paged_decode_attention(dec, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, ds.context_lens)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(pre.cpu().numpy(), dec.cpu().numpy(), rtol=0, atol=2e-5)
+
+
+def sampled_prefill_reference(st, kc, vc, rows):
+    """Oracle rows of the prefill part via attention over [0, position]."""
+    q_p, cu_p, bt_p, cl_p = st.prefill_part()
+    ref = []
+    for c, i in rows:
+        q_len = int(cu_p[c + 1] - cu_p[c])
+        pos = int(cl_p[c]) - q_len + i
+        m, l, acc = oracle.decode_range(q_p[int(cu_p[c]) + i], kc, vc, bt_p[c], 0, pos + 1, st.dtype)
+        ref.append(acc / l[:, None])
+    return np.stack(ref)
+
+
+def test_mixed_step_full_size_sampled(cuda_lib):
+    """The mixed step: append 4344 tokens, prefill 8 chunks of 512, decode 248
+    sequences -- in the launch configuration of the benchmark -- checked on
+    sampled rows of both parts."""
+    st = make_step("mixed")
+    ds = DeviceStep(st)
+    kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
+    p = st.n_prefill
+    t1 = int(st.cu_seqlens[p])
+    pre = torch.empty((t1, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    paged_prefill_attention(pre, ds.q[:t1], ds.cu_seqlens[:p + 1], 512, ds.k_cache, ds.v_cache,
+                            ds.block_tables[:p], ds.context_lens[:p], dev_status=ds.status)
+    dec = torch.empty((st.S - p, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    paged_decode_attention(dec, ds.q[t1:], ds.k_cache, ds.v_cache, ds.block_tables[p:], ds.context_lens[p:],
+                           dev_status=ds.status)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) == 0
+    kc, vc = oracle_after_append(st)
+    rng = np.random.default_rng(0)
+    rows = [(c, i) for c in range(p) for i in [0, 1, 255, 511, int(rng.integers(2, 511))]]
+    ref = sampled_prefill_reference(st, kc, vc, rows)
+    got = np.stack([out_to_f64(pre[int(st.cu_seqlens[c]) + i]) for c, i in rows])
+    e1 = assert_close(got, ref, "fp32", what="mixed prefill rows")
+    pick = [0, 5, 100, 247]
+    q_d, bt_d, cl_d = st.decode_part()
+    refd = oracle.decode(q_d[pick], kc, vc, bt_d[pick], cl_d[pick], st.dtype)
+    e2 = assert_close(out_to_f64(dec)[pick], refd, "fp32", what="mixed decode rows")
+    assert np.all(np.isfinite(pre.cpu().numpy()))
+    print("mixed sampled max-abs prefill %.3g decode %.3g" % (e1, e2))
+
+
+def test_prefill_flags_a_chunk_longer_than_its_context(cuda_lib):
+    st = chunk_step([10, 20], [5, 6], 8, 8, 64, "bf16", seed=4)
+    ds = DeviceStep(st)
+    cl = st.context_lens.copy()
+    cl[0] = 3                         # q_len 5 > ctx 3: skipped and flagged
+    out = torch.zeros((st.T, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    paged_prefill_attention(out, ds.q, ds.cu_seqlens, 6, ds.k_cache, ds.v_cache, ds.block_tables, dev(cl),
+                            dev_status=ds.status)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) & 16
+    assert torch.all(out[:5] == 0)    # the bad chunk's rows were not written
