@@ -73,8 +73,9 @@ extern "C" {
 /* Human-readable name of a status code (static string, never NULL). */
 const char *pkv_status_string(int status);
 
-/* Name of the last CUDA error seen by this thread inside the library
- * ("no error" if none).  Static/thread-local string, never NULL. */
+/* Name of the last CUDA error seen by this thread inside the library, or the
+ * reason for the last size-limit rejection ("no error" if none).
+ * Static/thread-local string, never NULL. */
 const char *pkv_last_cuda_error(void);
 
 /* Library version string, e.g. "pkv 0.1 sm_103a". */
@@ -173,6 +174,45 @@ int pkv_paged_prefill_attention(void *out, const void *q, const int32_t *cu_seql
                                 int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, float scale, int dtype, int out_dtype,
                                 int *dev_status, void *stream);
+
+/*
+ * pkv_paged_decode_attention_static -- the same decode attention, for callers
+ * that cannot allocate device memory.  The pages describe no counterpart:
+ * this entry point exists only for the memory model of some callers.
+ *
+ * pkv_paged_decode_attention needs a caller-provided workspace.  Some callers
+ * cannot allocate one: a serving engine that hands all free HBM to its KV
+ * pool at start-up and allows no allocation afterwards, a plugin whose host
+ * framework owns every device allocation, or a latency-critical loop that must
+ * not call cudaMalloc because it can synchronise the device.  This entry point
+ * takes the same arguments minus the workspace and uses one scratch array of
+ * PKV_STATIC_SCRATCH_BYTES that the library keeps in device global memory
+ * (a file-scope __device__ array: every GPU that loads the library holds it
+ * until the process exits).  It calls no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ *
+ * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS and a shape whose
+ *   pkv_decode_workspace_size() fits in PKV_STATIC_SCRATCH_BYTES (every
+ *   supported head_dim/group size does on a 152-SM GB300); otherwise
+ *   PKV_ERR_WORKSPACE is returned before anything is enqueued, and
+ *   pkv_last_cuda_error() names the limit.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ * - All calls on a device share the one array, and it keeps the last call's
+ *   contents.  The kernels read nothing from it that the same call did not
+ *   write first, so nothing needs clearing; but calls that overlap on the GPU
+ *   (different streams, or different host threads, without ordering between
+ *   them) race on the array and give wrong results.  Serialise them.
+ * Results equal pkv_paged_decode_attention's for the same inputs.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (24u << 20)
+#define PKV_STATIC_MAX_SEQS 16384
+int pkv_paged_decode_attention_static(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                      const int32_t *block_tables, int max_blocks_per_seq,
+                                      const int32_t *context_lens, int num_seqs, int num_blocks,
+                                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                      float scale, int dtype, int out_dtype, int *dev_status, void *stream);
 
 /* ---- host block pool ----------------------------------------------------------
  * A preallocated set of physical block ids with a free list used as a stack

@@ -71,6 +71,7 @@ def lib():
         "pkv_decode_workspace_size": ([I, I, I, I], SZ),
         "pkv_paged_decode_attention": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, SZ, P, P], I),
         "pkv_paged_prefill_attention": ([P, P, P, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, P], I),
+        "pkv_paged_decode_attention_static": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P], I),
         "pkv_pool_create": ([I, P], P),
         "pkv_pool_destroy": ([P], None),
         "pkv_pool_alloc": ([P, I, P], I),

@@ -24,6 +24,8 @@ int cuda_fail_driver(int cu_result, const char *what) {
     return PKV_ERR_CUDA;
 }
 
+void set_error_message(const char *msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 int current_sm_count(int *num_sms) {
     static int cached[64] = {0};
     int dev = 0;

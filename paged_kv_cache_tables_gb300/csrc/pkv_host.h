@@ -13,6 +13,8 @@ namespace pkv {
 // Records the CUDA error name for pkv_last_cuda_error() and returns PKV_ERR_CUDA.
 int cuda_fail(cudaError_t err);
 int cuda_fail_driver(int cu_result, const char *what);
+// Records a message for pkv_last_cuda_error() (size-limit rejections).
+void set_error_message(const char *msg);
 
 // SM count of the current device (cached per device).  PKV_OK or an error.
 int current_sm_count(int *num_sms);
