@@ -146,29 +146,32 @@ def to_dev_bits(a, dtype):
     return t.view(torch.bfloat16 if dtype == "bf16" else torch.float16).cuda()
 
 
-def cpu_oracle_sample(st, budget_s):
-    """Time the oracle on the first k sequences of the step, k sized to ~budget_s."""
+def oracle_sample_size(st, budget_s):
+    """Number k of leading sequences whose oracle decode takes about budget_s
+    on this host (calibrated on the first sequence)."""
     import oracle
-    q, bt, cl = st.q, st.block_tables, st.context_lens
-    kc, vc = st.k_cache, st.v_cache
-    # calibrate on one short sequence
-    order = list(range(st.S))
     t0 = time.perf_counter()
-    oracle.decode(q[:1], kc, vc, bt[:1], cl[:1], st.dtype)
-    per_tok = (time.perf_counter() - t0) / max(1, int(cl[0]))
+    oracle.decode(st.q[:1], st.k_cache, st.v_cache, st.block_tables[:1], st.context_lens[:1], st.dtype)
+    per_tok = (time.perf_counter() - t0) / max(1, int(st.context_lens[0]))
     k, acc = 0, 0.0
-    while k < st.S and acc + per_tok * int(cl[k]) <= budget_s:
-        acc += per_tok * int(cl[k])
+    while k < st.S and acc + per_tok * int(st.context_lens[k]) <= budget_s:
+        acc += per_tok * int(st.context_lens[k])
         k += 1
-    k = max(k, 1)
+    return max(k, 1)
+
+
+def cpu_oracle_run(st, k):
+    """Time the oracle (as it stands: one thread, FP64) on the first k sequences."""
+    import oracle
+    cl = st.context_lens[:k]
     t0 = time.perf_counter()
-    oracle.decode(q[:k], kc, vc, bt[:k], cl[:k], st.dtype)
+    oracle.decode(st.q[:k], st.k_cache, st.v_cache, st.block_tables[:k], cl, st.dtype)
     dt = time.perf_counter() - t0
-    nbytes = decode_bytes(cl[:k], st.Hq, st.Hkv, st.d)
+    nbytes = decode_bytes(cl, st.Hq, st.Hkv, st.d)
     return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "first %d of %d sequences of the step (%d attended tokens), decode only, %.1f s"
-                      % (k, st.S, int(cl[:k].sum()), dt),
-            "seconds": dt, "tokens_per_s": float(cl[:k].sum()) / dt}
+            "sample": "first %d of %d sequences of the step (%d attended tokens), decode only, %.2f s"
+                      % (k, st.S, int(cl.sum()), dt),
+            "seconds": dt}
 
 
 def run_reference(args):
@@ -177,9 +180,11 @@ def run_reference(args):
         return
     from synth import make_step
     st = make_step("llama8b")
+    budget = min(args.ref_budget, 150.0 / (args.steps + args.warmup))
+    k = oracle_sample_size(st, budget)
     vals = []
     for i in range(args.warmup + args.steps):
-        r = cpu_oracle_sample(st, args.ref_budget)
+        r = cpu_oracle_run(st, k)
         if i >= args.warmup:
             vals.append(r)
     v = statistics.median([r["value"] for r in vals])
@@ -324,17 +329,16 @@ def run_pkv(args):
         "kernels_ms": {"kv_append": round(app_ms, 4), "paged_decode_attention": round(dec_ms, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_kind,
-                     "kernel": "paged_decode_attention (split-KV + merge), bytes %d per launch" % dbytes},
+                     "kernel": "paged_decode_kernel (split-KV, fused merge), bytes %d per launch" % dbytes},
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and ws == 1:
-        cb = cpu_oracle_sample(st, args.cpu_budget)
+        cb = cpu_oracle_run(st, oracle_sample_size(st, args.cpu_budget))
         cb.pop("seconds")
-        cb.pop("tokens_per_s")
         line["cpu_baseline"] = cb
     print(json.dumps(line))
 
@@ -342,8 +346,8 @@ def run_pkv(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
@@ -355,8 +359,7 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
-        # each reference step is a bounded oracle sample; keep the whole run to a few minutes
-        args.ref_budget = min(args.ref_budget, 150.0 / (args.steps + args.warmup))
+        # each reference step is a bounded oracle sample sized so the run takes a few minutes
         run_reference(args)
     else:
         run_pkv(args)

@@ -11,7 +11,9 @@
 //    contiguous ranges, one per warp of a persistent grid (one CTA of 8 warps
 //    per SM).  Every warp streams the same number of 16-token blocks, whatever
 //    the context-length mix; a (sequence, head) range that crosses a warp
-//    boundary is finished by the merge kernel from per-warp partials (m, l, acc).
+//    boundary leaves per-warp partials (m, l, acc), and the warp that finishes
+//    the range's last piece combines them by log-sum-exp (an arrival counter
+//    per range, tagged with the call's epoch, tells it that it is last).
 //  * Each warp runs its own ring of STAGES shared-memory slots.  Lane 0 issues
 //    2-D TMA loads (128-byte swizzle) of the K and V tiles of a block -- the
 //    block id comes from the block table -- and the warp waits on the slot's
@@ -24,6 +26,7 @@
 //    rounding residual), so the weights keep ~16 significant bits.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "pkv.h"
@@ -41,12 +44,13 @@ struct DecodeParams {
     const int32_t *block_tables;
     const int32_t *context_lens;
     float *part;        // [2 * total_warps][record] partial results
-    int *seq_start;     // [S + 1]: exclusive prefix sum of blocks per sequence
+    unsigned long long *arrivals;   // [S * Hkv]: (epoch << 32) | pieces arrived
     int *dev_status;
     int S, max_blocks, num_blocks, Hq, Hkv, G;
     float scale_log2;   // scale * log2(e): scores are kept in base-2 units
     int out_dtype;
     int total_warps;
+    uint32_t epoch;     // nonzero, different for every call
 };
 
 template <int D, int NT>
@@ -101,6 +105,83 @@ __device__ __forceinline__ int64_t block_scan(int64_t v, int64_t *sh, int64_t *t
 
 __device__ __forceinline__ int64_t range_lo(int64_t w, int64_t total, int64_t nw) { return w * total / nw; }
 
+// The warp whose range holds flat position x: the largest w with range_lo(w) <= x.
+__device__ __forceinline__ int64_t owner_of(int64_t x, int64_t total, int64_t nw) {
+    return ((x + 1) * nw + total - 1) / total - 1;
+}
+
+// Counts one more finished piece of a split (sequence, KV head) range and
+// returns how many have finished in this call.  The counter carries the call's
+// epoch in its high half, so a value left by an earlier call counts as zero
+// and the workspace never needs clearing.  Returns 0 if the update kept losing
+// races (not expected: at most a handful of warps share a range).
+__device__ __forceinline__ uint32_t count_arrival(unsigned long long *ctr, uint32_t epoch) {
+    unsigned long long cur = atomicAdd(ctr, 0ull);
+    for (int it = 0; it < (1 << 16); ++it) {
+        const unsigned long long want =
+            (uint32_t)(cur >> 32) == epoch ? cur + 1ull : (((unsigned long long)epoch << 32) | 1ull);
+        const unsigned long long prev = atomicCAS(ctr, cur, want);
+        if (prev == cur) return (uint32_t)(want & 0xffffffffull);
+        cur = prev;
+    }
+    return 0;
+}
+
+// Log-sum-exp combination of the partial records of one split range, run by
+// the warp that finished its last piece.  Records: warp w0 left its piece in
+// slot 1 (range ended past its end), later warps in slot 0.  Lane hh folds the
+// (max, sum) pairs of head hh over the pieces; then every lane accumulates its
+// D/32 output columns of every head, with all loads of a piece independent.
+template <typename T, int D, int NT>
+__device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t w0, int64_t w1, int64_t total,
+                                             int64_t nw, int s, int h, int lane) {
+    using Sh = DecodeShape<D, NT>;
+    constexpr int HP = Sh::HP, PER = D / 32;
+    const int G = p.G;
+    auto rec_of = [&](int64_t w) { return p.part + (size_t)(w * 2 + (w == w0 ? 1 : 0)) * Sh::REC; };
+    auto empty_range = [&](int64_t w) { return range_lo(w + 1, total, nw) == range_lo(w, total, nw); };
+    float M = -INFINITY, L = 0.f;
+    if (lane < G) {
+        for (int64_t w = w0; w <= w1; ++w) {
+            if (empty_range(w)) continue;
+            const float *rec = rec_of(w);
+            const float mv = __ldcg(rec + lane), lv = __ldcg(rec + HP + lane);
+            const float Mn = fmaxf(M, mv);
+            L = L * exp2_approx(M - Mn) + lv * exp2_approx(mv - Mn);
+            M = Mn;
+        }
+    }
+    float Mh[HP], invL[HP], o[HP][PER];
+#pragma unroll
+    for (int hh = 0; hh < HP; ++hh) {
+        Mh[hh] = __shfl_sync(0xffffffffu, M, hh);
+        invL[hh] = 1.f / __shfl_sync(0xffffffffu, L, hh);
+#pragma unroll
+        for (int k = 0; k < PER; ++k) o[hh][k] = 0.f;
+    }
+    for (int64_t w = w0; w <= w1; ++w) {
+        if (empty_range(w)) continue;
+        const float *rec = rec_of(w);
+#pragma unroll
+        for (int hh = 0; hh < HP; ++hh) {
+            if (hh < G) {
+                const float f = exp2_approx(__ldcg(rec + hh) - Mh[hh]) * invL[hh];
+                const float *racc = rec + 2 * HP + hh * D;
+#pragma unroll
+                for (int k = 0; k < PER; ++k) o[hh][k] += f * __ldcg(racc + lane + 32 * k);
+            }
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < HP; ++hh) {
+        if (hh < G) {
+            const int64_t ob = ((int64_t)s * p.Hq + (int64_t)h * G + hh) * D;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) store_out<T>(p.out, p.out_dtype, ob + lane + 32 * k, o[hh][k]);
+        }
+    }
+}
+
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tk,
@@ -112,8 +193,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     uint8_t *ring = smem;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sh::RING_BYTES);
     int64_t *sh_scan = reinterpret_cast<int64_t *>(bars + kDecodeWarps * STAGES);
-    int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);
+    int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);   // segment holding each warp's first block
     int *plan_off = plan_s + kDecodeWarps;
+    int *plan_s2 = plan_off + kDecodeWarps;                             // ... and its last block
+    int *plan_off2 = plan_s2 + kDecodeWarps;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv;
@@ -133,24 +216,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         const int nb = s < p.S ? blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) : 0;
         int64_t tile_total;
         const int64_t excl = carry + block_scan(nb, sh_scan, &tile_total) - nb;
-        if (blockIdx.x == 0 && s < p.S) p.seq_start[s] = (int)excl;
         if (nb > 0) {
 #pragma unroll
             for (int w = 0; w < kDecodeWarps; ++w) {
                 const int64_t lo = range_lo((int64_t)blockIdx.x * kDecodeWarps + w, total, nw);
+                const int64_t last = range_lo((int64_t)blockIdx.x * kDecodeWarps + w + 1, total, nw) - 1;
                 if (lo >= excl * Hkv && lo < (excl + nb) * Hkv) {
                     plan_s[w] = s;
                     plan_off[w] = (int)(lo - excl * Hkv);
+                }
+                if (last >= excl * Hkv && last < (excl + nb) * Hkv) {
+                    plan_s2[w] = s;
+                    plan_off2[w] = (int)(last - excl * Hkv);
                 }
             }
         }
         carry += tile_total;
     }
-    if (blockIdx.x == 0 && tid == 0) p.seq_start[p.S] = (int)total_nblk;
     __syncthreads();
 
+    // sequences with an empty context get all-zero rows
+    for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
+        if (blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) != 0) continue;
+        for (int e = tid; e < p.Hq * D; e += blockDim.x) store_out<T>(p.out, p.out_dtype, (int64_t)s * p.Hq * D + e, 0.f);
+    }
+
     const int64_t wg = (int64_t)blockIdx.x * kDecodeWarps + warp;
-    const int n = (int)(range_lo(wg + 1, total, nw) - range_lo(wg, total, nw));
+    const int64_t lo_w = range_lo(wg, total, nw);
+    const int n = (int)(range_lo(wg + 1, total, nw) - lo_w);
     if (n <= 0 || plan_s[warp] < 0) return;
 
     // ---- this warp's ring ----
@@ -167,12 +260,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     __syncwarp();
     const uint64_t policy = l2_policy_evict_first();
 
-    // consumer and producer cursors over (sequence, head, block)
-    int cs = plan_s[warp], c_ctx;
-    int c_nb = blocks_of(p.context_lens, cs, p.max_blocks, nullptr, &c_ctx);
-    int ch = plan_off[warp] / c_nb, cj = plan_off[warp] % c_nb;
-    int ps = cs, p_nb = c_nb, ph = ch, pj = cj;
-    bool started_mid = cj != 0;
+    // Block order inside the range: if the range's last (sequence, KV head)
+    // segment continues into the next warp, that tail piece is streamed first,
+    // then the range from its start.  Both pieces of a split segment are then
+    // finished early in the kernel, so the warp that combines them does so
+    // while the other warps keep HBM busy, not at the very end.
+    const int s_head = plan_s[warp], off_head = plan_off[warp];
+    const int nb_head = blocks_of(p.context_lens, s_head, p.max_blocks, nullptr, nullptr);
+    const int s_last = plan_s2[warp];
+    const int nb_last = blocks_of(p.context_lens, s_last, p.max_blocks, nullptr, nullptr);
+    const int j_last = plan_off2[warp] % nb_last;
+    const int64_t t_start = lo_w + n - 1 - j_last;                  // flat start of the last segment
+    const int n_tail = (j_last < nb_last - 1 && t_start > lo_w) ? (int)(lo_w + n - t_start) : 0;
 
     auto next_seq = [&](int s, int &nb_out, int *ctx_out) {
         int nb;
@@ -183,8 +282,33 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         nb_out = nb;
         return s;
     };
+    // consumer (c*) and producer (p*) cursors over (sequence, head, block)
+    int cs, c_ctx, c_nb, ch, cj;
+    auto seek_head = [&](int &s_, int &nb_, int &h_, int &j_, int *ctx_) {
+        s_ = s_head;
+        nb_ = blocks_of(p.context_lens, s_, p.max_blocks, nullptr, ctx_);
+        h_ = off_head / nb_;
+        j_ = off_head % nb_;
+    };
+    if (n_tail > 0) {
+        cs = s_last;
+        c_nb = blocks_of(p.context_lens, cs, p.max_blocks, nullptr, &c_ctx);
+        ch = plan_off2[warp] / c_nb;
+        cj = 0;
+    } else {
+        seek_head(cs, c_nb, ch, cj, &c_ctx);
+    }
+    int ps = cs, p_nb = c_nb, ph = ch, pj = cj;
+    bool started_mid = n_tail == 0 && cj != 0;
+    (void)nb_head;
+
     auto table_entry = [&]() { return __ldg(p.block_tables + (int64_t)ps * p.max_blocks + pj); };
-    auto advance_producer = [&]() {
+    // move the producer from block k of the warp's order to block k + 1
+    auto advance_producer = [&](int k) {
+        if (k + 1 == n_tail) {
+            seek_head(ps, p_nb, ph, pj, nullptr);
+            return;
+        }
         if (++pj == p_nb) {
             pj = 0;
             if (++ph == Hkv) {
@@ -218,7 +342,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     for (int k = 0; k < pro; ++k) {
         issue(k, pending);
         if (k + 1 < n) {
-            advance_producer();
+            advance_producer(k);
             pending = table_entry();
         }
     }
@@ -375,14 +499,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         if (i + STAGES < n) {
             issue(stage, pending);
             if (i + STAGES + 1 < n) {
-                advance_producer();
+                advance_producer(i + STAGES);
                 pending = table_entry();
             }
         }
 
         // ---- end of a (sequence, head) range in this warp ----
         const bool seg_done = cj == c_nb - 1;
-        if (seg_done || i == n - 1) {
+        if (seg_done || i == n - 1 || i == n_tail - 1) {
             float lsum[NT];
 #pragma unroll
             for (int pn = 0; pn < NT; ++pn) {
@@ -433,12 +557,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                         racc[hb * D + d0 + 8] = acc[mt][pn][3];
                     }
                 }
+                // the warp that finishes the last piece of the range combines them
+                __threadfence();
+                __syncwarp();
+                const int64_t flat = i < n_tail ? t_start + i : lo_w + (i - n_tail);
+                const int64_t seg_lo = flat - cj, seg_hi = seg_lo + c_nb - 1;
+                const int64_t w0 = owner_of(seg_lo, total, nw), w1 = owner_of(seg_hi, total, nw);
+                uint32_t pieces = 0;
+                for (int64_t w = w0; w <= w1; ++w) pieces += range_lo(w + 1, total, nw) > range_lo(w, total, nw);
+                unsigned long long *ctr = p.arrivals + (size_t)cs * Hkv + ch;
+                uint32_t arrived = 0;
+                if (lane == 0) arrived = count_arrival(ctr, p.epoch);
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == pieces) {
+                    __threadfence();
+                    merge_pieces<T, D, NT>(p, w0, w1, total, nw, cs, ch, lane);
+                    if (lane == 0) atomicExch(ctr, 0ull);
+                } else if (arrived == 0) {
+                    set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+                }
             }
             started_mid = false;
             seg_fresh = true;
         }
         // advance the consumer cursor
-        if (i + 1 < n) {
+        if (i + 1 == n_tail) {
+            seek_head(cs, c_nb, ch, cj, &c_ctx);
+            started_mid = cj != 0;
+        } else if (i + 1 < n) {
             if (++cj == c_nb) {
                 cj = 0;
                 if (++ch == Hkv) {
@@ -447,62 +593,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 }
             }
         }
-    }
-}
-
-// Combines the partials of (sequence, KV head) ranges that crossed a warp
-// boundary, and writes zeros for sequences with an empty context.  One warp
-// per (sequence, KV head).
-template <typename T, int D, int NT>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const DecodeParams p) {
-    using Sh = DecodeShape<D, NT>;
-    const int lane = threadIdx.x & 31;
-    const int idx = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (idx >= p.S * p.Hkv) return;
-    const int s = idx / p.Hkv, h = idx - s * p.Hkv;
-    const int G = p.G;
-    const int nb = blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr);
-    constexpr int PER = D / 32;
-    if (nb == 0) {
-        for (int hh = 0; hh < G; ++hh) {
-            const int64_t o = ((int64_t)s * p.Hq + h * G + hh) * D;
-#pragma unroll
-            for (int k = 0; k < PER; ++k) store_out<T>(p.out, p.out_dtype, o + lane + 32 * k, 0.f);
-        }
-        return;
-    }
-    const int64_t total = (int64_t)p.seq_start[p.S] * p.Hkv;
-    const int64_t nw = p.total_warps;
-    const int64_t seg_lo = (int64_t)p.seq_start[s] * p.Hkv + (int64_t)h * nb;
-    const int64_t seg_hi = seg_lo + nb - 1;
-    // warp holding flat position x: the largest w with range_lo(w) <= x
-    auto owner = [&](int64_t x) { return ((x + 1) * nw + total - 1) / total - 1; };
-    const int64_t w0 = owner(seg_lo), w1 = owner(seg_hi);
-    if (w0 == w1) return;   // finished by its warp
-    for (int hh = 0; hh < G; ++hh) {
-        float M = -INFINITY;
-        for (int64_t w = w0; w <= w1; ++w) {
-            if (range_lo(w + 1, total, nw) == range_lo(w, total, nw)) continue;   // warp with no blocks
-            const float *rec = p.part + (size_t)(w * 2 + (w == w0 ? 1 : 0)) * Sh::REC;
-            M = fmaxf(M, rec[hh]);
-        }
-        float L = 0.f;
-        float o[PER];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) o[k] = 0.f;
-        for (int64_t w = w0; w <= w1; ++w) {
-            if (range_lo(w + 1, total, nw) == range_lo(w, total, nw)) continue;
-            const float *rec = p.part + (size_t)(w * 2 + (w == w0 ? 1 : 0)) * Sh::REC;
-            const float sc = exp2_approx(rec[hh] - M);
-            L += sc * rec[Sh::HP + hh];
-            const float *racc = rec + 2 * Sh::HP + hh * D;
-#pragma unroll
-            for (int k = 0; k < PER; ++k) o[k] += sc * racc[lane + 32 * k];
-        }
-        const float inv = 1.f / L;
-        const int64_t ob = ((int64_t)s * p.Hq + h * G + hh) * D;
-#pragma unroll
-        for (int k = 0; k < PER; ++k) store_out<T>(p.out, p.out_dtype, ob + lane + 32 * k, o[k] * inv);
     }
 }
 
@@ -519,10 +609,6 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
     }
     paged_decode_kernel<T, D, NT><<<grid, kDecodeWarps * 32, Sh::SMEM_BYTES, stream>>>(prm, tk, tv);
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
-    const int merge_blocks = (prm.S * prm.Hkv + 7) / 8;
-    decode_merge_kernel<T, D, NT><<<merge_blocks, 256, 0, stream>>>(prm);
-    e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
@@ -531,9 +617,18 @@ static size_t decode_record_floats(int G, int head_dim) {
     return (size_t)(2 * HP + HP * head_dim);
 }
 
-static size_t workspace_bytes_for(int S, int G, int head_dim, int total_warps) {
-    size_t head = ((size_t)(S + 1) * sizeof(int) + 255) & ~size_t(255);
-    return head + (size_t)2 * total_warps * decode_record_floats(G, head_dim) * sizeof(float);
+// Workspace: [arrival counters, S * Hkv x 8 B, padded to 256 B][partial records].
+static size_t arrivals_bytes(int S, int Hkv) { return ((size_t)S * Hkv * 8 + 255) & ~size_t(255); }
+
+static size_t workspace_bytes_for(int S, int Hkv, int G, int head_dim, int total_warps) {
+    return arrivals_bytes(S, Hkv) + (size_t)2 * total_warps * decode_record_floats(G, head_dim) * sizeof(float);
+}
+
+static uint32_t next_epoch() {
+    static std::atomic<uint32_t> epoch{0};
+    uint32_t e = ++epoch;
+    if (e == 0) e = ++epoch;
+    return e;
 }
 
 }  // namespace pkv
@@ -543,7 +638,7 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
     int sms = 0;
     if (current_sm_count(&sms) != PKV_OK) return 0;
-    return workspace_bytes_for(num_seqs, num_q_heads / num_kv_heads, head_dim, sms * kDecodeWarps);
+    return workspace_bytes_for(num_seqs, num_kv_heads, num_q_heads / num_kv_heads, head_dim, sms * kDecodeWarps);
 }
 
 extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -579,7 +674,8 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
     const int total_warps = grid * kDecodeWarps;
-    if (workspace_bytes < workspace_bytes_for(num_seqs, G, head_dim, total_warps)) return PKV_ERR_WORKSPACE;
+    if (workspace_bytes < workspace_bytes_for(num_seqs, num_kv_heads, G, head_dim, total_warps))
+        return PKV_ERR_WORKSPACE;
 
     CUtensorMap tk, tv;
     rc = encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
@@ -592,9 +688,8 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     prm.q = q;
     prm.block_tables = block_tables;
     prm.context_lens = context_lens;
-    prm.seq_start = static_cast<int *>(workspace);
-    prm.part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                         (((size_t)(num_seqs + 1) * sizeof(int) + 255) & ~size_t(255)));
+    prm.arrivals = static_cast<unsigned long long *>(workspace);
+    prm.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + arrivals_bytes(num_seqs, num_kv_heads));
     prm.dev_status = dev_status;
     prm.S = num_seqs;
     prm.max_blocks = max_blocks_per_seq;
@@ -605,6 +700,7 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.out_dtype = out_dtype;
     prm.total_warps = total_warps;
+    prm.epoch = next_epoch();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool wide = G > 8;
     if (dtype == PKV_DTYPE_BF16) {
