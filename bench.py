@@ -51,6 +51,28 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+def load_tensor_peak():
+    """bf16 dense peak for a kernel timed inside a long step (sustained)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops_sustained"]), "measured (sustained)"
+    except Exception:
+        return 1700.0, "fallback (sustained)"
+
+
+def prefill_flops(ctx, q_lens, Hq, d):
+    """Algorithmic FLOPs of causal chunked prefill: query i of a chunk of q_len
+    attends prior + i + 1 keys; QK^T and PV each take 2*d FLOPs per (query
+    head, key)."""
+    total = 0
+    for c, q in zip(ctx, q_lens):
+        prior = int(c) - int(q)
+        keys = q * prior + q * (q + 1) // 2
+        total += 4 * Hq * d * keys
+    return total
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
     Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -239,6 +261,75 @@ def run_e2e(args, ws, st, q, kn, vn, slots, bt, cl, out, kc, vc, work, status, s
 
 
 
+def run_mixed(args):
+    """The mixed step: append 4344 tokens, prefill 8 chunks of 512 (prior
+    context U{0..4096}), decode 248 sequences, on one stream."""
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    from synth import make_step
+    st = make_step("mixed")
+    p = st.n_prefill
+    t1 = int(st.cu_seqlens[p])
+    q = to_dev_bits(st.q, st.dtype)
+    kn, vn = to_dev_bits(st.k_new, st.dtype), to_dev_bits(st.v_new, st.dtype)
+    kc, vc = to_dev_bits(st.k_cache, st.dtype), to_dev_bits(st.v_cache, st.dtype)
+    slots = torch.from_numpy(st.slot_mapping).cuda()
+    bt = torch.from_numpy(st.block_tables).cuda()
+    cl = torch.from_numpy(st.context_lens).cuda()
+    cu = torch.from_numpy(st.cu_seqlens).cuda()
+    out = torch.empty((st.T, st.Hq, st.d), dtype=torch.bfloat16, device="cuda")
+    work = torch.empty(pkv.decode_workspace_size(st.S - p, st.Hq, st.Hkv, st.d), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    q_p, q_d, o_p, o_d = q[:t1], q[t1:], out[:t1], out[t1:]
+    bt_p, bt_d, cl_p, cl_d, cu_p = bt[:p], bt[p:], cl[:p], cl[p:], cu[:p + 1]
+    max_q = int(st.q_lens[:p].max())
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        pkv.kv_append(kn, vn, slots, kc, vc, dev_status=status, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        pkv.paged_prefill_attention(o_p, q_p, cu_p, max_q, kc, vc, bt_p, cl_p, dev_status=status, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        pkv.paged_decode_attention(o_d, q_d, kc, vc, bt_d, cl_d, workspace=work, dev_status=status, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    K = args.mixed_steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for k in range(K):
+        step(evs[k])
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the mixed step" % int(status.item()))
+    ms = lambda a, b: statistics.mean(evs[k][a].elapsed_time(evs[k][b]) for k in range(K))
+    step_ms, app_ms, pre_ms, dec_ms = ms(0, 3), ms(0, 1), ms(1, 2), ms(2, 3)
+    flops = prefill_flops(st.context_lens[:p], st.q_lens[:p], st.Hq, st.d)
+    dbytes = decode_bytes(st.context_lens[p:], st.Hq, st.Hkv, st.d)
+    tpeak, tkind = load_tensor_peak()
+    hpeak, hkind = load_peaks()
+    tfl = flops / (pre_ms * 1e-3) / 1e12
+    return {
+        "workload": "mixed: 8 prefill chunks x 512 (prior U{0..4096}) + 248 decodes (ctx U{256..4096}), 32/8 heads, "
+                    "d 128, bf16; append of 4344 tokens first",
+        "steps": K, "ms_per_step": round(step_ms, 4),
+        "kv_append_ms": round(app_ms, 4),
+        "prefill": {"ms": round(pre_ms, 4), "gflop": round(flops / 1e9, 2), "tflops": round(tfl, 1),
+                    "roofline": {"bound": "tensor", "achieved": round(tfl, 1), "peak": tpeak, "unit": "TFLOP/s",
+                                 "frac": round(tfl / tpeak, 4), "traffic": None, "peak_source": tkind}},
+        "decode": {"ms": round(dec_ms, 4), "bytes": dbytes,
+                   "roofline": {"bound": "hbm", "achieved": round(dbytes / (dec_ms * 1e-3) / 1e9, 1), "peak": hpeak,
+                                "unit": "GB/s", "frac": round(dbytes / (dec_ms * 1e-3) / 1e9 / hpeak, 4),
+                                "traffic": None, "peak_source": hkind}},
+    }
+
+
 def run_pkv(args):
     import torch
     import paged_kv_cache_tables_gb300 as pkv
@@ -336,6 +427,8 @@ def run_pkv(args):
         "gpu_launches": 2 * K,
         "clocks": clk.summary(),
     }
+    if not args.no_mixed:
+        line["mixed_step"] = run_mixed(args)
     if not args.no_cpu_baseline and ws == 1:
         cb = cpu_oracle_run(st, oracle_sample_size(st, args.cpu_budget))
         cb.pop("seconds")
@@ -353,6 +446,8 @@ def main():
     ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-mixed", action="store_true", help="skip the mixed prefill + decode step")
+    ap.add_argument("--mixed-steps", type=int, default=50)
     ap.add_argument("--seqs", type=int, default=0, help="override the sequence count (profiling cases)")
     ap.add_argument("--pool", type=int, default=0, help="override the pool size in blocks (profiling cases)")
     args = ap.parse_args()

@@ -369,8 +369,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 const int c0 = (kk * 16 + 2 * t4) >> 1;
                 qa[kk][0] = g < G ? __ldg(qbase + g * (D / 2) + c0) : 0u;
                 qa[kk][2] = g < G ? __ldg(qbase + g * (D / 2) + c0 + 4) : 0u;
-                qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0) : 0u;
-                qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0 + 4) : 0u;
+                if constexpr (NT == 1) {   // group of at most 8 heads: rows 8..15 are padding
+                    qa[kk][1] = 0u;
+                    qa[kk][3] = 0u;
+                } else {
+                    qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0) : 0u;
+                    qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0 + 4) : 0u;
+                }
             }
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt)
@@ -398,6 +403,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         const uint32_t kbase = ring_addr + stage * Sh::STAGE_BYTES;
         const uint32_t vbase = kbase + Sh::TILE_BYTES;
 
+        // ---- pull the block's K and V fragments into registers, then hand the
+        // slot straight back to the TMA engine: the slot is held for the
+        // ldmatrix reads only, not for the whole block's arithmetic ----
+        uint32_t kf[D / 16][4], vf[D / 16][4];
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int chunk = ((kk & 3) << 1) + (mi & 1);
+            const uint32_t off = (kk >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
+            ldsm_x4(kbase + off, kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
+            ldsm_x4_t(vbase + off, vf[kk][0], vf[kk][1], vf[kk][2], vf[kk][3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (i + STAGES < n) {
+            issue(stage, pending);
+            if (i + STAGES + 1 < n) {
+                advance_producer(i + STAGES);
+                pending = table_entry();
+            }
+        }
+
         // ---- S = Q K^T over the 16 tokens of this block ----
         float sacc[2][4];
 #pragma unroll
@@ -406,12 +432,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const int chunk = ((kk & 3) << 1) + (mi & 1);
-            const uint32_t addr = kbase + (kk >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
-            uint32_t b00, b01, b10, b11;
-            ldsm_x4(addr, b00, b01, b10, b11);
-            mma_16816<T>(sacc[0], qa[kk], b00, b01);
-            mma_16816<T>(sacc[1], qa[kk], b10, b11);
+            mma_16816<T>(sacc[0], qa[kk], kf[kk][0], kf[kk][1]);
+            mma_16816<T>(sacc[1], qa[kk], kf[kk][2], kf[kk][3]);
         }
 
         // ---- mask, online softmax (base 2) ----
@@ -446,19 +468,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             l_run[pn] = l_run[pn] * alpha[pn] + rs;
         }
 
-        // rows beyond the context may hold anything: zero them in V so that
-        // 0-weight x garbage cannot reach the accumulator
+        // tokens beyond the context may hold anything (even NaN): clear their
+        // V values in the fragments so 0-weight x garbage cannot reach the
+        // accumulator.  Fragment registers 0/1 hold tokens 2*t4 (low half)
+        // and 2*t4+1 (high half); registers 2/3 the same tokens + 8.
         if (lim < 16) {
-            const int bad_rows = 16 - lim;
-            for (int idx = lane; idx < bad_rows * 8 * Sh::HALVES; idx += 32) {
-                const int hf = idx / (bad_rows * 8);
-                const int rem = idx - hf * bad_rows * 8;
-                const int row = lim + (rem >> 3);
-                uint4 *dst = reinterpret_cast<uint4 *>(wring + stage * Sh::STAGE_BYTES + Sh::TILE_BYTES +
-                                                       hf * Sh::HALF_BYTES + row * 128 + ((rem & 7) << 4));
-                *dst = make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t m01 = (2 * t4 < lim ? 0x0000ffffu : 0u) | (2 * t4 + 1 < lim ? 0xffff0000u : 0u);
+            const uint32_t m23 = (2 * t4 + 8 < lim ? 0x0000ffffu : 0u) | (2 * t4 + 9 < lim ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                vf[mt][0] &= m01;
+                vf[mt][1] &= m01;
+                vf[mt][2] &= m23;
+                vf[mt][3] &= m23;
             }
-            __syncwarp();
         }
 
         // ---- rescale the accumulator, O^T += V^T P^T ----
@@ -482,25 +505,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         }
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
-            const int chunk = ((mt & 3) << 1) + (mi & 1);
-            const uint32_t addr = vbase + (mt >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
-            uint32_t a[4];
-            ldsm_x4_t(addr, a[0], a[1], a[2], a[3]);
 #pragma unroll
             for (int pn = 0; pn < NT; ++pn) {
-                mma_16816<T>(acc[mt][pn], a, pb0[pn][0], pb1[pn][0]);
-                mma_16816<T>(acc[mt][pn], a, pb0[pn][1], pb1[pn][1]);
-            }
-        }
-
-        // release the slot to the TMA engine and refill it
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (i + STAGES < n) {
-            issue(stage, pending);
-            if (i + STAGES + 1 < n) {
-                advance_producer(i + STAGES);
-                pending = table_entry();
+                mma_16816<T>(acc[mt][pn], vf[mt], pb0[pn][0], pb1[pn][0]);
+                mma_16816<T>(acc[mt][pn], vf[mt], pb0[pn][1], pb1[pn][1]);
             }
         }
 
