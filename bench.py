@@ -67,7 +67,8 @@ def prefill_flops(ctx, q_lens, Hq, d):
     head, key)."""
     total = 0
     for c, q in zip(ctx, q_lens):
-        prior = int(c) - int(q)
+        q = int(q)
+        prior = int(c) - q
         keys = q * prior + q * (q + 1) // 2
         total += 4 * Hq * d * keys
     return total

@@ -63,6 +63,25 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
+int encode_tiled_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                     const uint32_t *box) {
+    auto fn = get_encode_fn();
+    if (!fn) return cuda_fail_driver(-1, "cuTensorMapEncodeTiled lookup");
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cuda_fail_driver((int)r, "cuTensorMapEncodeTiled");
+    return PKV_OK;
+}
+
 int encode_cache_map(CUtensorMap *map, const void *base, int num_blocks, int num_kv_heads, int block_size,
                      int head_dim) {
     auto fn = get_encode_fn();

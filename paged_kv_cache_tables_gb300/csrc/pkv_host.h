@@ -26,6 +26,11 @@ int current_sm_count(int *num_sms);
 int encode_cache_map(CUtensorMap *map, const void *base, int num_blocks, int num_kv_heads,
                      int block_size, int head_dim);
 
+// Generic 2..5-D tiled TMA descriptor over 16-bit elements with 128-byte
+// swizzle; strides in bytes for dims 1..rank-1.  Out-of-range boxes read 0.
+int encode_tiled_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                     const uint32_t *box);
+
 inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace pkv

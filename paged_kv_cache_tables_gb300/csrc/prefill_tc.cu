@@ -1,0 +1,427 @@
+// K4 on the 5th-generation tensor cores: paged prefill attention for chunked
+// prefill with tcgen05.mma, accumulators in tensor memory.
+//
+// What is computed: "Continuous Batching" (infra.pidoku.co.in) §5 "Mixed
+// batching (prefill + decode in one step)": chunk c's query row i sits at
+// position ctx_c - q_len_c + i and attends every key at or before it, the
+// keys and values gathered through the sequence's block table ("Project 17",
+// Step 6).
+//
+// One CTA per (chunk, tile of 128 / G query tokens, KV head); the G query
+// heads that share the KV head are packed into the 128 MMA rows
+// (row = token * G + head), so each K/V tile feeds the whole group.
+// Warp roles:
+//   warp 0   TMA producer: the query tile once (3-D box, 128-byte swizzle),
+//            then K and V tiles of 128 keys = 8 pages of 16, each page a 2-D
+//            box addressed through the block table, into a 2-stage ring;
+//   warp 1   allocates 512 tensor-memory columns and issues the MMAs from one
+//            thread: S_j = Q K_j^T into one of two S buffers, then
+//            O += P_j V_j (P as rounded bf16/fp16 + its rounding residual);
+//   warps 2-5  softmax, one query row per thread (the tensor-memory lane of
+//            the row): read S_j, causal mask, running max in base 2 with lazy
+//            rescaling of O (only when the max grows by more than 2^8), write
+//            P_j to shared memory in the MMA's swizzled K-major layout.
+// S_{j+1} runs on the tensor core while the softmax threads work on S_j.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "pkv.h"
+#include "pkv_device.cuh"
+#include "pkv_host.h"
+#include "pkv_tc.cuh"
+
+namespace pkv {
+
+constexpr int kTcThreads = 192;
+constexpr int kTcRows = 128;    // MMA rows = (token, head) pairs per CTA
+constexpr int kTcKeys = 128;    // keys per K/V tile
+constexpr int kTcStages = 2;
+constexpr uint64_t kTcWaitNs = 2000000000ull;
+constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256, 256 + D)
+
+struct PrefillTcParams {
+    void *out;
+    const int32_t *cu_seqlens;
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    int *dev_status;
+    int S, max_blocks, num_blocks, Hq, Hkv, G;
+    int rtok, tiles_per_seq;
+    float scale_log2;
+    int out_dtype;
+};
+
+template <int D>
+struct TcShape {
+    static constexpr int HALVES = D / 64;
+    static constexpr int Q_HALF = kTcRows * 128;            // 128 rows x 64 columns
+    static constexpr int Q_BYTES = HALVES * Q_HALF;
+    static constexpr int KV_HALF = kTcKeys * 128;           // 128 keys x 64 columns
+    static constexpr int K_BYTES = HALVES * KV_HALF;
+    static constexpr int STAGE_BYTES = 2 * K_BYTES;         // K then V
+    static constexpr int P_HALF = kTcRows * 128;            // 128 rows x 64 keys
+    static constexpr int P_BYTES = 2 * P_HALF;              // 128 rows x 128 keys
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+    static constexpr int OFF_PH = OFF_KV + kTcStages * STAGE_BYTES;
+    static constexpr int OFF_PL = OFF_PH + P_BYTES;
+    static constexpr int OFF_BAR = OFF_PL + P_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_prefill_tc_kernel(const PrefillTcParams p, const __grid_constant__ CUtensorMap tk,
+                            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq) {
+    using Sh = TcShape<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::OFF_BAR);
+    uint64_t *q_full = bars + 0;
+    uint64_t *kv_full = bars + 1;     // [2]
+    uint64_t *kv_empty = bars + 3;    // [2]
+    uint64_t *s_full = bars + 5;      // [2]
+    uint64_t *s_free = bars + 7;      // [2]
+    uint64_t *p_full = bars + 9;
+    uint64_t *o_done = bars + 10;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int Hkv = p.Hkv, G = p.G;
+    const int h = blockIdx.x % Hkv;
+    const int rest = blockIdx.x / Hkv;
+    const int tile = p.tiles_per_seq - 1 - rest % p.tiles_per_seq;
+    const int c = rest / p.tiles_per_seq;
+    const int q0 = __ldg(p.cu_seqlens + c);
+    const int q_len = __ldg(p.cu_seqlens + c + 1) - q0;
+    const int ctx = __ldg(p.context_lens + c);
+    if (q_len < 0 || q_len > ctx) {
+        if (tid == 0 && tile == 0) set_status(p.dev_status, PKV_DEV_BAD_CHUNK);
+        return;
+    }
+    if (ctx > p.max_blocks * 16) {
+        if (tid == 0 && tile == 0) set_status(p.dev_status, PKV_DEV_BAD_CONTEXT);
+        return;
+    }
+    const int i0 = tile * p.rtok;
+    if (i0 >= q_len) return;
+    const int ntok = min(p.rtok, q_len - i0);
+    const int prior = ctx - q_len;
+    const int ntiles = (prior + i0 + ntok - 1) / kTcKeys + 1;
+    const int nblk = (ctx + 15) / 16;
+
+    if (tid == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kTcStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&s_full[s], 1);
+            mbar_init(&s_free[s], 128);
+        }
+        mbar_init(p_full, 128);
+        mbar_init(o_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sbase = smem_addr(sm);
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            const int qrows = G * p.rtok;
+            mbar_arrive_expect_tx(q_full, (uint32_t)(Sh::HALVES * qrows * 128));
+#pragma unroll
+            for (int hf = 0; hf < Sh::HALVES; ++hf)
+                tc::tma_load_3d(sm + Sh::OFF_Q + hf * Sh::Q_HALF, &tq, hf * 64, h * G, q0 + i0, q_full);
+            const uint64_t policy = l2_policy_evict_first();
+            const int32_t *row = p.block_tables + (int64_t)c * p.max_blocks;
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j % kTcStages;
+                if (j >= kTcStages &&
+                    !mbar_wait(&kv_empty[st], (uint32_t)(((j - kTcStages) / kTcStages) & 1), kTcWaitNs)) {
+                    set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+                    break;
+                }
+                mbar_arrive_expect_tx(&kv_full[st], Sh::STAGE_BYTES);
+                uint8_t *kd = sm + Sh::OFF_KV + st * Sh::STAGE_BYTES;
+                for (int pg = 0; pg < kTcKeys / 16; ++pg) {
+                    const int page = j * (kTcKeys / 16) + pg;
+                    int y = p.num_blocks * Hkv * 16;             // past the pool: zero fill
+                    if (page < nblk) {
+                        const int blk = __ldg(row + page);
+                        if (blk >= 0 && blk < p.num_blocks)
+                            y = (blk * Hkv + h) * 16;
+                        else
+                            set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                    }
+#pragma unroll
+                    for (int hf = 0; hf < Sh::HALVES; ++hf) {
+                        tma_load_2d(kd + hf * Sh::KV_HALF + pg * 2048, &tk, hf * 64, y, &kv_full[st], policy);
+                        tma_load_2d(kd + Sh::K_BYTES + hf * Sh::KV_HALF + pg * 2048, &tv, hf * 64, y, &kv_full[st],
+                                    policy);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+            constexpr uint32_t idesc_s = tc::idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
+            constexpr uint32_t idesc_o = tc::idesc_f16(kBf16, false, true, kTcRows, D);
+            bool ok = mbar_wait(q_full, 0, kTcWaitNs);
+            for (int j = 0; ok && j <= ntiles; ++j) {
+                if (j < ntiles) {
+                    const int st = j % kTcStages, sb = j & 1;
+                    ok = mbar_wait(&kv_full[st], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
+                    if (ok && j >= 2) ok = mbar_wait(&s_free[sb], (uint32_t)(((j - 2) / 2) & 1), kTcWaitNs);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t kb = sbase + Sh::OFF_KV + st * Sh::STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * Sh::Q_HALF + (kk & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(sbase + Sh::OFF_Q + off, 16, 1024);
+                        const uint64_t b = tc::smem_desc_sw128(kb + (kk >> 2) * Sh::KV_HALF + (kk & 3) * 32, 16, 1024);
+                        tc::mma_f16_ss(tmem + sb * kTcKeys, a, b, idesc_s, kk > 0);
+                    }
+                    tc::mma_commit(&s_full[sb]);
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, st = jj % kTcStages;
+                    ok = mbar_wait(p_full, (uint32_t)(jj & 1), kTcWaitNs);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t vb = sbase + Sh::OFF_KV + st * Sh::STAGE_BYTES + Sh::K_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                        const uint32_t poff = (kk >> 2) * Sh::P_HALF + (kk & 3) * 32;
+                        const uint64_t bv = tc::smem_desc_sw128(vb + kk * 2048, Sh::KV_HALF, 1024);
+                        const uint64_t ah = tc::smem_desc_sw128(sbase + Sh::OFF_PH + poff, 16, 1024);
+                        const uint64_t al = tc::smem_desc_sw128(sbase + Sh::OFF_PL + poff, 16, 1024);
+                        tc::mma_f16_ss(tmem + 2 * kTcKeys, ah, bv, idesc_o, jj > 0 || kk > 0);
+                        tc::mma_f16_ss(tmem + 2 * kTcKeys, al, bv, idesc_o, true);
+                    }
+                    tc::mma_commit(o_done);
+                    tc::mma_commit(&kv_empty[st]);
+                }
+            }
+            if (!ok) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+        }
+    } else {
+        // ---------------- softmax: one row per thread ----------------
+        const int lane_base = 32 * (warp & 3);          // tensor-memory lanes this warp may touch
+        const int r = lane_base + lane;                 // MMA row
+        const int tok = r / G, head = r - tok * G;
+        const bool valid = tok < ntok;
+        const int pos = valid ? prior + i0 + tok : ctx - 1;   // padding rows see every key
+        const uint32_t trow = tmem + ((uint32_t)lane_base << 16);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int sb = j & 1, st = j % kTcStages;
+            ok = mbar_wait(&s_full[sb], (uint32_t)((j / 2) & 1), kTcWaitNs) &&
+                 mbar_wait(&kv_full[st], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
+            if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+            float s[kTcKeys];
+#pragma unroll
+            for (int cc = 0; cc < kTcKeys / 32; ++cc) {
+                float v[32];
+                tc::tmem_ld32(trow + sb * kTcKeys + cc * 32, v);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[cc * 32 + e] = v[e];
+            }
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            tc::mbar_arrive_cta(&s_free[sb]);
+
+            const int key0 = j * kTcKeys;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < kTcKeys; ++e) {
+                s[e] = key0 + e <= pos ? s[e] * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, s[e]);
+            }
+            const bool first = m_used == -INFINITY;
+            const float m_new = fmaxf(m_used, mx);
+            const bool rescale = !first && m_new > m_used + 8.f;
+            if (j >= 1) {
+                ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1), kTcWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after_sync();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float alpha = rescale ? exp2_approx(m_used - m_new) : 1.f;
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    float v[32];
+                    tc::tmem_ld32(trow + 2 * kTcKeys + cc * 32, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] *= alpha;
+                    tc::tmem_st32(trow + 2 * kTcKeys + cc * 32, v);
+                }
+                tc::tmem_wait_st();
+                l *= alpha;
+            }
+            if (first || rescale) m_used = m_new;
+
+            // P = 2^(x - m_used) as (rounded, residual) 16-bit pairs, row r of
+            // two K-major 128-byte-swizzled tiles of 128 rows x 64 keys
+#pragma unroll
+            for (int ch = 0; ch < kTcKeys / 8; ++ch) {
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = exp2_approx(s[ch * 8 + 2 * e] - m_used);
+                    const float b = exp2_approx(s[ch * 8 + 2 * e + 1] - m_used);
+                    l += a + b;
+                    pack2_split<T>(a, b, hi[e], lo[e]);
+                }
+                const uint32_t off = (ch >> 3) * Sh::P_HALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                *reinterpret_cast<uint4 *>(sm + Sh::OFF_PH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4 *>(sm + Sh::OFF_PL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+            // keys at or past the context in the last stored page may hold
+            // anything: clear those V rows so 0 x garbage cannot reach O
+            const int zlo = max(ctx - key0, 0), zhi = min(kTcKeys, nblk * 16 - key0);
+            if (r >= zlo && r < zhi) {
+                uint8_t *vrow = sm + Sh::OFF_KV + st * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
+#pragma unroll
+                for (int hf = 0; hf < Sh::HALVES; ++hf)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        *reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            tc::mbar_arrive_cta(p_full);
+        }
+        if (ok) {
+            ok = mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), kTcWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc::fence_after_sync();
+            const float inv = 1.f / l;
+            const int64_t ob = ((int64_t)(q0 + i0 + tok) * p.Hq + (int64_t)h * G + head) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                float v[32];
+                tc::tmem_ld32(trow + 2 * kTcKeys + cc * 32, v);
+                tc::tmem_wait_ld();
+                if (valid) {
+                    if (p.out_dtype == PKV_DTYPE_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out) + ob + cc * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(v[4 * e] * inv, v[4 * e + 1] * inv, v[4 * e + 2] * inv,
+                                                 v[4 * e + 3] * inv);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<T *>(p.out) + ob + cc * 32);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(pack2<T>(v[8 * e] * inv, v[8 * e + 1] * inv),
+                                                pack2<T>(v[8 * e + 2] * inv, v[8 * e + 3] * inv),
+                                                pack2<T>(v[8 * e + 4] * inv, v[8 * e + 5] * inv),
+                                                pack2<T>(v[8 * e + 6] * inv, v[8 * e + 7] * inv));
+                    }
+                }
+            }
+        } else {
+            set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// 3-D TMA descriptor over q viewed as [total_q][Hq][head_dim]: box of 64
+// columns x G heads x rtok tokens, 128-byte swizzle; rows past total_q read 0.
+static int encode_q_map(CUtensorMap *map, const void *q, int total_q, int Hq, int head_dim, int G, int rtok) {
+    const uint64_t dims[3] = {(uint64_t)head_dim, (uint64_t)Hq, (uint64_t)total_q};
+    const uint64_t strides[2] = {(uint64_t)head_dim * 2, (uint64_t)Hq * head_dim * 2};
+    const uint32_t box[3] = {64, (uint32_t)G, (uint32_t)rtok};
+    return encode_tiled_map(map, q, 3, dims, strides, box);
+}
+
+template <typename T, int D>
+int launch_prefill_tc(const PrefillTcParams &prm, const CUtensorMap &tk, const CUtensorMap &tv,
+                      const CUtensorMap &tq, int grid, cudaStream_t stream) {
+    using Sh = TcShape<D>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
+        attr_set = true;
+    }
+    paged_prefill_tc_kernel<T, D><<<grid, kTcThreads, Sh::SMEM_BYTES, stream>>>(prm, tk, tv, tq);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}
+
+int prefill_tc(void *out, const void *q, const int32_t *cu_seqlens, int num_seqs, int max_q_len, int total_q,
+               const void *k_cache, const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+               const int32_t *context_lens, int num_blocks, int Hq, int Hkv, int head_dim, float scale, int dtype,
+               int out_dtype, int *dev_status, cudaStream_t stream) {
+    const int G = Hq / Hkv;
+    const int rtok = kTcRows / G;
+    const int tiles = (max_q_len + rtok - 1) / rtok;
+    const int64_t grid64 = (int64_t)num_seqs * tiles * Hkv;
+    if (grid64 >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
+    if (!aligned(out, 16)) return PKV_ERR_INVALID_ARG;
+    CUtensorMap tk, tv, tq;
+    int rc = encode_cache_map(&tk, k_cache, num_blocks, Hkv, 16, head_dim);
+    if (rc != PKV_OK) return rc;
+    rc = encode_cache_map(&tv, v_cache, num_blocks, Hkv, 16, head_dim);
+    if (rc != PKV_OK) return rc;
+    rc = encode_q_map(&tq, q, total_q, Hq, head_dim, G, rtok);
+    if (rc != PKV_OK) return rc;
+    PrefillTcParams prm;
+    prm.out = out;
+    prm.cu_seqlens = cu_seqlens;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.dev_status = dev_status;
+    prm.S = num_seqs;
+    prm.max_blocks = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.G = G;
+    prm.rtok = rtok;
+    prm.tiles_per_seq = tiles;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+    prm.out_dtype = out_dtype;
+    const int grid = (int)grid64;
+    if (dtype == PKV_DTYPE_BF16)
+        return head_dim == 128 ? launch_prefill_tc<__nv_bfloat16, 128>(prm, tk, tv, tq, grid, stream)
+                               : launch_prefill_tc<__nv_bfloat16, 64>(prm, tk, tv, tq, grid, stream);
+    return head_dim == 128 ? launch_prefill_tc<__half, 128>(prm, tk, tv, tq, grid, stream)
+                           : launch_prefill_tc<__half, 64>(prm, tk, tv, tq, grid, stream);
+}
+
+}  // namespace pkv
