@@ -268,7 +268,8 @@ def run_mixed(args):
     import torch
     import paged_kv_cache_tables_gb300 as pkv
     from synth import make_step
-    st = make_step("mixed")
+    over = {"n_chunks": args.mixed_chunks} if args.mixed_chunks else {}
+    st = make_step("mixed", **over)
     p = st.n_prefill
     t1 = int(st.cu_seqlens[p])
     q = to_dev_bits(st.q, st.dtype)
@@ -449,11 +450,19 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed prefill + decode step")
     ap.add_argument("--mixed-steps", type=int, default=50)
+    ap.add_argument("--mixed-chunks", type=int, default=0, help="override the prefill chunk count (profiling)")
+    ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
     ap.add_argument("--seqs", type=int, default=0, help="override the sequence count (profiling cases)")
     ap.add_argument("--pool", type=int, default=0, help="override the pool size in blocks (profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.only_mixed:
+        import torch
+        torch.cuda.set_device(0)
+        args.warmup = max(args.warmup, 3)
+        print(json.dumps({"mixed_step": run_mixed(args)}))
+        return
     if args.impl == "reference":
         # each reference step is a bounded oracle sample sized so the run takes a few minutes
         run_reference(args)

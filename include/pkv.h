@@ -291,6 +291,8 @@ typedef struct pkv_step_meta {
     const int64_t *slot_mapping;  /* [num_tokens] cache slot of every new token */
     const int64_t *token_rids;    /* [num_tokens] request id of every new token */
     const int32_t *token_pos;     /* [num_tokens] position of every new token in its request */
+    int num_finished;             /* requests retired at the end of this step */
+    const int64_t *finished_rids; /* [num_finished] their ids, in scheduling order */
 } pkv_step_meta;
 
 typedef struct pkv_sched_stats {

@@ -103,6 +103,7 @@ class StepMeta:
     token_rids: np.ndarray         # int64 [T]
     token_pos: np.ndarray          # int32 [T]
     num_prefill: int
+    finished_rids: np.ndarray = None   # int64: requests retired at the end of this step
 
 
 def cdiv(a: int, b: int) -> int:
@@ -190,6 +191,7 @@ class Scheduler:
         self.sum_running += len(self.running)
         meta = self._emit(scheduled) if scheduled else None
         # the iteration ran: advance, emit a token where the context caught up, retire
+        done = []
         for r, q in scheduled:
             r.num_computed += q
             if r.num_computed == r.length:
@@ -202,6 +204,9 @@ class Scheduler:
                     r.finish_step = self.step_no
                     self.running.remove(r)
                     self.finished.append(r)
+                    done.append(r.rid)
+        if meta is not None:
+            meta.finished_rids = np.array(done, dtype=np.int64)
         self.step_no += 1
         return meta
 

@@ -38,7 +38,8 @@ class StepMeta(ctypes.Structure):
                 ("q_lens", ctypes.POINTER(ctypes.c_int32)), ("context_lens", ctypes.POINTER(ctypes.c_int32)),
                 ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)), ("block_tables", ctypes.POINTER(ctypes.c_int32)),
                 ("slot_mapping", ctypes.POINTER(ctypes.c_int64)), ("token_rids", ctypes.POINTER(ctypes.c_int64)),
-                ("token_pos", ctypes.POINTER(ctypes.c_int32))]
+                ("token_pos", ctypes.POINTER(ctypes.c_int32)), ("num_finished", ctypes.c_int),
+                ("finished_rids", ctypes.POINTER(ctypes.c_int64))]
 
 
 class SchedConfig(ctypes.Structure):
@@ -280,6 +281,8 @@ class Scheduler:
             "block_tables": arr(m.block_tables, S * MB, np.int32).reshape(S, MB),
             "slot_mapping": arr(m.slot_mapping, T, np.int64), "token_rids": arr(m.token_rids, T, np.int64),
             "token_pos": arr(m.token_pos, T, np.int32), "num_prefill": m.num_prefill,
+            "finished_rids": arr(m.finished_rids, m.num_finished, np.int64) if m.num_finished else
+            np.zeros(0, np.int64),
         }
 
     def stats(self):

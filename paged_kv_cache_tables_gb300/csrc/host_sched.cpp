@@ -145,7 +145,7 @@ struct pkv_sched {
     pkv_sched_stats stats{};
 
     // emitted arrays (valid until the next step)
-    std::vector<int64_t> seq_rids, slot_mapping, token_rids;
+    std::vector<int64_t> seq_rids, slot_mapping, token_rids, finished_rids;
     std::vector<int32_t> q_lens, context_lens, cu_seqlens, block_tables, token_pos;
 
     void preempt(int idx) {
@@ -267,6 +267,7 @@ int pkv_sched::step(pkv_step_meta *out) {
         out->max_blocks = max_blocks;
     }
     // 3. the iteration ran: account tokens, emit, retire
+    finished_rids.clear();
     for (auto &x : scheduled) {
         Request &r = reqs[x.first];
         r.num_computed += x.second;
@@ -281,9 +282,12 @@ int pkv_sched::step(pkv_step_meta *out) {
                 r.state = FINISHED;
                 running.erase(std::find(running.begin(), running.end(), x.first));
                 ++stats.finished;
+                finished_rids.push_back(r.rid);
             }
         }
     }
+    out->num_finished = (int)finished_rids.size();
+    out->finished_rids = finished_rids.data();
     ++stats.steps;
     return (int)scheduled.size();
 }

@@ -70,6 +70,7 @@ def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fai
                       "token_rids", "token_pos"]:
                 assert np.array_equal(getattr(a, k), b[k]), "step %d field %s" % (step, k)
             assert a.num_prefill == b["num_prefill"]
+            assert np.array_equal(a.finished_rids, b["finished_rids"]), "step %d finished" % step
         sa, sb = py.stats(), nat.stats()
         for k in ["free_blocks", "running", "waiting", "finished", "preemptions", "sum_running"]:
             assert sa[k] == sb[k], "step %d stat %s" % (step, k)
