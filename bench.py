@@ -332,6 +332,83 @@ def run_mixed(args):
     }
 
 
+def run_trace_bench(args):
+    """The continuous-batching trace: 1000 requests, Poisson(20) arrivals per
+    step, prompts lognormal (mean 512, sigma 1, clipped 8..4096), outputs
+    geometric (mean 256), max batch 256, 8192-token budget, 512-token prefill
+    chunks, a pool of 200k 16-token blocks, preemption by recompute; every
+    step runs append + prefill chunks + decode for 32 layers of the 8B shape.
+    The 32 layers rotate over 4 physical caches (52 GB) so the trace fits in
+    HBM; every layer still streams its full context."""
+    import torch
+    from paged_kv_cache_tables_gb300.engine import PagedEngine, run_trace
+    from synth import SEEDS
+    from synth.trace import make_fill, make_requests, pick_rows
+    torch.cuda.set_device(0)
+    seed = SEEDS["trace"]
+    n, L, R, NB = args.trace_requests, args.trace_layers, args.trace_caches, args.trace_pool
+    arrival, prompt, eos = make_requests(seed, n=n)
+    eng = PagedEngine(NB, num_layers=L, num_caches=R, initial_order=np.random.default_rng(seed).permutation(NB))
+    rng = np.random.default_rng(seed + 1)
+    clk = ClockSampler(0)
+    with clk:
+        res = run_trace(eng, arrival, prompt, eos, max_tokens=4096, fill=make_fill(), sample_every=50,
+                        pick=lambda info: pick_rows(info, rng, n_decode=1, n_prefill=1))
+    if int(eng.status.item()) != 0:
+        raise RuntimeError("device status %d in the trace" % int(eng.status.item()))
+    st = eng.sched.stats()
+    steps = res["steps"]
+    Hq, Hkv, d = 32, 8, 128
+    dec_tokens = pre_keys = kv_bytes = 0
+    for s in steps:
+        ctx, ql = s["context_lens"], s["q_lens"]
+        dmask = ql == 1
+        dec_tokens += int(ctx[dmask].sum())
+        for c, q in zip(ctx[~dmask], ql[~dmask]):
+            c, q = int(c), int(q)
+            pre_keys += q * (c - q) + q * (q + 1) // 2
+        kv_bytes += int(ctx.sum()) * 2 * Hkv * d * 2
+    gen = sum(min(int(eos[i]), 4096, 8192 - int(prompt[i])) for i in range(n))
+    lat = np.array([res["finish_step"][i] - int(arrival[i]) for i in range(n)])
+    dev_s = res["stream_ms"] / 1e3
+    # oracle check of the sampled layer-0 rows, and the oracle's own time on them
+    import oracle
+    from oracle.trace_check import layer0_row
+    worst, checked, t_or, keys = 0.0, 0, 0.0, 0
+    for rows, vals in res["samples"]:
+        for (row, rid, pos), got in zip(rows, vals.numpy()):
+            t0 = time.perf_counter()
+            ref = layer0_row(rid, pos, Hq, Hkv, d)
+            t_or += time.perf_counter() - t0
+            keys += pos + 1
+            err = np.abs(got.astype(np.float64) - ref)
+            bound = np.maximum(2e-3, np.exp2(np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 8) + 1e-4)
+            if np.any(err > bound):
+                raise RuntimeError("trace sample rid %d pos %d off by %g" % (rid, pos, float(err.max())))
+            worst = max(worst, float(err.max()))
+            checked += 1
+    line = {
+        "metric": "continuous-batching trace: output tokens/s and aggregate paged-attention KV GB/s",
+        "workload": "trace: %d requests, Poisson(20)/step, prompt lognormal mean 512 clip 8-4096, output geometric "
+                    "mean 256, max batch 256, budget 8192, chunk 512, pool %d blocks, %d layers (8B shape) over %d "
+                    "physical caches" % (n, NB, L, R),
+        "engine_steps": len(steps), "wall_s": round(res["wall_s"], 3), "stream_s": round(dev_s, 3),
+        "host_sched_ms_per_step": round(st["host_ms"] / max(1, st["steps"]), 4),
+        "host_ms_per_step": round(eng.host_ms / max(1, len(steps)), 4),
+        "output_tokens": gen, "output_tokens_per_s": round(gen / res["wall_s"], 1),
+        "attended_tokens_per_s": round((dec_tokens + pre_keys) * L / res["wall_s"], 1),
+        "kv_gbs": round(kv_bytes * L / res["wall_s"] / 1e9, 1),
+        "preemptions": st["preemptions"], "preemption_rate": round(st["preemptions"] / max(1, st["steps"]), 4),
+        "avg_running_batch": round(st["sum_running"] / max(1, st["steps"]), 2),
+        "latency_steps_p50": float(np.percentile(lat, 50)), "latency_steps_p99": float(np.percentile(lat, 99)),
+        "upload_bytes_per_step": int(eng.upload_bytes / max(1, len(steps))),
+        "oracle_check": {"rows": checked, "max_abs_err": worst, "every": "50th engine step, layer 0",
+                         "oracle_s": round(t_or, 2), "oracle_keys_per_s": round(keys / max(t_or, 1e-9), 1)},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line))
+
+
 def run_pkv(args):
     import torch
     import paged_kv_cache_tables_gb300 as pkv
@@ -452,11 +529,19 @@ def main():
     ap.add_argument("--mixed-steps", type=int, default=50)
     ap.add_argument("--mixed-chunks", type=int, default=0, help="override the prefill chunk count (profiling)")
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace"])
+    ap.add_argument("--trace-requests", type=int, default=1000)
+    ap.add_argument("--trace-layers", type=int, default=32)
+    ap.add_argument("--trace-caches", type=int, default=4)
+    ap.add_argument("--trace-pool", type=int, default=200000)
     ap.add_argument("--seqs", type=int, default=0, help="override the sequence count (profiling cases)")
     ap.add_argument("--pool", type=int, default=0, help="override the pool size in blocks (profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "trace":
+        run_trace_bench(args)
+        return
     if args.only_mixed:
         import torch
         torch.cuda.set_device(0)

@@ -1,0 +1,28 @@
+"""Oracle values for sampled rows of the continuous-batching trace.
+
+TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).  Rebuilds, from the
+counter-based generator in synth.trace, the K/V rows that layer 0's cache
+must hold for one request and runs the FP64 oracle for one query position
+over keys 0..pos (for a decode row pos = ctx - 1; for a prefill-chunk row the
+causal bound is the row's own position).
+"""
+import numpy as np
+
+from synth import NAN_BITS
+from synth.trace import kv_tag, q_tag, token_rows
+
+from . import decode
+
+
+def layer0_row(rid, pos, Hq, Hkv, d, dtype="bf16"):
+    n = pos + 1
+    nb = -(-n // 16)
+    ks = token_rows(np.full(n, rid), np.arange(n), kv_tag(0, "k"), Hkv * d, dtype).reshape(n, Hkv, d)
+    vs = token_rows(np.full(n, rid), np.arange(n), kv_tag(0, "v"), Hkv * d, dtype).reshape(n, Hkv, d)
+    kc = np.full((nb * 16, Hkv, d), NAN_BITS[dtype], np.uint16)
+    vc = kc.copy()
+    kc[:n], vc[:n] = ks, vs
+    kc = kc.reshape(nb, 16, Hkv, d).transpose(0, 2, 1, 3).copy()
+    vc = vc.reshape(nb, 16, Hkv, d).transpose(0, 2, 1, 3).copy()
+    q = token_rows(np.array([rid]), np.array([pos]), q_tag(0), Hq * d, dtype).reshape(1, Hq, d)
+    return decode(q, kc, vc, np.arange(nb, dtype=np.int32)[None], np.array([n], np.int32), dtype)[0]

@@ -1,0 +1,172 @@
+"""A minimal engine loop over the library: the native scheduler builds each
+step's metadata, one upload carries it to the device, and every layer runs
+append -> prefill chunks -> decode on the paged caches.
+
+Orchestration only: the scheduling rules live in libpkv.so's scheduler and
+all arithmetic in its kernels.  Per-layer Q/K/V rows of the step's new tokens
+come from a caller-supplied `fill(layer, cache_id, q, k, v, token_rids,
+token_pos)` (the model would produce them; benchmarks and tests pass a
+synthetic generator).
+
+Layers share one block table per sequence ("tiny-vllm part 7" keeps one per
+layer and re-uploads all of them every layer; here the step's metadata goes
+up once).  `num_caches` physical K/V caches are rotated over the layers
+(layer l uses cache l % num_caches) so that a many-layer trace fits in HBM;
+every layer still streams its own full context.
+"""
+import ctypes
+import time
+
+import numpy as np
+
+from . import _binding as B
+
+
+class PagedEngine:
+    def __init__(self, num_blocks, num_layers=32, num_caches=4, Hq=32, Hkv=8, d=128, dtype="bf16",
+                 max_batch=256, max_num_batched_tokens=8192, chunk=512, max_model_len=8192, initial_order=None,
+                 device="cuda"):
+        import torch
+        self.torch = torch
+        self.L, self.R = num_layers, num_caches
+        self.Hq, self.Hkv, self.d, self.bs = Hq, Hkv, d, 16
+        self.NB = num_blocks
+        self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+        self.sched = B.Scheduler(num_blocks, 16, max_batch, max_num_batched_tokens, chunk, max_model_len,
+                                 initial_order=initial_order)
+        self.max_blocks = self.sched.max_blocks
+        self.max_T = max_num_batched_tokens
+        self.max_S = max_batch
+        dev = torch.device(device)
+        shape = (num_blocks, Hkv, 16, d)
+        self.k_cache = [torch.zeros(shape, dtype=self.tdt, device=dev) for _ in range(num_caches)]
+        self.v_cache = [torch.zeros(shape, dtype=self.tdt, device=dev) for _ in range(num_caches)]
+        T, S = self.max_T, self.max_S
+        self.q = torch.empty((T, Hq, d), dtype=self.tdt, device=dev)
+        self.k = torch.empty((T, Hkv, d), dtype=self.tdt, device=dev)
+        self.v = torch.empty((T, Hkv, d), dtype=self.tdt, device=dev)
+        self.out = torch.empty((T, Hq, d), dtype=self.tdt, device=dev)
+        self.work = torch.empty(max(16, B.decode_workspace_size(S, Hq, Hkv, d)), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # one pinned staging area and one device area for the step's metadata
+        self.n_i64 = 3 * T                       # slot_mapping, token_rids, (spare)
+        self.n_i32 = T + 2 * S + 1 + S * self.max_blocks
+        # two pinned staging areas used alternately: the host may only rewrite
+        # one after the device has finished copying it (the GPU can be a step
+        # behind the host)
+        self.h_i64 = [torch.empty(self.n_i64, dtype=torch.int64).pin_memory() for _ in range(2)]
+        self.h_i32 = [torch.empty(self.n_i32, dtype=torch.int32).pin_memory() for _ in range(2)]
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.nstep = 0
+        self.d_i64 = torch.empty(self.n_i64, dtype=torch.int64, device=dev)
+        self.d_i32 = torch.empty(self.n_i32, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream()
+        self.host_ms = 0.0
+        self.upload_bytes = 0
+
+    def add(self, rid, prompt_len, max_tokens, eos_after):
+        self.sched.add(rid, prompt_len, max_tokens, eos_after)
+
+    def step(self, fill, on_layer_done=None):
+        """One engine step.  Returns None when nothing was scheduled, else a
+        dict with the step's metadata (numpy) and device views."""
+        torch = self.torch
+        t0 = time.perf_counter()
+        m = self.sched.step_raw()
+        S, T, P = m.num_seqs, m.num_tokens, m.num_prefill
+        if S == 0:
+            self.host_ms += (time.perf_counter() - t0) * 1e3
+            return None
+        MB = m.max_blocks
+        arr = lambda ptr, n: np.ctypeslib.as_array(ptr, shape=(n,))
+        # stage: i64 = [slot_mapping T][token_rids T]; i32 = [token_pos T][ctx S][cu S+1][tables S*MB]
+        buf = self.nstep & 1
+        self.nstep += 1
+        self.copied[buf].synchronize()
+        h64, h32 = self.h_i64[buf].numpy(), self.h_i32[buf].numpy()
+        h64[:T] = arr(m.slot_mapping, T)
+        h64[T:2 * T] = arr(m.token_rids, T)
+        o = 0
+        h32[o:o + T] = arr(m.token_pos, T); o += T
+        h32[o:o + S] = arr(m.context_lens, S); o += S
+        h32[o:o + S + 1] = arr(m.cu_seqlens, S + 1); o += S + 1
+        h32[o:o + S * MB] = arr(m.block_tables, S * MB); o += S * MB
+        n32 = o
+        self.d_i64[:2 * T].copy_(self.h_i64[buf][:2 * T], non_blocking=True)
+        self.d_i32[:n32].copy_(self.h_i32[buf][:n32], non_blocking=True)
+        self.copied[buf].record(self.stream)
+        self.upload_bytes += 2 * T * 8 + n32 * 4
+        slots, trids = self.d_i64[:T], self.d_i64[T:2 * T]
+        o = 0
+        tpos = self.d_i32[o:o + T]; o += T
+        ctx = self.d_i32[o:o + S]; o += S
+        cu = self.d_i32[o:o + S + 1]; o += S + 1
+        tables = self.d_i32[o:o + S * MB].view(S, MB)
+        cu_h = arr(m.cu_seqlens, S + 1)
+        t1 = int(cu_h[P])
+        max_q = int(np.diff(cu_h[:P + 1]).max()) if P else 0
+        q, k, v, out = self.q[:T], self.k[:T], self.v[:T], self.out[:T]
+        info = {"S": S, "T": T, "P": P, "t1": t1, "seq_rids": arr(m.seq_rids, S).copy(),
+                "context_lens": arr(m.context_lens, S).copy(), "cu_seqlens": cu_h.copy(),
+                "q_lens": arr(m.q_lens, S).copy(),
+                "finished": arr(m.finished_rids, m.num_finished).copy() if m.num_finished else np.zeros(0, np.int64)}
+        self.host_ms += (time.perf_counter() - t0) * 1e3
+        for layer in range(self.L):
+            cid = layer % self.R
+            fill(layer, cid, q, k, v, trids, tpos)
+            B.kv_append(k, v, slots, self.k_cache[cid], self.v_cache[cid], dev_status=self.status, stream=self.stream)
+            if P:
+                B.paged_prefill_attention(out[:t1], q[:t1], cu[:P + 1], max_q, self.k_cache[cid], self.v_cache[cid],
+                                          tables[:P], ctx[:P], dev_status=self.status, stream=self.stream)
+            if S > P:
+                B.paged_decode_attention(out[t1:], q[t1:], self.k_cache[cid], self.v_cache[cid], tables[P:], ctx[P:],
+                                         workspace=self.work, dev_status=self.status, stream=self.stream)
+            if on_layer_done is not None:
+                on_layer_done(layer, info, out)
+        return info
+
+
+def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pick=None, max_steps=1000000):
+    """Drive `engine` through a request trace: request i is added at engine
+    step arrival[i]; steps run until every request has finished.  On every
+    `sample_every`-th engine step, pick(info) names (output row, rid,
+    position) samples whose layer-0 outputs are copied back for checking.
+    Returns per-step records, finish steps, timings and the sampled rows."""
+    torch = engine.torch
+    n = len(arrival)
+    order = np.argsort(arrival, kind="stable")
+    nxt = 0
+    finish_step = {}
+    steps = []
+    samples = []
+    state = {"sample": False}
+
+    def on_layer(layer, info, out):
+        if layer == 0 and state["sample"]:
+            rows = pick(info)
+            if rows:
+                idx = torch.tensor([r[0] for r in rows], device=out.device)
+                samples.append((rows, out.index_select(0, idx).float().to("cpu")))
+
+    t_wall = time.perf_counter()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(engine.stream)
+    for step in range(max_steps):
+        while nxt < n and arrival[order[nxt]] <= step:
+            i = int(order[nxt])
+            engine.add(i, int(prompt[i]), int(max_tokens), int(eos[i]))
+            nxt += 1
+        state["sample"] = bool(sample_every) and pick is not None and len(steps) % sample_every == 0
+        info = engine.step(fill, on_layer_done=on_layer)
+        if info is not None:
+            for rid in info["finished"]:
+                finish_step[int(rid)] = step
+            steps.append({"step": step, "S": info["S"], "T": info["T"], "P": info["P"],
+                          "context_lens": info["context_lens"], "q_lens": info["q_lens"]})
+        if nxt >= n and len(finish_step) == n:
+            break
+    ev1.record(engine.stream)
+    torch.cuda.synchronize()
+    return {"steps": steps, "finish_step": finish_step, "wall_s": time.perf_counter() - t_wall,
+            "stream_ms": ev0.elapsed_time(ev1), "samples": samples}
