@@ -1,5 +1,6 @@
 // K4 on the 5th-generation tensor cores: paged prefill attention for chunked
-// prefill with tcgen05.mma, accumulators in tensor memory.
+// prefill with tcgen05.mma, accumulators and the probability tile in tensor
+// memory.
 //
 // What is computed: "Continuous Batching" (infra.pidoku.co.in) §5 "Mixed
 // batching (prefill + decode in one step)": chunk c's query row i sits at
@@ -7,21 +8,26 @@
 // keys and values gathered through the sequence's block table ("Project 17",
 // Step 6).
 //
-// One CTA per (chunk, tile of 128 / G query tokens, KV head); the G query
-// heads that share the KV head are packed into the 128 MMA rows
-// (row = token * G + head), so each K/V tile feeds the whole group.
-// Warp roles:
-//   warp 0   TMA producer: the query tile once (3-D box, 128-byte swizzle),
-//            then K and V tiles of 128 keys = 8 pages of 16, each page a 2-D
-//            box addressed through the block table, into a 2-stage ring;
-//   warp 1   allocates 512 tensor-memory columns and issues the MMAs from one
-//            thread: S_j = Q K_j^T into one of two S buffers, then
-//            O += P_j V_j (P as rounded bf16/fp16 + its rounding residual);
-//   warps 2-5  softmax, one query row per thread (the tensor-memory lane of
-//            the row): read S_j, causal mask, running max in base 2 with lazy
-//            rescaling of O (only when the max grows by more than 2^8), write
-//            P_j to shared memory in the MMA's swizzled K-major layout.
-// S_{j+1} runs on the tensor core while the softmax threads work on S_j.
+// One CTA per (chunk, pair of query tiles, KV head).  A query tile is 128 MMA
+// rows = 128 / G tokens x the G query heads that share the KV head
+// (row = token * G + head), so each K/V tile feeds the whole group; the two
+// tiles of a pair (adjacent tokens) share every K/V tile.  Warp roles:
+//   warp 0     TMA: both query tiles once (3-D boxes, 128-byte swizzle), then
+//              K and V tiles of 128 keys = 8 pages of 16 through the block
+//              table into a 2-stage ring;
+//   warp 1     allocates all 512 tensor-memory columns (S and O of each tile)
+//              and issues every MMA from one thread, ping-ponging the tiles:
+//              O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
+//              S_B = Q_B K_{j+1}^T, ...;
+//   warps 2-5  softmax of tile A, warps 6-9 of tile B, one row per thread (the
+//              tensor-memory lane of the row): two passes over S (causal mask,
+//              running max in base 2 with lazy rescaling of O when the max
+//              grows by more than 2^8), then P written back over S as fp16,
+//              which the MMA reads as its A operand straight from tensor
+//              memory.  fp16 keeps 11 significant bits of P; for bf16 inputs
+//              the tile-A warps convert each V tile to fp16 in shared memory
+//              first (exact: bf16 values carry 8 significant bits).
+// While one tile's softmax runs, the tensor core works on the other tile.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -33,12 +39,12 @@
 
 namespace pkv {
 
-constexpr int kTcThreads = 192;
-constexpr int kTcRows = 128;    // MMA rows = (token, head) pairs per CTA
+constexpr int kTcThreads = 320;
+constexpr int kTcRows = 128;    // MMA rows = (token, head) pairs per query tile
 constexpr int kTcKeys = 128;    // keys per K/V tile
 constexpr int kTcStages = 2;
 constexpr uint64_t kTcWaitNs = 2000000000ull;
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256, 256 + D)
+constexpr uint32_t kTmemCols = 512;   // tile t: S/P at 256 t, O at 256 t + 128
 
 struct PrefillTcParams {
     void *out;
@@ -47,7 +53,7 @@ struct PrefillTcParams {
     const int32_t *context_lens;
     int *dev_status;
     int S, max_blocks, num_blocks, Hq, Hkv, G;
-    int rtok, tiles_per_seq;
+    int rtok, pairs_per_seq;
     float scale_log2;
     int out_dtype;
 };
@@ -60,15 +66,23 @@ struct TcShape {
     static constexpr int KV_HALF = kTcKeys * 128;           // 128 keys x 64 columns
     static constexpr int K_BYTES = HALVES * KV_HALF;
     static constexpr int STAGE_BYTES = 2 * K_BYTES;         // K then V
-    static constexpr int P_HALF = kTcRows * 128;            // 128 rows x 64 keys
-    static constexpr int P_BYTES = 2 * P_HALF;              // 128 rows x 128 keys
-    static constexpr int OFF_Q = 0;
-    static constexpr int OFF_KV = OFF_Q + Q_BYTES;
-    static constexpr int OFF_PH = OFF_KV + kTcStages * STAGE_BYTES;
-    static constexpr int OFF_PL = OFF_PH + P_BYTES;
-    static constexpr int OFF_BAR = OFF_PL + P_BYTES;
+    static constexpr int OFF_Q = 0;                         // tile A, then tile B
+    static constexpr int OFF_KV = 2 * Q_BYTES;
+    static constexpr int OFF_BAR = OFF_KV + kTcStages * STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
 };
+
+// Eight bf16 values to fp16 (exact for |x| in the fp16 normal range, which
+// holds every bf16 with magnitude between 2^-14 and 65504).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
+    uint32_t in[4] = {x.x, x.y, x.z, x.w}, o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float lo = __uint_as_float(in[i] << 16), hi = __uint_as_float(in[i] & 0xffff0000u);
+        o[i] = pack2<__half>(lo, hi);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -81,32 +95,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *q_full = bars + 0;
     uint64_t *kv_full = bars + 1;     // [2]
     uint64_t *kv_empty = bars + 3;    // [2]
-    uint64_t *s_full = bars + 5;      // [2]
-    uint64_t *s_free = bars + 7;      // [2]
-    uint64_t *p_full = bars + 9;
-    uint64_t *o_done = bars + 10;
+    uint64_t *s_full = bars + 5;      // [tile]
+    uint64_t *p_full = bars + 7;      // [tile]
+    uint64_t *o_done = bars + 9;      // [tile]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
     const int h = blockIdx.x % Hkv;
     const int rest = blockIdx.x / Hkv;
-    const int tile = p.tiles_per_seq - 1 - rest % p.tiles_per_seq;
-    const int c = rest / p.tiles_per_seq;
+    const int pair = p.pairs_per_seq - 1 - rest % p.pairs_per_seq;   // the pairs with the most keys first
+    const int c = rest / p.pairs_per_seq;
     const int q0 = __ldg(p.cu_seqlens + c);
     const int q_len = __ldg(p.cu_seqlens + c + 1) - q0;
     const int ctx = __ldg(p.context_lens + c);
     if (q_len < 0 || q_len > ctx) {
-        if (tid == 0 && tile == 0) set_status(p.dev_status, PKV_DEV_BAD_CHUNK);
+        if (tid == 0 && pair == 0) set_status(p.dev_status, PKV_DEV_BAD_CHUNK);
         return;
     }
     if (ctx > p.max_blocks * 16) {
-        if (tid == 0 && tile == 0) set_status(p.dev_status, PKV_DEV_BAD_CONTEXT);
+        if (tid == 0 && pair == 0) set_status(p.dev_status, PKV_DEV_BAD_CONTEXT);
         return;
     }
-    const int i0 = tile * p.rtok;
+    const int i0 = pair * 2 * p.rtok;
     if (i0 >= q_len) return;
-    const int ntok = min(p.rtok, q_len - i0);
+    const int ntok = min(2 * p.rtok, q_len - i0);      // tokens of this pair (tile A first)
     const int prior = ctx - q_len;
     const int ntiles = (prior + i0 + ntok - 1) / kTcKeys + 1;
     const int nblk = (ctx + 15) / 16;
@@ -117,12 +130,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&kv_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&s_full[s], 1);
-            mbar_init(&s_free[s], 128);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], 128);
+            mbar_init(&o_done[t], 1);
         }
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -139,10 +151,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const int qrows = G * p.rtok;
-            mbar_arrive_expect_tx(q_full, (uint32_t)(Sh::HALVES * qrows * 128));
+            mbar_arrive_expect_tx(q_full, (uint32_t)(2 * Sh::HALVES * qrows * 128));
 #pragma unroll
-            for (int hf = 0; hf < Sh::HALVES; ++hf)
-                tc::tma_load_3d(sm + Sh::OFF_Q + hf * Sh::Q_HALF, &tq, hf * 64, h * G, q0 + i0, q_full);
+            for (int t = 0; t < 2; ++t)
+#pragma unroll
+                for (int hf = 0; hf < Sh::HALVES; ++hf)
+                    tc::tma_load_3d(sm + Sh::OFF_Q + t * Sh::Q_BYTES + hf * Sh::Q_HALF, &tq, hf * 64, h * G,
+                                    q0 + i0 + t * p.rtok, q_full);
             const uint64_t policy = l2_policy_evict_first();
             const int32_t *row = p.block_tables + (int64_t)c * p.max_blocks;
             for (int j = 0; j < ntiles; ++j) {
@@ -178,154 +193,162 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
             constexpr uint32_t idesc_s = tc::idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
-            constexpr uint32_t idesc_o = tc::idesc_f16(kBf16, false, true, kTcRows, D);
-            bool ok = mbar_wait(q_full, 0, kTcWaitNs);
-            for (int j = 0; ok && j <= ntiles; ++j) {
-                if (j < ntiles) {
-                    const int st = j % kTcStages, sb = j & 1;
-                    ok = mbar_wait(&kv_full[st], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
-                    if (ok && j >= 2) ok = mbar_wait(&s_free[sb], (uint32_t)(((j - 2) / 2) & 1), kTcWaitNs);
+            constexpr uint32_t idesc_o = tc::idesc_f16(false, false, true, kTcRows, D);   // P and V in fp16
+            auto issue_s = [&](int j, int t) {   // S_t = Q_t K_j^T
+                const uint32_t kb = sbase + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES;
+                const uint32_t qb = sbase + Sh::OFF_Q + t * Sh::Q_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * Sh::Q_HALF + (kk & 3) * 32;
+                    const uint64_t a = tc::smem_desc_sw128(qb + off, 16, 1024);
+                    const uint64_t b = tc::smem_desc_sw128(kb + (kk >> 2) * Sh::KV_HALF + (kk & 3) * 32, 16, 1024);
+                    tc::mma_f16_ss(tmem + t * 256, a, b, idesc_s, kk > 0);
+                }
+                tc::mma_commit(&s_full[t]);
+            };
+            auto issue_pv = [&](int j, int t) {   // O_t += P_t V_j, P_t from tensor memory
+                const uint32_t vb = sbase + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                    const uint64_t bv = tc::smem_desc_sw128(vb + kk * 2048, Sh::KV_HALF, 1024);
+                    tc::mma_f16_ts(tmem + t * 256 + 128, tmem + t * 256 + 8 * kk, bv, idesc_o, j > 0 || kk > 0);
+                }
+                tc::mma_commit(&o_done[t]);
+            };
+            bool ok = mbar_wait(q_full, 0, kTcWaitNs) && mbar_wait(&kv_full[0], 0, kTcWaitNs);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_s(0, 0);
+                issue_s(0, 1);
+            }
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const bool more = j + 1 < ntiles;
+                ok = mbar_wait(&p_full[0], (uint32_t)(j & 1), kTcWaitNs);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_pv(j, 0);
+                if (more) {
+                    ok = mbar_wait(&kv_full[(j + 1) % kTcStages], (uint32_t)(((j + 1) / kTcStages) & 1), kTcWaitNs);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    const uint32_t kb = sbase + Sh::OFF_KV + st * Sh::STAGE_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * Sh::Q_HALF + (kk & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(sbase + Sh::OFF_Q + off, 16, 1024);
-                        const uint64_t b = tc::smem_desc_sw128(kb + (kk >> 2) * Sh::KV_HALF + (kk & 3) * 32, 16, 1024);
-                        tc::mma_f16_ss(tmem + sb * kTcKeys, a, b, idesc_s, kk > 0);
-                    }
-                    tc::mma_commit(&s_full[sb]);
+                    issue_s(j + 1, 0);
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, st = jj % kTcStages;
-                    ok = mbar_wait(p_full, (uint32_t)(jj & 1), kTcWaitNs);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    const uint32_t vb = sbase + Sh::OFF_KV + st * Sh::STAGE_BYTES + Sh::K_BYTES;
-#pragma unroll
-                    for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                        const uint32_t poff = (kk >> 2) * Sh::P_HALF + (kk & 3) * 32;
-                        const uint64_t bv = tc::smem_desc_sw128(vb + kk * 2048, Sh::KV_HALF, 1024);
-                        const uint64_t ah = tc::smem_desc_sw128(sbase + Sh::OFF_PH + poff, 16, 1024);
-                        const uint64_t al = tc::smem_desc_sw128(sbase + Sh::OFF_PL + poff, 16, 1024);
-                        tc::mma_f16_ss(tmem + 2 * kTcKeys, ah, bv, idesc_o, jj > 0 || kk > 0);
-                        tc::mma_f16_ss(tmem + 2 * kTcKeys, al, bv, idesc_o, true);
-                    }
-                    tc::mma_commit(o_done);
-                    tc::mma_commit(&kv_empty[st]);
-                }
+                ok = mbar_wait(&p_full[1], (uint32_t)(j & 1), kTcWaitNs);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_pv(j, 1);
+                tc::mma_commit(&kv_empty[j % kTcStages]);
+                if (more) issue_s(j + 1, 1);
             }
             if (!ok) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
         }
     } else {
-        // ---------------- softmax: one row per thread ----------------
+        // ---------------- softmax: tile t, one row per thread ----------------
+        const int t = (warp - 2) >> 2;
         const int lane_base = 32 * (warp & 3);          // tensor-memory lanes this warp may touch
-        const int r = lane_base + lane;                 // MMA row
-        const int tok = r / G, head = r - tok * G;
-        const bool valid = tok < ntok;
+        const int r = lane_base + lane;                 // row within the tile
+        const int tok = t * p.rtok + r / G, head = r % G;
+        const bool valid = r < G * p.rtok && tok < ntok;
         const int pos = valid ? prior + i0 + tok : ctx - 1;   // padding rows see every key
-        const uint32_t trow = tmem + ((uint32_t)lane_base << 16);
+        const uint32_t trow = tmem + ((uint32_t)lane_base << 16) + t * 256;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const int sb = j & 1, st = j % kTcStages;
-            ok = mbar_wait(&s_full[sb], (uint32_t)((j / 2) & 1), kTcWaitNs) &&
-                 mbar_wait(&kv_full[st], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
+            ok = mbar_wait(&s_full[t], (uint32_t)(j & 1), kTcWaitNs) &&
+                 mbar_wait(&kv_full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
-            float s[kTcKeys];
-#pragma unroll
+            const int key0 = j * kTcKeys;
+            // pass 1: row maximum of the masked, scaled scores
+            float mx = -INFINITY;
+#pragma unroll 1
             for (int cc = 0; cc < kTcKeys / 32; ++cc) {
                 float v[32];
-                tc::tmem_ld32(trow + sb * kTcKeys + cc * 32, v);
+                tc::tmem_ld32(trow + cc * 32, v);
+                tc::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[cc * 32 + e] = v[e];
-            }
-            tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            tc::mbar_arrive_cta(&s_free[sb]);
-
-            const int key0 = j * kTcKeys;
-            float mx = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < kTcKeys; ++e) {
-                s[e] = key0 + e <= pos ? s[e] * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[e]);
+                for (int e = 0; e < 32; ++e)
+                    if (key0 + cc * 32 + e <= pos) mx = fmaxf(mx, v[e] * p.scale_log2);
             }
             const bool first = m_used == -INFINITY;
             const float m_new = fmaxf(m_used, mx);
             const bool rescale = !first && m_new > m_used + 8.f;
-            if (j >= 1) {
-                ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1), kTcWaitNs);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    ok = false;
-                    break;
-                }
-                tc::fence_after_sync();
-            }
+            const float alpha = rescale ? exp2_approx(m_used - m_new) : 1.f;
+            if (first || rescale) m_used = m_new;
+            // O was last written by P_t V_{j-1}, which the tensor core finished
+            // before S_t = Q_t K_j^T (issued after it) completed
             if (__any_sync(0xffffffffu, rescale)) {
-                const float alpha = rescale ? exp2_approx(m_used - m_new) : 1.f;
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     float v[32];
-                    tc::tmem_ld32(trow + 2 * kTcKeys + cc * 32, v);
+                    tc::tmem_ld32(trow + 128 + cc * 32, v);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                    tc::tmem_st32(trow + 2 * kTcKeys + cc * 32, v);
+                    tc::tmem_st32(trow + 128 + cc * 32, v);
                 }
-                tc::tmem_wait_st();
-                l *= alpha;
             }
-            if (first || rescale) m_used = m_new;
-
-            // P = 2^(x - m_used) as (rounded, residual) 16-bit pairs, row r of
-            // two K-major 128-byte-swizzled tiles of 128 rows x 64 keys
+            // pass 2: P = 2^(x - m_used) as fp16 pairs; keys 32cc..32cc+31 go
+            // to columns 16cc..16cc+15, which were read before (pass 2 runs
+            // over cc in order), so P overwrites only consumed scores
+            float lt = 0.f;
+#pragma unroll 1
+            for (int cc = 0; cc < kTcKeys / 32; ++cc) {
+                float v[32];
+                tc::tmem_ld32(trow + cc * 32, v);
+                tc::tmem_wait_ld();
+                uint32_t w[16];
 #pragma unroll
-            for (int ch = 0; ch < kTcKeys / 8; ++ch) {
-                uint32_t hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a = exp2_approx(s[ch * 8 + 2 * e] - m_used);
-                    const float b = exp2_approx(s[ch * 8 + 2 * e + 1] - m_used);
-                    l += a + b;
-                    pack2_split<T>(a, b, hi[e], lo[e]);
+                for (int e = 0; e < 16; ++e) {
+                    const int k0 = key0 + cc * 32 + 2 * e;
+                    const float a = k0 <= pos ? exp2_approx(v[2 * e] * p.scale_log2 - m_used) : 0.f;
+                    const float b = k0 + 1 <= pos ? exp2_approx(v[2 * e + 1] * p.scale_log2 - m_used) : 0.f;
+                    lt += a + b;
+                    w[e] = pack2<__half>(a, b);
                 }
-                const uint32_t off = (ch >> 3) * Sh::P_HALF + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(sm + Sh::OFF_PH + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                *reinterpret_cast<uint4 *>(sm + Sh::OFF_PL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                tc::tmem_st16(trow + cc * 16, w);
             }
-            // keys at or past the context in the last stored page may hold
-            // anything: clear those V rows so 0 x garbage cannot reach O
-            const int zlo = max(ctx - key0, 0), zhi = min(kTcKeys, nblk * 16 - key0);
-            if (r >= zlo && r < zhi) {
-                uint8_t *vrow = sm + Sh::OFF_KV + st * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
+            tc::tmem_wait_st();
+            l = l * alpha + lt;
+            // V row r of this tile (key key0 + r), tile-A warps only: keys at
+            // or past the context in the last stored page may hold anything,
+            // so they are cleared (0 x garbage must not reach O); the rest is
+            // converted to fp16 in place when the inputs are bf16.  The tile-B
+            // product is issued after the tile-A one, so it sees the result.
+            if (t == 0) {
+                uint8_t *vrow = sm + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
+                const bool clear = r >= max(ctx - key0, 0) && r < nblk * 16 - key0;
+                if (clear || std::is_same<T, __nv_bfloat16>::value) {
 #pragma unroll
-                for (int hf = 0; hf < Sh::HALVES; ++hf)
+                    for (int hf = 0; hf < Sh::HALVES; ++hf)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        *reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        for (int e = 0; e < 8; ++e) {
+                            uint4 *ptr = reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16);
+                            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                            if (!clear) x = bf16x8_to_f16x8(*ptr);
+                            *ptr = x;
+                        }
+                }
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
-            tc::mbar_arrive_cta(p_full);
+            tc::mbar_arrive_cta(&p_full[t]);
         }
         if (ok) {
-            ok = mbar_wait(o_done, (uint32_t)((ntiles - 1) & 1), kTcWaitNs);
+            ok = mbar_wait(&o_done[t], (uint32_t)((ntiles - 1) & 1), kTcWaitNs);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
             tc::fence_after_sync();
             const float inv = 1.f / l;
             const int64_t ob = ((int64_t)(q0 + i0 + tok) * p.Hq + (int64_t)h * G + head) * D;
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < D / 32; ++cc) {
                 float v[32];
-                tc::tmem_ld32(trow + 2 * kTcKeys + cc * 32, v);
+                tc::tmem_ld32(trow + 128 + cc * 32, v);
                 tc::tmem_wait_ld();
                 if (valid) {
                     if (p.out_dtype == PKV_DTYPE_F32) {
@@ -389,8 +412,8 @@ int prefill_tc(void *out, const void *q, const int32_t *cu_seqlens, int num_seqs
                int out_dtype, int *dev_status, cudaStream_t stream) {
     const int G = Hq / Hkv;
     const int rtok = kTcRows / G;
-    const int tiles = (max_q_len + rtok - 1) / rtok;
-    const int64_t grid64 = (int64_t)num_seqs * tiles * Hkv;
+    const int pairs = (max_q_len + 2 * rtok - 1) / (2 * rtok);
+    const int64_t grid64 = (int64_t)num_seqs * pairs * Hkv;
     if (grid64 >= ((int64_t)1 << 31)) return PKV_ERR_UNSUPPORTED;
     if (!aligned(out, 16)) return PKV_ERR_INVALID_ARG;
     CUtensorMap tk, tv, tq;
@@ -413,7 +436,7 @@ int prefill_tc(void *out, const void *q, const int32_t *cu_seqlens, int num_seqs
     prm.Hkv = Hkv;
     prm.G = G;
     prm.rtok = rtok;
-    prm.tiles_per_seq = tiles;
+    prm.pairs_per_seq = pairs;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.out_dtype = out_dtype;
     const int grid = (int)grid64;
