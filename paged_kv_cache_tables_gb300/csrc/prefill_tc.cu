@@ -22,11 +22,9 @@
 //   warps 2-5  softmax of tile A, warps 6-9 of tile B, one row per thread (the
 //              tensor-memory lane of the row): two passes over S (causal mask,
 //              running max in base 2 with lazy rescaling of O when the max
-//              grows by more than 2^8), then P written back over S as fp16,
-//              which the MMA reads as its A operand straight from tensor
-//              memory.  fp16 keeps 11 significant bits of P; for bf16 inputs
-//              the tile-A warps convert each V tile to fp16 in shared memory
-//              first (exact: bf16 values carry 8 significant bits).
+//              grows by more than 2^8), then P written back over S as
+//              16-bit (rounded value, rounding residual) pairs, which the MMA
+//              reads as its A operand straight from tensor memory.
 // While one tile's softmax runs, the tensor core works on the other tile.
 #include <cuda_runtime.h>
 
@@ -71,18 +69,6 @@ struct TcShape {
     static constexpr int OFF_BAR = OFF_KV + kTcStages * STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + OFF_BAR + 256;
 };
-
-// Eight bf16 values to fp16 (exact for |x| in the fp16 normal range, which
-// holds every bf16 with magnitude between 2^-14 and 65504).
-__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
-    uint32_t in[4] = {x.x, x.y, x.z, x.w}, o[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = __uint_as_float(in[i] << 16), hi = __uint_as_float(in[i] & 0xffff0000u);
-        o[i] = pack2<__half>(lo, hi);
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
-}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -193,7 +179,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (lane == 0) {
             constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
             constexpr uint32_t idesc_s = tc::idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
-            constexpr uint32_t idesc_o = tc::idesc_f16(false, false, true, kTcRows, D);   // P and V in fp16
+            constexpr uint32_t idesc_o = tc::idesc_f16(kBf16, false, true, kTcRows, D);
             auto issue_s = [&](int j, int t) {   // S_t = Q_t K_j^T
                 const uint32_t kb = sbase + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES;
                 const uint32_t qb = sbase + Sh::OFF_Q + t * Sh::Q_BYTES;
@@ -211,7 +197,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk) {
                     const uint64_t bv = tc::smem_desc_sw128(vb + kk * 2048, Sh::KV_HALF, 1024);
-                    tc::mma_f16_ts(tmem + t * 256 + 128, tmem + t * 256 + 8 * kk, bv, idesc_o, j > 0 || kk > 0);
+                    const uint32_t ph = tmem + t * 256 + 32 * (kk >> 1) + 8 * (kk & 1);
+                    tc::mma_f16_ts(tmem + t * 256 + 128, ph, bv, idesc_o, j > 0 || kk > 0);
+                    tc::mma_f16_ts(tmem + t * 256 + 128, ph + 16, bv, idesc_o, true);
                 }
                 tc::mma_commit(&o_done[t]);
             };
@@ -291,47 +279,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc::tmem_st32(trow + 128 + cc * 32, v);
                 }
             }
-            // pass 2: P = 2^(x - m_used) as fp16 pairs; keys 32cc..32cc+31 go
-            // to columns 16cc..16cc+15, which were read before (pass 2 runs
-            // over cc in order), so P overwrites only consumed scores
+            // pass 2: P = 2^(x - m_used) over the same columns, 32 keys at a
+            // time: 16 columns of rounded pairs, then 16 of residual pairs
             float lt = 0.f;
 #pragma unroll 1
             for (int cc = 0; cc < kTcKeys / 32; ++cc) {
                 float v[32];
                 tc::tmem_ld32(trow + cc * 32, v);
                 tc::tmem_wait_ld();
-                uint32_t w[16];
+                float w[32];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int k0 = key0 + cc * 32 + 2 * e;
                     const float a = k0 <= pos ? exp2_approx(v[2 * e] * p.scale_log2 - m_used) : 0.f;
                     const float b = k0 + 1 <= pos ? exp2_approx(v[2 * e + 1] * p.scale_log2 - m_used) : 0.f;
                     lt += a + b;
-                    w[e] = pack2<__half>(a, b);
+                    uint32_t hi, lo;
+                    pack2_split<T>(a, b, hi, lo);
+                    w[e] = __uint_as_float(hi);
+                    w[16 + e] = __uint_as_float(lo);
                 }
-                tc::tmem_st16(trow + cc * 16, w);
+                tc::tmem_st32(trow + cc * 32, w);
             }
             tc::tmem_wait_st();
             l = l * alpha + lt;
-            // V row r of this tile (key key0 + r), tile-A warps only: keys at
-            // or past the context in the last stored page may hold anything,
-            // so they are cleared (0 x garbage must not reach O); the rest is
-            // converted to fp16 in place when the inputs are bf16.  The tile-B
-            // product is issued after the tile-A one, so it sees the result.
-            if (t == 0) {
+            // keys at or past the context in the last stored page may hold
+            // anything: clear those V rows so 0 x garbage cannot reach O
+            // (both tiles' warps write the same zeros before their product)
+            const int zlo = max(ctx - key0, 0), zhi = min(kTcKeys, nblk * 16 - key0);
+            if (r >= zlo && r < zhi) {
                 uint8_t *vrow = sm + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
-                const bool clear = r >= max(ctx - key0, 0) && r < nblk * 16 - key0;
-                if (clear || std::is_same<T, __nv_bfloat16>::value) {
 #pragma unroll
-                    for (int hf = 0; hf < Sh::HALVES; ++hf)
+                for (int hf = 0; hf < Sh::HALVES; ++hf)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            uint4 *ptr = reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16);
-                            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-                            if (!clear) x = bf16x8_to_f16x8(*ptr);
-                            *ptr = x;
-                        }
-                }
+                    for (int e = 0; e < 8; ++e)
+                        *reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();
