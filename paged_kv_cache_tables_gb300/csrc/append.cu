@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
                                                         uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                                                         int num_blocks, int block_size, int num_kv_heads,
                                                         int vec_per_row, int *dev_status) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
     const int64_t items = (int64_t)num_tokens * num_kv_heads * vec_per_row;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < items; i += stride) {
@@ -63,10 +65,11 @@ extern "C" int pkv_kv_append(const void *k, const void *v, const int64_t *slot_m
     const int threads = 256;
     int64_t blocks = (items + threads - 1) / threads;
     if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
-    kv_append_kernel<<<(unsigned)blocks, threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), num_blocks, block_size, num_kv_heads,
-        vec_per_row, dev_status);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0,
+                               static_cast<cudaStream_t>(stream), static_cast<const uint4 *>(k),
+                               static_cast<const uint4 *>(v), slot_mapping, num_tokens, static_cast<uint4 *>(k_cache),
+                               static_cast<uint4 *>(v_cache), num_blocks, block_size, num_kv_heads, vec_per_row,
+                               dev_status);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }

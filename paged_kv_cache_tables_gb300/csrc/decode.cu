@@ -120,7 +120,11 @@ __device__ __forceinline__ uint32_t count_arrival(unsigned long long *ctr, uint3
     for (int it = 0; it < (1 << 16); ++it) {
         const unsigned long long want =
             (uint32_t)(cur >> 32) == epoch ? cur + 1ull : (((unsigned long long)epoch << 32) | 1ull);
-        const unsigned long long prev = atomicCAS(ctr, cur, want);
+        unsigned long long prev;
+        asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
+                     : "=l"(prev)
+                     : "l"(ctr), "l"(cur), "l"(want)
+                     : "memory");
         if (prev == cur) return (uint32_t)(want & 0xffffffffull);
         cur = prev;
     }
@@ -200,6 +204,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv;
+
+    // inputs may come from the previous kernel on the stream (the append)
+    pdl_wait_primary();
+    pdl_launch_dependents();
 
     // ---- plan: total blocks, this CTA's warp ranges, per-sequence offsets ----
     int64_t local = 0;
@@ -430,11 +438,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+        // two accumulator chains per n-tile (even / odd k-steps) halve the
+        // dependent MMA chain
+        float sacc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; kk += 2) {
             mma_16816<T>(sacc[0], qa[kk], kf[kk][0], kf[kk][1]);
             mma_16816<T>(sacc[1], qa[kk], kf[kk][2], kf[kk][3]);
+            mma_16816<T>(sacc2[0], qa[kk + 1], kf[kk + 1][0], kf[kk + 1][1]);
+            mma_16816<T>(sacc2[1], qa[kk + 1], kf[kk + 1][2], kf[kk + 1][3]);
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
 
         // ---- mask, online softmax (base 2) ----
         const int lim = c_ctx - cj * 16;   // valid tokens in this block (>= 16: all)
@@ -484,7 +501,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             }
         }
 
-        // ---- rescale the accumulator, O^T += V^T P^T ----
+        // ---- rescale the accumulator (skipped when no row max moved, the
+        // common case once a range is under way), O^T += V^T P^T ----
+        bool moved = false;
+#pragma unroll
+        for (int pn = 0; pn < NT; ++pn) moved |= alpha[pn] != 1.f;
+        if (__any_sync(0xffffffffu, moved))
 #pragma unroll
         for (int pn = 0; pn < NT; ++pn) {
             const float a_lo = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4);
@@ -565,8 +587,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                         racc[hb * D + d0 + 8] = acc[mt][pn][3];
                     }
                 }
-                // the warp that finishes the last piece of the range combines them
-                __threadfence();
+                // the warp that finishes the last piece of the range combines
+                // them; the counter update is a release (it publishes the
+                // record the lanes wrote before the __syncwarp) and an acquire
+                // (the last arriver then sees every other piece's record)
                 __syncwarp();
                 const int64_t flat = i < n_tail ? t_start + i : lo_w + (i - n_tail);
                 const int64_t seg_lo = flat - cj, seg_hi = seg_lo + c_nb - 1;
@@ -578,7 +602,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 if (lane == 0) arrived = count_arrival(ctr, p.epoch);
                 arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == pieces) {
-                    __threadfence();
+                    __syncwarp();
                     merge_pieces<T, D, NT>(p, w0, w1, total, nw, cs, ch, lane);
                     if (lane == 0) atomicExch(ctr, 0ull);
                 } else if (arrived == 0) {
@@ -615,8 +639,9 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
         if (e != cudaSuccess) return cuda_fail(e);
         attr_set = true;
     }
-    paged_decode_kernel<T, D, NT><<<grid, kDecodeWarps * 32, Sh::SMEM_BYTES, stream>>>(prm, tk, tv);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(paged_decode_kernel<T, D, NT>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES,
+                               stream, prm, tk, tv);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 

@@ -24,6 +24,11 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// launch now / wait here until the previous kernel's writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void set_status(int *dev_status, int bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }

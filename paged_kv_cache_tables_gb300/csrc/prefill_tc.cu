@@ -88,10 +88,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
+    // inputs may come from the previous kernel on the stream (the append)
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    // CTAs in launch order: the last tile pairs of every chunk (the most keys)
+    // first, so the hardware scheduler runs the longest work first and the
+    // short pairs fill the tail
     const int h = blockIdx.x % Hkv;
     const int rest = blockIdx.x / Hkv;
-    const int pair = p.pairs_per_seq - 1 - rest % p.pairs_per_seq;   // the pairs with the most keys first
-    const int c = rest / p.pairs_per_seq;
+    const int c = rest % p.S;
+    const int pair = p.pairs_per_seq - 1 - rest / p.S;
     const int q0 = __ldg(p.cu_seqlens + c);
     const int q_len = __ldg(p.cu_seqlens + c + 1) - q0;
     const int ctx = __ldg(p.context_lens + c);
@@ -383,8 +389,9 @@ int launch_prefill_tc(const PrefillTcParams &prm, const CUtensorMap &tk, const C
         if (e != cudaSuccess) return cuda_fail(e);
         attr_set = true;
     }
-    paged_prefill_tc_kernel<T, D><<<grid, kTcThreads, Sh::SMEM_BYTES, stream>>>(prm, tk, tv, tq);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(paged_prefill_tc_kernel<T, D>, dim3(grid), dim3(kTcThreads), Sh::SMEM_BYTES, stream,
+                               prm, tk, tv, tq);
+    if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
