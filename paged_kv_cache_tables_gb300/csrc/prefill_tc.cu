@@ -91,13 +91,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // inputs may come from the previous kernel on the stream (the append)
     pdl_wait_primary();
     pdl_launch_dependents();
-    // CTAs in launch order: the last tile pairs of every chunk (the most keys)
-    // first, so the hardware scheduler runs the longest work first and the
-    // short pairs fill the tail
+    // CTAs in launch order: chunk by chunk, and within a chunk its last tile
+    // pair (the most keys) first.  The pairs of one chunk read the same
+    // context pages, so running them side by side serves the repeats from L2.
     const int h = blockIdx.x % Hkv;
     const int rest = blockIdx.x / Hkv;
-    const int c = rest % p.S;
-    const int pair = p.pairs_per_seq - 1 - rest / p.S;
+    const int pair = p.pairs_per_seq - 1 - rest % p.pairs_per_seq;
+    const int c = rest / p.pairs_per_seq;
     const int q0 = __ldg(p.cu_seqlens + c);
     const int q_len = __ldg(p.cu_seqlens + c + 1) - q0;
     const int ctx = __ldg(p.context_lens + c);
