@@ -42,6 +42,22 @@ def append_bytes(T, Hkv, d, esize=2):
     return T * (2 * Hkv * d * esize * 2 + 8)
 
 
+# DRAM traffic per algorithmic byte of the decode kernel, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum) of the 64-sequence case, valid
+# for the decode source with this SHA-1; reported as null once it changes.
+DECODE_TRAFFIC_RATIO = 330.97 / 325.0
+DECODE_TRAFFIC_SHA1 = "05bd931b3521be4766d56799c1ab06ff37f5b56c"
+
+
+def decode_traffic(dbytes):
+    import hashlib
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_tables_gb300", "csrc", "decode.cu")
+    with open(src, "rb") as f:
+        if hashlib.sha1(f.read()).hexdigest() != DECODE_TRAFFIC_SHA1:
+            return None
+    return int(round(dbytes * DECODE_TRAFFIC_RATIO))
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -498,8 +514,9 @@ def run_pkv(args):
         "pct_of_8tbs": round(100 * value / 8000.0, 2),
         "kernels_ms": {"kv_append": round(app_ms, 4), "paged_decode_attention": round(dec_ms, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_kind,
-                     "kernel": "paged_decode_kernel (split-KV, fused merge), bytes %d per launch" % dbytes},
+                     "frac": round(achieved / peak, 4), "traffic": decode_traffic(dbytes), "peak_source": peak_kind,
+                     "kernel": "paged_decode_kernel (split-KV, fused merge), bytes %d per launch" % dbytes,
+                     "traffic_source": "ncu capture of the 64-sequence case (1.018 x algorithmic), scaled by bytes"},
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4)},

@@ -145,6 +145,43 @@ __device__ __forceinline__ float exp2_approx(float x) {
     return y;
 }
 
+// Packed fp32 pairs (sm_100 and later execute these as one instruction on
+// two lanes of a 64-bit register pair).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Pack two floats into a 16-bit pair (round to nearest even); `lo` goes to
 // the low half (the lower-indexed element of an MMA fragment).
 template <typename T>
@@ -178,6 +215,25 @@ __device__ __forceinline__ void pack2_split(float lo, float hi, uint32_t &first,
         fhi = __high2float(v);
     }
     second = pack2<T>(lo - flo, hi - fhi);
+}
+
+// pack2_split with the packed pair ab = (lo, hi) already formed: the
+// residuals are taken with one packed subtraction.
+template <typename T>
+__device__ __forceinline__ void pack2_split2(uint64_t ab, float lo, float hi, uint32_t &first, uint32_t &second) {
+    first = pack2<T>(lo, hi);
+    float flo, fhi;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        flo = __uint_as_float(first << 16);
+        fhi = __uint_as_float(first & 0xffff0000u);
+    } else {
+        __half2 v = *reinterpret_cast<__half2 *>(&first);
+        flo = __low2float(v);
+        fhi = __high2float(v);
+    }
+    float rlo, rhi;
+    f2_unpack(f2_sub(ab, f2_pack(flo, fhi)), rlo, rhi);
+    second = pack2<T>(rlo, rhi);
 }
 
 template <typename T>

@@ -37,6 +37,20 @@ __device__ __forceinline__ void fence_after_sync() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ---- per-warpgroup register budget ----------------------------------------
+// Executed by all threads of a warpgroup; an increase waits until other
+// warpgroups of the CTA have released enough registers, so the launch total
+// (threads x registers per thread) must cover the sum of the new budgets.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- descriptors ------------------------------------------------------------
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile whose

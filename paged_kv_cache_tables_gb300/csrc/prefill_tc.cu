@@ -19,16 +19,20 @@
 //              and issues every MMA from one thread, ping-ponging the tiles:
 //              O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
 //              S_B = Q_B K_{j+1}^T, ...;
-//   warps 2-5  softmax of tile A, warps 6-9 of tile B, one row per thread (the
-//              tensor-memory lane of the row): two passes over S (causal mask,
-//              running max in base 2 with lazy rescaling of O when the max
-//              grows by more than 2^8), then P written back over S as
+//   warps 2-3  idle (they complete the first warpgroup, whose register
+//              budget drops so that the softmax warpgroups can grow);
+//   warps 4-7  softmax of tile A, warps 8-11 of tile B, one row per thread (the
+//              tensor-memory lane of the row): one pass over S held in
+//              registers (causal mask on diagonal tiles only, running max in
+//              base 2 with lazy rescaling of O when the max grows by more
+//              than 2^8, packed fp32x2 arithmetic), then P written back over S as
 //              16-bit (rounded value, rounding residual) pairs, which the MMA
 //              reads as its A operand straight from tensor memory.
 // While one tile's softmax runs, the tensor core works on the other tile.
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstdio>
 
 #include "pkv.h"
 #include "pkv_device.cuh"
@@ -37,7 +41,14 @@
 
 namespace pkv {
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 384;
+// registers per thread: the launch gives every thread kTcLaunchRegs; the
+// TMA/MMA warpgroup then drops to kTcLowRegs and the two softmax warpgroups
+// rise to kTcHighRegs, which must not exceed what the drop frees
+constexpr int kTcLaunchRegs = 168;
+constexpr int kTcLowRegs = 56;
+constexpr int kTcHighRegs = 224;
+static_assert(128 * kTcLowRegs + 256 * kTcHighRegs <= kTcThreads * kTcLaunchRegs, "register split");
 constexpr int kTcRows = 128;    // MMA rows = (token, head) pairs per query tile
 constexpr int kTcKeys = 128;    // keys per K/V tile
 constexpr int kTcStages = 2;
@@ -139,7 +150,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t sbase = smem_addr(sm);
 
-    if (warp == 0) {
+    if (warp < 4) {
+      tc::setmaxnreg_dec<kTcLowRegs>();
+      if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             const int qrows = G * p.rtok;
@@ -236,9 +249,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (!ok) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
         }
+      }
     } else {
+        tc::setmaxnreg_inc<kTcHighRegs>();
         // ---------------- softmax: tile t, one row per thread ----------------
-        const int t = (warp - 2) >> 2;
+        const int t = (warp - 4) >> 2;
         const int lane_base = 32 * (warp & 3);          // tensor-memory lanes this warp may touch
         const int r = lane_base + lane;                 // row within the tile
         const int tok = t * p.rtok + r / G, head = r % G;
@@ -246,27 +261,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int pos = valid ? prior + i0 + tok : ctx - 1;   // padding rows see every key
         const uint32_t trow = tmem + ((uint32_t)lane_base << 16) + t * 256;
         float m_used = -INFINITY, l = 0.f;
+        const uint64_t scale2 = f2_pack(p.scale_log2, p.scale_log2);
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            ok = mbar_wait(&s_full[t], (uint32_t)(j & 1), kTcWaitNs) &&
-                 mbar_wait(&kv_full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
+            ok = mbar_wait(&s_full[t], (uint32_t)(j & 1), kTcWaitNs);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
             }
             tc::fence_after_sync();
             const int key0 = j * kTcKeys;
-            // pass 1: row maximum of the masked, scaled scores
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int cc = 0; cc < kTcKeys / 32; ++cc) {
-                float v[32];
-                tc::tmem_ld32(trow + cc * 32, v);
-                tc::tmem_wait_ld();
+            // one pass: the whole row of 128 scores in registers
+            float v[kTcKeys];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    if (key0 + cc * 32 + e <= pos) mx = fmaxf(mx, v[e] * p.scale_log2);
+            for (int cc = 0; cc < kTcKeys / 32; ++cc)
+                tc::tmem_ld32(trow + cc * 32, *reinterpret_cast<float(*)[32]>(v + cc * 32));
+            tc::tmem_wait_ld();
+            // causal mask, only on tiles that reach past some row's position
+            const int lim = pos - key0;
+            if (__any_sync(0xffffffffu, lim < kTcKeys - 1)) {
+#pragma unroll
+                for (int e = 0; e < kTcKeys; ++e)
+                    if (e > lim) v[e] = -INFINITY;
             }
+            // four independent chains of 3-input maxima over the 124 scores
+            // after the first four
+            float mx4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+            for (int pr = 0; pr < (kTcKeys - 4) / 2; ++pr)
+                mx4[pr & 3] = fmax3(mx4[pr & 3], v[4 + 2 * pr], v[5 + 2 * pr]);
+            // scale_log2 > 0, so the scaled maximum is the maximum scaled
+            const float mx = fmax3(fmaxf(mx4[0], mx4[1]), mx4[2], mx4[3]) * p.scale_log2;
             const bool first = m_used == -INFINITY;
             const float m_new = fmaxf(m_used, mx);
             const bool rescale = !first && m_new > m_used + 8.f;
@@ -277,51 +302,58 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
-                    float v[32];
-                    tc::tmem_ld32(trow + 128 + cc * 32, v);
+                    float o[32];
+                    tc::tmem_ld32(trow + 128 + cc * 32, o);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] *= alpha;
-                    tc::tmem_st32(trow + 128 + cc * 32, v);
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tc::tmem_st32(trow + 128 + cc * 32, o);
                 }
             }
-            // pass 2: P = 2^(x - m_used) over the same columns, 32 keys at a
-            // time: 16 columns of rounded pairs, then 16 of residual pairs
-            float lt = 0.f;
-#pragma unroll 1
+            // P = 2^(x - m_used) over the same columns, 32 keys at a time: 16
+            // columns of rounded pairs, then 16 of residual pairs
+            const uint64_t negm2 = f2_pack(-m_used, -m_used);
+            uint64_t sum2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
             for (int cc = 0; cc < kTcKeys / 32; ++cc) {
-                float v[32];
-                tc::tmem_ld32(trow + cc * 32, v);
-                tc::tmem_wait_ld();
                 float w[32];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int k0 = key0 + cc * 32 + 2 * e;
-                    const float a = k0 <= pos ? exp2_approx(v[2 * e] * p.scale_log2 - m_used) : 0.f;
-                    const float b = k0 + 1 <= pos ? exp2_approx(v[2 * e + 1] * p.scale_log2 - m_used) : 0.f;
-                    lt += a + b;
+                    float a, b;
+                    f2_unpack(f2_fma(f2_pack(v[32 * cc + 2 * e], v[32 * cc + 2 * e + 1]), scale2, negm2), a, b);
+                    a = exp2_approx(a);
+                    b = exp2_approx(b);
+                    const uint64_t ab = f2_pack(a, b);
+                    sum2[e & 1] = f2_add(sum2[e & 1], ab);
                     uint32_t hi, lo;
-                    pack2_split<T>(a, b, hi, lo);
+                    pack2_split2<T>(ab, a, b, hi, lo);
                     w[e] = __uint_as_float(hi);
                     w[16 + e] = __uint_as_float(lo);
                 }
                 tc::tmem_st32(trow + cc * 32, w);
             }
-            tc::tmem_wait_st();
-            l = l * alpha + lt;
+            float s0, s1, s2, s3;
+            f2_unpack(sum2[0], s0, s1);
+            f2_unpack(sum2[1], s2, s3);
+            l = l * alpha + ((s0 + s1) + (s2 + s3));
             // keys at or past the context in the last stored page may hold
             // anything: clear those V rows so 0 x garbage cannot reach O
-            // (both tiles' warps write the same zeros before their product)
+            // (both tiles' warps write the same zeros before their product;
+            // the tile has landed: its S product waited for the whole stage)
             const int zlo = max(ctx - key0, 0), zhi = min(kTcKeys, nblk * 16 - key0);
-            if (r >= zlo && r < zhi) {
-                uint8_t *vrow = sm + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
+            if (zlo < zhi) {
+                if (r >= zlo && r < zhi) {
+                    uint8_t *vrow = sm + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
 #pragma unroll
-                for (int hf = 0; hf < Sh::HALVES; ++hf)
+                    for (int hf = 0; hf < Sh::HALVES; ++hf)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        *reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        for (int e = 0; e < 8; ++e)
+                            *reinterpret_cast<uint4 *>(vrow + hf * Sh::KV_HALF + e * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             tc::mbar_arrive_cta(&p_full[t]);
         }
@@ -387,6 +419,18 @@ int launch_prefill_tc(const PrefillTcParams &prm, const CUtensorMap &tk, const C
         cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
+        // the register split inside the kernel waits for registers that only
+        // exist if the compiled count is the one it was sized for
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, paged_prefill_tc_kernel<T, D>);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (fa.numRegs != kTcLaunchRegs) {
+            char msg[128];
+            std::snprintf(msg, sizeof msg, "prefill kernel compiled to %d registers per thread, its split needs %d",
+                          fa.numRegs, kTcLaunchRegs);
+            set_error_message(msg);
+            return PKV_ERR_UNSUPPORTED;
+        }
         attr_set = true;
     }
     cudaError_t e = launch_pdl(paged_prefill_tc_kernel<T, D>, dim3(grid), dim3(kTcThreads), Sh::SMEM_BYTES, stream,
