@@ -285,6 +285,10 @@ def run_mixed(args):
     import paged_kv_cache_tables_gb300 as pkv
     from synth import make_step
     over = {"n_chunks": args.mixed_chunks} if args.mixed_chunks else {}
+    if args.mixed_prior >= 0:
+        over["prior_fixed"] = args.mixed_prior
+    if args.pool:
+        over["NB"] = args.pool
     st = make_step("mixed", **over)
     p = st.n_prefill
     t1 = int(st.cu_seqlens[p])
@@ -334,8 +338,9 @@ def run_mixed(args):
     hpeak, hkind = load_peaks()
     tfl = flops / (pre_ms * 1e-3) / 1e12
     return {
-        "workload": "mixed: 8 prefill chunks x 512 (prior U{0..4096}) + 248 decodes (ctx U{256..4096}), 32/8 heads, "
-                    "d 128, bf16; append of 4344 tokens first",
+        "workload": "mixed: %d prefill chunks x 512 (prior %s) + 248 decodes (ctx U{256..4096}), 32/8 heads, "
+                    "d 128, bf16; append of %d tokens first"
+                    % (p, "U{0..4096}" if args.mixed_prior < 0 else args.mixed_prior, st.T),
         "steps": K, "ms_per_step": round(step_ms, 4),
         "kv_append_ms": round(app_ms, 4),
         "prefill": {"ms": round(pre_ms, 4), "gflop": round(flops / 1e9, 2), "tflops": round(tfl, 1),
@@ -545,6 +550,8 @@ def main():
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed prefill + decode step")
     ap.add_argument("--mixed-steps", type=int, default=50)
     ap.add_argument("--mixed-chunks", type=int, default=0, help="override the prefill chunk count (profiling)")
+    ap.add_argument("--mixed-prior", type=int, default=-1,
+                    help="give every prefill chunk this prior context instead of U{0..4096} (profiling)")
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace"])
     ap.add_argument("--trace-requests", type=int, default=1000)

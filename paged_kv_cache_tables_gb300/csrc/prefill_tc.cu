@@ -14,7 +14,9 @@
 // tiles of a pair (adjacent tokens) share every K/V tile.  Warp roles:
 //   warp 0     TMA: both query tiles once (3-D boxes, 128-byte swizzle), then
 //              K and V tiles of 128 keys = 8 pages of 16 through the block
-//              table into a 2-stage ring;
+//              table (ids read one tile ahead) into 2-stage K and V rings
+//              with their own barriers: a K slot frees after the second
+//              Q.K^T of its tile, a V slot after the second P.V;
 //   warp 1     allocates all 512 tensor-memory columns (S and O of each tile)
 //              and issues every MMA from one thread, ping-ponging the tiles:
 //              O_A += P_A V_j, S_A = Q_A K_{j+1}^T, O_B += P_B V_j,
@@ -90,12 +92,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + Sh::OFF_BAR);
     uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;     // [2]
-    uint64_t *kv_empty = bars + 3;    // [2]
-    uint64_t *s_full = bars + 5;      // [tile]
-    uint64_t *p_full = bars + 7;      // [tile]
-    uint64_t *o_done = bars + 9;      // [tile]
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 11);
+    uint64_t *k_full = bars + 1;      // [stage]
+    uint64_t *v_full = bars + 3;      // [stage]
+    uint64_t *k_empty = bars + 5;     // [stage]
+    uint64_t *v_empty = bars + 7;     // [stage]
+    uint64_t *s_full = bars + 9;      // [tile]
+    uint64_t *p_full = bars + 11;     // [tile]
+    uint64_t *o_done = bars + 13;     // [tile]
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
@@ -130,8 +134,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kTcStages; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int t = 0; t < 2; ++t) {
             mbar_init(&s_full[t], 1);
@@ -154,6 +160,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::setmaxnreg_dec<kTcLowRegs>();
       if (warp == 0) {
         // ---------------- TMA producer ----------------
+        // lane 0 issues the copies; lanes 0-7 read the block ids of the next
+        // tile's eight pages one tile ahead, so no table read sits between
+        // a slot becoming free and its copies starting
+        constexpr int kPages = kTcKeys / 16;
+        const int32_t *row = p.block_tables + (int64_t)c * p.max_blocks;
+        auto in_context = [&](int jt) { return lane < kPages && jt * kPages + lane < nblk; };
+        auto fetch = [&](int jt) { return in_context(jt) ? __ldg(row + jt * kPages + lane) : 0; };
+        int blk_next = fetch(0);
         if (lane == 0) {
             const int qrows = G * p.rtok;
             mbar_arrive_expect_tx(q_full, (uint32_t)(2 * Sh::HALVES * qrows * 128));
@@ -163,35 +177,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int hf = 0; hf < Sh::HALVES; ++hf)
                     tc::tma_load_3d(sm + Sh::OFF_Q + t * Sh::Q_BYTES + hf * Sh::Q_HALF, &tq, hf * 64, h * G,
                                     q0 + i0 + t * p.rtok, q_full);
-            const uint64_t policy = l2_policy_evict_first();
-            const int32_t *row = p.block_tables + (int64_t)c * p.max_blocks;
-            for (int j = 0; j < ntiles; ++j) {
-                const int st = j % kTcStages;
-                if (j >= kTcStages &&
-                    !mbar_wait(&kv_empty[st], (uint32_t)(((j - kTcStages) / kTcStages) & 1), kTcWaitNs)) {
-                    set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
-                    break;
-                }
-                mbar_arrive_expect_tx(&kv_full[st], Sh::STAGE_BYTES);
-                uint8_t *kd = sm + Sh::OFF_KV + st * Sh::STAGE_BYTES;
-                for (int pg = 0; pg < kTcKeys / 16; ++pg) {
-                    const int page = j * (kTcKeys / 16) + pg;
-                    int y = p.num_blocks * Hkv * 16;             // past the pool: zero fill
-                    if (page < nblk) {
-                        const int blk = __ldg(row + page);
-                        if (blk >= 0 && blk < p.num_blocks)
-                            y = (blk * Hkv + h) * 16;
-                        else
-                            set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                    }
-#pragma unroll
-                    for (int hf = 0; hf < Sh::HALVES; ++hf) {
-                        tma_load_2d(kd + hf * Sh::KV_HALF + pg * 2048, &tk, hf * 64, y, &kv_full[st], policy);
-                        tma_load_2d(kd + Sh::K_BYTES + hf * Sh::KV_HALF + pg * 2048, &tv, hf * 64, y, &kv_full[st],
-                                    policy);
-                    }
-                }
+        }
+        const uint64_t policy = l2_policy_evict_first();
+        for (int j = 0; j < ntiles; ++j) {
+            const int blk = blk_next;
+            if (j + 1 < ntiles) blk_next = fetch(j + 1);
+            int y = p.num_blocks * Hkv * 16;               // past the pool: zero fill
+            if (in_context(j)) {
+                if (blk >= 0 && blk < p.num_blocks)
+                    y = (blk * Hkv + h) * 16;
+                else
+                    set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
             }
+            int ys[kPages];
+#pragma unroll
+            for (int pg = 0; pg < kPages; ++pg) ys[pg] = __shfl_sync(0xffffffffu, y, pg);
+            const int st = j % kTcStages;
+            const uint32_t par = (uint32_t)(((j - kTcStages) / kTcStages) & 1);
+            bool ok = true;
+            if (lane == 0) {
+                // K of tile j - 2 is free once both S products of that tile are done
+                if (j >= kTcStages) ok = mbar_wait(&k_empty[st], par, kTcWaitNs);
+                if (ok) {
+                    mbar_arrive_expect_tx(&k_full[st], Sh::K_BYTES);
+                    uint8_t *kd = sm + Sh::OFF_KV + st * Sh::STAGE_BYTES;
+#pragma unroll
+                    for (int pg = 0; pg < kPages; ++pg)
+#pragma unroll
+                        for (int hf = 0; hf < Sh::HALVES; ++hf)
+                            tma_load_2d(kd + hf * Sh::KV_HALF + pg * 2048, &tk, hf * 64, ys[pg], &k_full[st], policy);
+                }
+                // V of tile j - 2 is free once both P.V products of that tile are done
+                if (ok && j >= kTcStages) ok = mbar_wait(&v_empty[st], par, kTcWaitNs);
+                if (ok) {
+                    mbar_arrive_expect_tx(&v_full[st], Sh::K_BYTES);
+                    uint8_t *vd = sm + Sh::OFF_KV + st * Sh::STAGE_BYTES + Sh::K_BYTES;
+#pragma unroll
+                    for (int pg = 0; pg < kPages; ++pg)
+#pragma unroll
+                        for (int hf = 0; hf < Sh::HALVES; ++hf)
+                            tma_load_2d(vd + hf * Sh::KV_HALF + pg * 2048, &tv, hf * 64, ys[pg], &v_full[st], policy);
+                }
+                if (!ok) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -222,20 +251,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc::mma_commit(&o_done[t]);
             };
-            bool ok = mbar_wait(q_full, 0, kTcWaitNs) && mbar_wait(&kv_full[0], 0, kTcWaitNs);
+            bool ok = mbar_wait(q_full, 0, kTcWaitNs) && mbar_wait(&k_full[0], 0, kTcWaitNs);
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0, 0);
                 issue_s(0, 1);
+                tc::mma_commit(&k_empty[0]);
             }
             for (int j = 0; ok && j < ntiles; ++j) {
                 const bool more = j + 1 < ntiles;
-                ok = mbar_wait(&p_full[0], (uint32_t)(j & 1), kTcWaitNs);
+                ok = mbar_wait(&p_full[0], (uint32_t)(j & 1), kTcWaitNs) &&
+                     mbar_wait(&v_full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
                 if (!ok) break;
                 tc::fence_after_sync();
                 issue_pv(j, 0);
                 if (more) {
-                    ok = mbar_wait(&kv_full[(j + 1) % kTcStages], (uint32_t)(((j + 1) / kTcStages) & 1), kTcWaitNs);
+                    ok = mbar_wait(&k_full[(j + 1) % kTcStages], (uint32_t)(((j + 1) / kTcStages) & 1), kTcWaitNs);
                     if (!ok) break;
                     tc::fence_after_sync();
                     issue_s(j + 1, 0);
@@ -244,8 +275,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
                 issue_pv(j, 1);
-                tc::mma_commit(&kv_empty[j % kTcStages]);
-                if (more) issue_s(j + 1, 1);
+                tc::mma_commit(&v_empty[j % kTcStages]);
+                if (more) {
+                    issue_s(j + 1, 1);
+                    tc::mma_commit(&k_empty[(j + 1) % kTcStages]);
+                }
             }
             if (!ok) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
         }
@@ -338,10 +372,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             l = l * alpha + ((s0 + s1) + (s2 + s3));
             // keys at or past the context in the last stored page may hold
             // anything: clear those V rows so 0 x garbage cannot reach O
-            // (both tiles' warps write the same zeros before their product;
-            // the tile has landed: its S product waited for the whole stage)
+            // (both tiles' warps write the same zeros before their product)
             const int zlo = max(ctx - key0, 0), zhi = min(kTcKeys, nblk * 16 - key0);
             if (zlo < zhi) {
+                // V_j cannot be reloaded before this tile's P.V products,
+                // so the phase waited for here is this tile's
+                ok = mbar_wait(&v_full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
                 if (r >= zlo && r < zhi) {
                     uint8_t *vrow = sm + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES + r * 128;
 #pragma unroll

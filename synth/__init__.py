@@ -204,6 +204,9 @@ def make_step(name: str, seed: Optional[int] = None, **over) -> Step:
         n_dec = over.pop("n_decode", 248)
         NB = over.pop("NB", 65536)
         prior_p = rng.integers(0, 4096, size=n_chunks, endpoint=True)
+        fixed = over.pop("prior_fixed", None)
+        if fixed is not None:   # profiling case: every chunk behind the same prior context
+            prior_p = np.full(n_chunks, int(fixed), dtype=prior_p.dtype)
         ctx_d = rng.integers(256, 4096, size=n_dec, endpoint=True)
         ctx = np.concatenate([prior_p + chunk, ctx_d])
         q_lens = np.concatenate([np.full(n_chunks, chunk), np.ones(n_dec, dtype=np.int64)])
