@@ -48,8 +48,8 @@ constexpr int kTcThreads = 384;
 // TMA/MMA warpgroup then drops to kTcLowRegs and the two softmax warpgroups
 // rise to kTcHighRegs, which must not exceed what the drop frees
 constexpr int kTcLaunchRegs = 168;
-constexpr int kTcLowRegs = 56;
-constexpr int kTcHighRegs = 224;
+constexpr int kTcLowRegs = 88;
+constexpr int kTcHighRegs = 208;
 static_assert(128 * kTcLowRegs + 256 * kTcHighRegs <= kTcThreads * kTcLaunchRegs, "register split");
 constexpr int kTcRows = 128;    // MMA rows = (token, head) pairs per query tile
 constexpr int kTcKeys = 128;    // keys per K/V tile
@@ -224,65 +224,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-            constexpr uint32_t idesc_s = tc::idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
-            constexpr uint32_t idesc_o = tc::idesc_f16(kBf16, false, true, kTcRows, D);
-            auto issue_s = [&](int j, int t) {   // S_t = Q_t K_j^T
-                const uint32_t kb = sbase + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES;
-                const uint32_t qb = sbase + Sh::OFF_Q + t * Sh::Q_BYTES;
+        // The whole warp walks the schedule, so the waits and the descriptor
+        // arithmetic are warp-uniform; one elected lane issues each MMA and
+        // commit.  Shared-memory descriptors are built once and moved by
+        // adding (byte offset >> 4) to their address field: every operand
+        // lies below 256 KB, so the 14-bit field never carries.
+        const bool leader = tc::elect_one();
+        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+        constexpr uint32_t idesc_s = tc::idesc_f16(kBf16, false, false, kTcRows, kTcKeys);
+        constexpr uint32_t idesc_o = tc::idesc_f16(kBf16, false, true, kTcRows, D);
+        const uint64_t q_desc = tc::smem_desc_sw128(sbase + Sh::OFF_Q, 16, 1024);
+        const uint64_t k_desc = tc::smem_desc_sw128(sbase + Sh::OFF_KV, 16, 1024);
+        const uint64_t v_desc = tc::smem_desc_sw128(sbase + Sh::OFF_KV + Sh::K_BYTES, Sh::KV_HALF, 1024);
+        auto issue_s = [&](int j, int t) {   // S_t = Q_t K_j^T
+            const uint64_t kb = k_desc + (uint64_t)(((j % kTcStages) * Sh::STAGE_BYTES) >> 4);
+            const uint64_t qb = q_desc + (uint64_t)((t * Sh::Q_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * Sh::Q_HALF + (kk & 3) * 32;
-                    const uint64_t a = tc::smem_desc_sw128(qb + off, 16, 1024);
-                    const uint64_t b = tc::smem_desc_sw128(kb + (kk >> 2) * Sh::KV_HALF + (kk & 3) * 32, 16, 1024);
-                    tc::mma_f16_ss(tmem + t * 256, a, b, idesc_s, kk > 0);
-                }
-                tc::mma_commit(&s_full[t]);
-            };
-            auto issue_pv = [&](int j, int t) {   // O_t += P_t V_j, P_t from tensor memory
-                const uint32_t vb = sbase + Sh::OFF_KV + (j % kTcStages) * Sh::STAGE_BYTES + Sh::K_BYTES;
-#pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-                    const uint64_t bv = tc::smem_desc_sw128(vb + kk * 2048, Sh::KV_HALF, 1024);
-                    const uint32_t ph = tmem + t * 256 + 32 * (kk >> 1) + 8 * (kk & 1);
-                    tc::mma_f16_ts(tmem + t * 256 + 128, ph, bv, idesc_o, j > 0 || kk > 0);
-                    tc::mma_f16_ts(tmem + t * 256 + 128, ph + 16, bv, idesc_o, true);
-                }
-                tc::mma_commit(&o_done[t]);
-            };
-            bool ok = mbar_wait(q_full, 0, kTcWaitNs) && mbar_wait(&k_full[0], 0, kTcWaitNs);
-            if (ok) {
-                tc::fence_after_sync();
-                issue_s(0, 0);
-                issue_s(0, 1);
-                tc::mma_commit(&k_empty[0]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t qo = ((kk >> 2) * Sh::Q_HALF + (kk & 3) * 32) >> 4;
+                const uint32_t ko = ((kk >> 2) * Sh::KV_HALF + (kk & 3) * 32) >> 4;
+                if (leader) tc::mma_f16_ss(tmem + t * 256, qb + qo, kb + ko, idesc_s, kk > 0);
             }
-            for (int j = 0; ok && j < ntiles; ++j) {
-                const bool more = j + 1 < ntiles;
-                ok = mbar_wait(&p_full[0], (uint32_t)(j & 1), kTcWaitNs) &&
-                     mbar_wait(&v_full[j % kTcStages], (uint32_t)((j / kTcStages) & 1), kTcWaitNs);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_pv(j, 0);
-                if (more) {
-                    ok = mbar_wait(&k_full[(j + 1) % kTcStages], (uint32_t)(((j + 1) / kTcStages) & 1), kTcWaitNs);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    issue_s(j + 1, 0);
-                }
-                ok = mbar_wait(&p_full[1], (uint32_t)(j & 1), kTcWaitNs);
-                if (!ok) break;
-                tc::fence_after_sync();
-                issue_pv(j, 1);
-                tc::mma_commit(&v_empty[j % kTcStages]);
-                if (more) {
-                    issue_s(j + 1, 1);
-                    tc::mma_commit(&k_empty[(j + 1) % kTcStages]);
+            if (leader) tc::mma_commit(&s_full[t]);
+        };
+        auto issue_pv = [&](int j, int t) {   // O_t += P_t V_j, P_t from tensor memory
+            const uint64_t vb = v_desc + (uint64_t)(((j % kTcStages) * Sh::STAGE_BYTES) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+                const uint32_t ph = tmem + t * 256 + 32 * (kk >> 1) + 8 * (kk & 1);
+                if (leader) {
+                    tc::mma_f16_ts(tmem + t * 256 + 128, ph, vb + (uint32_t)(kk * 2048 >> 4), idesc_o, j > 0 || kk > 0);
+                    tc::mma_f16_ts(tmem + t * 256 + 128, ph + 16, vb + (uint32_t)(kk * 2048 >> 4), idesc_o, true);
                 }
             }
-            if (!ok) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+            if (leader) tc::mma_commit(&o_done[t]);
+        };
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait(bar, parity, kTcWaitNs));
+        };
+        bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+        if (ok) {
+            tc::fence_after_sync();
+            issue_s(0, 0);
+            issue_s(0, 1);
+            if (leader) tc::mma_commit(&k_empty[0]);
         }
+        for (int j = 0; ok && j < ntiles; ++j) {
+            const bool more = j + 1 < ntiles;
+            ok = wait_all(&p_full[0], (uint32_t)(j & 1)) &&
+                 wait_all(&v_full[j % kTcStages], (uint32_t)((j / kTcStages) & 1));
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_pv(j, 0);
+            if (more) {
+                ok = wait_all(&k_full[(j + 1) % kTcStages], (uint32_t)(((j + 1) / kTcStages) & 1));
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_s(j + 1, 0);
+            }
+            ok = wait_all(&p_full[1], (uint32_t)(j & 1));
+            if (!ok) break;
+            tc::fence_after_sync();
+            issue_pv(j, 1);
+            if (leader) tc::mma_commit(&v_empty[j % kTcStages]);
+            if (more) {
+                issue_s(j + 1, 1);
+                if (leader) tc::mma_commit(&k_empty[(j + 1) % kTcStages]);
+            }
+        }
+        if (!ok && leader) set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
       }
     } else {
         tc::setmaxnreg_inc<kTcHighRegs>();
