@@ -381,6 +381,8 @@ def run_trace_bench(args):
     steps = res["steps"]
     Hq, Hkv, d = 32, 8, 128
     dec_tokens = pre_keys = kv_bytes = 0
+    big_bytes, big_ms, big_steps, dev_ms = 0, 0.0, 0, 0.0
+    l2_bytes = 129e6
     for s in steps:
         ctx, ql = s["context_lens"], s["q_lens"]
         dmask = ql == 1
@@ -388,7 +390,15 @@ def run_trace_bench(args):
         for c, q in zip(ctx[~dmask], ql[~dmask]):
             c, q = int(c), int(q)
             pre_keys += q * (c - q) + q * (q + 1) // 2
-        kv_bytes += int(ctx.sum()) * 2 * Hkv * d * 2
+        layer_bytes = int(ctx.sum()) * 2 * Hkv * d * 2
+        kv_bytes += layer_bytes
+        dev_ms += s["device_ms"]
+        # steps whose per-layer working set is more than 4x L2: no layer can
+        # be served from the previous layer's cached pages
+        if layer_bytes > 4 * l2_bytes:
+            big_bytes += layer_bytes * L
+            big_ms += s["device_ms"]
+            big_steps += 1
     gen = sum(min(int(eos[i]), 4096, 8192 - int(prompt[i])) for i in range(n))
     lat = np.array([res["finish_step"][i] - int(arrival[i]) for i in range(n)])
     dev_s = res["stream_ms"] / 1e3
@@ -416,9 +426,15 @@ def run_trace_bench(args):
         "engine_steps": len(steps), "wall_s": round(res["wall_s"], 3), "stream_s": round(dev_s, 3),
         "host_sched_ms_per_step": round(st["host_ms"] / max(1, st["steps"]), 4),
         "host_ms_per_step": round(eng.host_ms / max(1, len(steps)), 4),
+        "host_wait_ms_per_step": round(eng.wait_ms / max(1, len(steps)), 4),
         "output_tokens": gen, "output_tokens_per_s": round(gen / res["wall_s"], 1),
         "attended_tokens_per_s": round((dec_tokens + pre_keys) * L / res["wall_s"], 1),
         "kv_gbs": round(kv_bytes * L / res["wall_s"] / 1e9, 1),
+        "device_s": round(dev_ms / 1e3, 3),
+        "kv_gbs_device": round(kv_bytes * L / (dev_ms * 1e-3) / 1e9, 1),
+        "kv_gbs_steps_over_4x_l2": {"steps": big_steps, "gbs": round(big_bytes / max(big_ms * 1e-3, 1e-12) / 1e9, 1),
+                                    "note": "KV bytes / device time of the steps whose per-layer working set "
+                                            "exceeds 4 x 129 MB (append, prefill and decode of all layers)"},
         "preemptions": st["preemptions"], "preemption_rate": round(st["preemptions"] / max(1, st["steps"]), 4),
         "avg_running_batch": round(st["sum_running"] / max(1, st["steps"]), 2),
         "latency_steps_p50": float(np.percentile(lat, 50)), "latency_steps_p99": float(np.percentile(lat, 99)),

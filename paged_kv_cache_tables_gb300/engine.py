@@ -61,7 +61,8 @@ class PagedEngine:
         self.d_i64 = torch.empty(self.n_i64, dtype=torch.int64, device=dev)
         self.d_i32 = torch.empty(self.n_i32, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream()
-        self.host_ms = 0.0
+        self.host_ms = 0.0      # host work per step, without waiting for the device
+        self.wait_ms = 0.0      # host time spent waiting for a staging buffer
         self.upload_bytes = 0
 
     def add(self, rid, prompt_len, max_tokens, eos_after):
@@ -82,7 +83,10 @@ class PagedEngine:
         # stage: i64 = [slot_mapping T][token_rids T]; i32 = [token_pos T][ctx S][cu S+1][tables S*MB]
         buf = self.nstep & 1
         self.nstep += 1
-        self.copied[buf].synchronize()
+        tw = time.perf_counter()
+        self.copied[buf].synchronize()    # the device is at most one step behind
+        waited = (time.perf_counter() - tw) * 1e3
+        self.wait_ms += waited
         h64, h32 = self.h_i64[buf].numpy(), self.h_i32[buf].numpy()
         h64[:T] = arr(m.slot_mapping, T)
         h64[T:2 * T] = arr(m.token_rids, T)
@@ -110,19 +114,40 @@ class PagedEngine:
                 "context_lens": arr(m.context_lens, S).copy(), "cu_seqlens": cu_h.copy(),
                 "q_lens": arr(m.q_lens, S).copy(),
                 "finished": arr(m.finished_rids, m.num_finished).copy() if m.num_finished else np.zeros(0, np.int64)}
-        self.host_ms += (time.perf_counter() - t0) * 1e3
+        # the step's device pointers are resolved once; every layer then calls
+        # the C ABI directly (the same entry points the binding wraps)
+        L = B.lib()
+        esz = 2
+        row_q = self.Hq * self.d * esz
+        pq, pk, pv, pout = q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr()
+        pslots, pcu, pctx, ptab = slots.data_ptr(), cu.data_ptr(), ctx.data_ptr(), tables.data_ptr()
+        pst, pstream = self.status.data_ptr(), self.stream.cuda_stream
+        pwork, nwork = self.work.data_ptr(), self.work.numel()
+        dt = B.DTYPE_BF16 if self.tdt == torch.bfloat16 else B.DTYPE_F16
+        scale = 1.0 / float(np.sqrt(self.d))
+        kc = [t.data_ptr() for t in self.k_cache]
+        vc = [t.data_ptr() for t in self.v_cache]
+        NB, Hq, Hkv, d = self.NB, self.Hq, self.Hkv, self.d
+        self.host_ms += (time.perf_counter() - t0) * 1e3 - waited
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev[0].record(self.stream)
         for layer in range(self.L):
             cid = layer % self.R
             fill(layer, cid, q, k, v, trids, tpos)
-            B.kv_append(k, v, slots, self.k_cache[cid], self.v_cache[cid], dev_status=self.status, stream=self.stream)
-            if P:
-                B.paged_prefill_attention(out[:t1], q[:t1], cu[:P + 1], max_q, self.k_cache[cid], self.v_cache[cid],
-                                          tables[:P], ctx[:P], dev_status=self.status, stream=self.stream)
-            if S > P:
-                B.paged_decode_attention(out[t1:], q[t1:], self.k_cache[cid], self.v_cache[cid], tables[P:], ctx[P:],
-                                         workspace=self.work, dev_status=self.status, stream=self.stream)
+            rc = L.pkv_kv_append(pk, pv, pslots, T, kc[cid], vc[cid], NB, 16, Hkv, d, dt, pst, pstream)
+            if rc == B.PKV_OK and P:
+                rc = L.pkv_paged_prefill_attention(pout, pq, pcu, P, max_q, t1, kc[cid], vc[cid], ptab, MB, pctx, NB,
+                                                   Hq, Hkv, d, 16, scale, dt, dt, pst, pstream)
+            if rc == B.PKV_OK and S > P:
+                rc = L.pkv_paged_decode_attention(pout + t1 * row_q, pq + t1 * row_q, kc[cid], vc[cid],
+                                                  ptab + P * MB * 4, MB, pctx + P * 4, S - P, NB, Hq, Hkv, d, 16,
+                                                  scale, dt, dt, pwork, nwork, pst, pstream)
+            if rc != B.PKV_OK:
+                raise B.PkvError("engine step, layer %d" % layer, rc)
             if on_layer_done is not None:
                 on_layer_done(layer, info, out)
+        ev[1].record(self.stream)
+        info["events"] = ev
         return info
 
 
@@ -163,10 +188,13 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
             for rid in info["finished"]:
                 finish_step[int(rid)] = step
             steps.append({"step": step, "S": info["S"], "T": info["T"], "P": info["P"],
-                          "context_lens": info["context_lens"], "q_lens": info["q_lens"]})
+                          "context_lens": info["context_lens"], "q_lens": info["q_lens"], "events": info["events"]})
         if nxt >= n and len(finish_step) == n:
             break
     ev1.record(engine.stream)
     torch.cuda.synchronize()
+    for s in steps:   # device time of each step's layer launches
+        e = s.pop("events")
+        s["device_ms"] = e[0].elapsed_time(e[1])
     return {"steps": steps, "finish_step": finish_step, "wall_s": time.perf_counter() - t_wall,
             "stream_ms": ev0.elapsed_time(ev1), "samples": samples}
