@@ -105,9 +105,11 @@ int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int
                   int head_dim, int dtype, int *dev_status, void *stream);
 
 /*
- * Bytes of device workspace pkv_paged_decode_attention needs on the current
- * device for these head counts and head_dim (independent of the contexts).
- * Returns 0 if no device is current.
+ * Bytes of device workspace pkv_paged_decode_attention should be given on the
+ * current device for these head counts and head_dim (independent of the
+ * contexts).  The call also accepts less, down to two partial records per
+ * warp of its grid (it then rebalances work between SMs less); below that it
+ * returns PKV_ERR_WORKSPACE.  Returns 0 if no device is current.
  */
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 
@@ -137,9 +139,15 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  *                  ignored.  Owned by the caller; must not be used by another
  *                  call that may run concurrently.
  *   dev_status     device int or NULL (see conventions)
- * The KV range of every (sequence, KV head) pair is split across warps so
- * every SM gets the same number of blocks; split ranges are combined by a
- * log-sum-exp merge in a second small kernel on the same stream.
+ * One persistent kernel: every warp starts on an equal share of the
+ * (sequence, KV head, block) list, and warps that finish early take over the
+ * far half of busier warps' unclaimed blocks.  A (sequence, KV head) range
+ * processed in several pieces is combined by a log-sum-exp merge, done by the
+ * warp that finishes the range's last block, pieces taken in block order.
+ * Which blocks are taken over depends on timing, so the last bits of the
+ * output may differ from call to call; with the environment variable
+ * PKV_DETERMINISTIC=1 (read at every call) nothing is taken over and equal
+ * inputs give equal bits.
  */
 int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                                const int32_t *block_tables, int max_blocks_per_seq,
@@ -191,9 +199,10 @@ int pkv_paged_prefill_attention(void *out, const void *q, const int32_t *cu_seql
  * until the process exits).  It calls no cudaMalloc/cudaFree and no
  * allocating library routine.
  *
- * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS and a shape whose
- *   pkv_decode_workspace_size() fits in PKV_STATIC_SCRATCH_BYTES (every
- *   supported head_dim/group size does on a 152-SM GB300); otherwise
+ * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS and a shape whose smallest
+ *   accepted workspace (see pkv_decode_workspace_size) fits in
+ *   PKV_STATIC_SCRATCH_BYTES (every supported head_dim/group size does on a
+ *   152-SM GB300; the rest of the array is room for rebalancing); otherwise
  *   PKV_ERR_WORKSPACE is returned before anything is enqueued, and
  *   pkv_last_cuda_error() names the limit.
  * - The first call on each device looks up the array's device address

@@ -1,4 +1,4 @@
-// K2 + K3: paged decode attention with a split KV range and a log-sum-exp merge.
+// K2 + K3: paged decode attention with split KV ranges and a log-sum-exp merge.
 //
 // What is computed: "Project 17: Production Serving: Continuous Batching and
 // PagedAttention", Step 6 "Implement attention over paged storage" -- walk a
@@ -7,13 +7,20 @@
 // values -- per query head, with query head h reading KV head h / G.
 //
 // How (GB300):
-//  * Work = the flat list of (sequence, KV head, block) triples, cut into equal
-//    contiguous ranges, one per warp of a persistent grid (one CTA of 8 warps
-//    per SM).  Every warp streams the same number of 16-token blocks, whatever
-//    the context-length mix; a (sequence, head) range that crosses a warp
-//    boundary leaves per-warp partials (m, l, acc), and the warp that finishes
-//    the range's last piece combines them by log-sum-exp (an arrival counter
-//    per range, tagged with the call's epoch, tells it that it is last).
+//  * Work = the flat list of (sequence, KV head, block) triples.  Every warp
+//    of a persistent grid (one CTA of 8 warps per SM) starts on an equal
+//    contiguous range of it and claims its blocks a few at a time with one
+//    atomic add on its range word (begin and end packed in 64 bits).  The SMs
+//    of one GPU do not stream at the same rate, so equal ranges finish at
+//    different times: a warp that runs out of work steals the far half of the
+//    unclaimed blocks of the busiest warp it can see, with one compare-and-
+//    swap on the same word, and streams that piece too.  Owner and thief can
+//    never both get a block.
+//  * A (sequence, KV head) range processed in more than one piece leaves one
+//    partial record (m, l, acc) per piece on a per-range list; a per-range
+//    counter of finished blocks (tagged with the call's epoch, so the
+//    workspace never needs clearing) tells the warp that finishes the range's
+//    last block to combine the records by log-sum-exp.
 //  * Each warp runs its own ring of STAGES shared-memory slots.  Lane 0 issues
 //    2-D TMA loads (128-byte swizzle) of the K and V tiles of a block -- the
 //    block id comes from the block table -- and the warp waits on the slot's
@@ -28,6 +35,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 
 #include "pkv.h"
 #include "pkv_device.cuh"
@@ -37,19 +45,29 @@ namespace pkv {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a tile that has not landed in 2 s never will
 constexpr int kDecodeWarps = 8;
+constexpr int kClaimBatch = 4;      // blocks an owner claims per atomic add
+constexpr int kStealMin = 10;       // unclaimed blocks a warp must hold to be robbed
+constexpr int kMaxWarpBlocks = 1 << 22;   // range offsets live in 24-bit fields
+constexpr int kMinWarpBlocks = 20;  // a small step uses fewer warps, each with at least this many blocks
 
 struct DecodeParams {
     void *out;
     const void *q;
     const int32_t *block_tables;
     const int32_t *context_lens;
-    float *part;        // [2 * total_warps][record] partial results
-    unsigned long long *arrivals;   // [S * Hkv]: (epoch << 32) | pieces arrived
+    unsigned long long *seg_done;   // [S * Hkv]: (epoch << 32) | blocks of the range finished
+    unsigned long long *seg_list;   // [S * Hkv]: (epoch << 32) | 1 + first partial record (0: none)
+    unsigned long long *ranges;     // [total_warps]: (tag << 48) | (end << 24) | begin
+    unsigned long long *ctl;        // [0] CTAs ready, [1] steals reserved, [2] records taken, [3] drained
+    long long *prefix;              // [S + 1]: blocks before sequence s (written by CTA 0)
+    float *part;                    // [pool_cap][rec_floats] partial records
     int *dev_status;
     int S, max_blocks, num_blocks, Hq, Hkv, G;
     float scale_log2;   // scale * log2(e): scores are kept in base-2 units
     int out_dtype;
     int total_warps;
+    int rec_floats;     // m[G], l[G], acc[G][D], next, first block, padding to 16 B
+    int pool_cap, steal_cap;
     uint32_t epoch;     // nonzero, different for every call
 };
 
@@ -60,8 +78,7 @@ struct DecodeShape {
     static constexpr int TILE_BYTES = HALVES * HALF_BYTES;
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K + V
     static constexpr int STAGES = D == 128 ? 3 : 6;
-    static constexpr int HP = 8 * NT;                   // heads held by a partial record
-    static constexpr int REC = 2 * HP + HP * D;         // m[HP], l[HP], acc[HP][D]
+    static constexpr int HP = 8 * NT;                   // heads an MMA tile holds
     static constexpr int RING_BYTES = kDecodeWarps * STAGES * STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + RING_BYTES + kDecodeWarps * STAGES * 8 + 256;
 };
@@ -105,51 +122,137 @@ __device__ __forceinline__ int64_t block_scan(int64_t v, int64_t *sh, int64_t *t
 
 __device__ __forceinline__ int64_t range_lo(int64_t w, int64_t total, int64_t nw) { return w * total / nw; }
 
-// The warp whose range holds flat position x: the largest w with range_lo(w) <= x.
-__device__ __forceinline__ int64_t owner_of(int64_t x, int64_t total, int64_t nw) {
-    return ((x + 1) * nw + total - 1) / total - 1;
+// ---- range words: (tag << 48) | (end << 24) | begin, offsets from the warp's range start
+__device__ __forceinline__ int rw_begin(unsigned long long w) { return (int)(w & 0xFFFFFFull); }
+__device__ __forceinline__ int rw_end(unsigned long long w) { return (int)((w >> 24) & 0xFFFFFFull); }
+__device__ __forceinline__ uint32_t rw_tag(unsigned long long w) { return (uint32_t)(w >> 48); }
+__device__ __forceinline__ unsigned long long rw_make(uint32_t tag, int b, int e) {
+    return ((unsigned long long)(tag & 0xFFFFu) << 48) | ((unsigned long long)e << 24) | (unsigned long long)b;
 }
 
-// Counts one more finished piece of a split (sequence, KV head) range and
-// returns how many have finished in this call.  The counter carries the call's
-// epoch in its high half, so a value left by an earlier call counts as zero
-// and the workspace never needs clearing.  Returns 0 if the update kept losing
-// races (not expected: at most a handful of warps share a range).
-__device__ __forceinline__ uint32_t count_arrival(unsigned long long *ctr, uint32_t epoch) {
-    unsigned long long cur = atomicAdd(ctr, 0ull);
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long *p, unsigned long long cmp,
+                                                          unsigned long long val) {
+    unsigned long long prev;
+    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(prev) : "l"(p), "l"(cmp), "l"(val)
+                 : "memory");
+    return prev;
+}
+
+// Adds n to an epoch-tagged counter ((epoch << 32) | count) and returns the
+// new count of this call; a value left by an earlier call counts as zero.
+// Acquire and release: it publishes this thread's earlier writes and sees
+// those of every earlier adder.  Returns 0 if the update kept losing races.
+__device__ __forceinline__ uint32_t epoch_add(unsigned long long *ctr, uint32_t epoch, uint32_t n) {
+    unsigned long long cur = ld_relaxed_u64(ctr);
     for (int it = 0; it < (1 << 16); ++it) {
         const unsigned long long want =
-            (uint32_t)(cur >> 32) == epoch ? cur + 1ull : (((unsigned long long)epoch << 32) | 1ull);
-        unsigned long long prev;
-        asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;"
-                     : "=l"(prev)
-                     : "l"(ctr), "l"(cur), "l"(want)
-                     : "memory");
+            (uint32_t)(cur >> 32) == epoch ? cur + n : (((unsigned long long)epoch << 32) | n);
+        const unsigned long long prev = cas_acq_rel(ctr, cur, want);
         if (prev == cur) return (uint32_t)(want & 0xffffffffull);
         cur = prev;
     }
     return 0;
 }
 
-// Log-sum-exp combination of the partial records of one split range, run by
-// the warp that finished its last piece.  Records: warp w0 left its piece in
-// slot 1 (range ended past its end), later warps in slot 0.  Lane hh folds the
-// (max, sum) pairs of head hh over the pieces; then every lane accumulates its
-// D/32 output columns of every head, with all loads of a piece independent.
+// Shared counters hit by every warp of the grid ((epoch << 32) | count): each
+// CTA first moves a counter left by an earlier call to (epoch, 0) -- only the
+// first such swap succeeds, later ones see this epoch -- and then counts with
+// plain atomic adds, which do not serialise the way a compare-and-swap loop
+// does under contention.
+__device__ __forceinline__ void epoch_open(unsigned long long *ctr, uint32_t epoch) {
+    const unsigned long long v = ld_relaxed_u64(ctr);
+    if ((uint32_t)(v >> 32) != epoch) atomicCAS(ctr, v, (unsigned long long)epoch << 32);
+}
+
+// Count after adding n to an opened counter (0 if it was not opened).
+__device__ __forceinline__ uint32_t epoch_fetch_add(unsigned long long *ctr, uint32_t epoch, uint32_t n) {
+    const unsigned long long old = atomicAdd(ctr, (unsigned long long)n);
+    return (uint32_t)(old >> 32) == epoch ? (uint32_t)old + n : 0u;
+}
+
+// The sequence holding flat triple x (the last s with prefix[s] * Hkv <= x,
+// which skips empty sequences), by a 32-way search of the prefix array.
+__device__ __forceinline__ int locate_seq(const DecodeParams &p, int64_t x, int lane) {
+    int lo = 0, hi = p.S;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) / 32;
+        const int c = lo + lane * step;
+        const bool le = c < hi && __ldcg(p.prefix + c) * p.Hkv <= x;
+        const unsigned m = __ballot_sync(0xffffffffu, le);
+        const int k = 31 - __clz(m);
+        lo += k * step;
+        hi = min(hi, lo + step);
+    }
+    return lo;
+}
+
+// Log-sum-exp combination of the partial records on the list of (s, h), run
+// by the warp that finished the range's last block.  The records are taken in
+// the order of their first block (not the order they were linked), so a given
+// split always combines to the same bits.  Lane hh folds the (max, sum) pairs
+// of head hh; then every lane accumulates its D/32 output columns of every
+// head.
 template <typename T, int D, int NT>
-__device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t w0, int64_t w1, int64_t total,
-                                             int64_t nw, int s, int h, int lane) {
-    using Sh = DecodeShape<D, NT>;
-    constexpr int HP = Sh::HP, PER = D / 32;
+__device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, int lane) {
+    constexpr int HP = 8 * NT, PER = D / 32;
     const int G = p.G;
-    auto rec_of = [&](int64_t w) { return p.part + (size_t)(w * 2 + (w == w0 ? 1 : 0)) * Sh::REC; };
-    auto empty_range = [&](int64_t w) { return range_lo(w + 1, total, nw) == range_lo(w, total, nw); };
+    const int next_at = 2 * G + G * D;
+    auto rec_of = [&](uint32_t idx1) { return p.part + (size_t)(idx1 - 1) * p.rec_floats; };
+    // lane k takes the k-th record of the list: (first block, record)
+    uint32_t r = (uint32_t)ld_acquire_u64(p.seg_list + (size_t)s * p.Hkv + h);
+    int n = 0;
+    int key = INT32_MAX;
+    uint32_t mine = 0u;
+    while (r != 0u && n < 32) {
+        const float *rec = rec_of(r);
+        if (lane == n) {
+            key = __float_as_int(__ldcg(rec + next_at + 1));
+            mine = r;
+        }
+        r = __float_as_uint(__ldcg(rec + next_at));
+        ++n;
+    }
+    const uint32_t rest = r;   // pieces past the 32nd (not produced by the usual splits) follow in list order
+    // bitonic sort of the 32 (key, record) pairs by key, ascending
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const int ok = __shfl_xor_sync(0xffffffffu, key, j);
+            const uint32_t om = __shfl_xor_sync(0xffffffffu, mine, j);
+            const bool up = (lane & k) == 0;
+            const bool lower = (lane & j) == 0;
+            const bool take = lower == up ? ok < key : ok > key;
+            if (take) {
+                key = ok;
+                mine = om;
+            }
+        }
+    }
+    auto record_k = [&](int k, uint32_t &walk) -> const float * {
+        if (k < n) return rec_of(__shfl_sync(0xffffffffu, mine, k));
+        const float *rec = rec_of(walk);
+        walk = __float_as_uint(__ldcg(rec + next_at));
+        return rec;
+    };
     float M = -INFINITY, L = 0.f;
-    if (lane < G) {
-        for (int64_t w = w0; w <= w1; ++w) {
-            if (empty_range(w)) continue;
-            const float *rec = rec_of(w);
-            const float mv = __ldcg(rec + lane), lv = __ldcg(rec + HP + lane);
+    uint32_t walk = rest;
+    for (int k = 0; k < n || walk != 0u; ++k) {
+        const float *rec = record_k(k, walk);
+        if (lane < G) {
+            const float mv = __ldcg(rec + lane), lv = __ldcg(rec + G + lane);
             const float Mn = fmaxf(M, mv);
             L = L * exp2_approx(M - Mn) + lv * exp2_approx(mv - Mn);
             M = Mn;
@@ -163,16 +266,16 @@ __device__ __forceinline__ void merge_pieces(const DecodeParams &p, int64_t w0, 
 #pragma unroll
         for (int k = 0; k < PER; ++k) o[hh][k] = 0.f;
     }
-    for (int64_t w = w0; w <= w1; ++w) {
-        if (empty_range(w)) continue;
-        const float *rec = rec_of(w);
+    walk = rest;
+    for (int k = 0; k < n || walk != 0u; ++k) {
+        const float *rec = record_k(k, walk);
 #pragma unroll
         for (int hh = 0; hh < HP; ++hh) {
             if (hh < G) {
                 const float f = exp2_approx(__ldcg(rec + hh) - Mh[hh]) * invL[hh];
-                const float *racc = rec + 2 * HP + hh * D;
+                const float *racc = rec + 2 * G + hh * D;
 #pragma unroll
-                for (int k = 0; k < PER; ++k) o[hh][k] += f * __ldcg(racc + lane + 32 * k);
+                for (int k2 = 0; k2 < PER; ++k2) o[hh][k2] += f * __ldcg(racc + lane + 32 * k2);
             }
         }
     }
@@ -199,23 +302,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int64_t *sh_scan = reinterpret_cast<int64_t *>(bars + kDecodeWarps * STAGES);
     int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);   // segment holding each warp's first block
     int *plan_off = plan_s + kDecodeWarps;
-    int *plan_s2 = plan_off + kDecodeWarps;                             // ... and its last block
-    int *plan_off2 = plan_s2 + kDecodeWarps;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int Hkv = p.Hkv;
+    const int Hkv = p.Hkv, G = p.G;
+    const uint32_t tag = p.epoch & 0xFFFFu;
 
     // inputs may come from the previous kernel on the stream (the append)
     pdl_wait_primary();
     pdl_launch_dependents();
 
-    // ---- plan: total blocks, this CTA's warp ranges, per-sequence offsets ----
+    if (tid == 0)
+        for (int k = 0; k < 3; ++k) epoch_open(p.ctl + k, p.epoch);
+
+    // ---- plan: total blocks, this CTA's warp starts; CTA 0 publishes the
+    // per-sequence block offsets that thieves search ----
     int64_t local = 0;
     for (int s = tid; s < p.S; s += blockDim.x) local += blocks_of(p.context_lens, s, p.max_blocks, p.dev_status, nullptr);
     int64_t total_nblk;
     block_scan(local, sh_scan, &total_nblk);
     const int64_t total = total_nblk * Hkv;
-    const int64_t nw = p.total_warps;
+    // warps that get a share: all of them, unless the step is too small to
+    // give each at least kMinWarpBlocks blocks
+    int64_t nw = (total + kMinWarpBlocks - 1) / kMinWarpBlocks;
+    if (nw > p.total_warps) nw = p.total_warps;
+    if (nw < 1) nw = 1;
     if (tid < kDecodeWarps) plan_s[tid] = -1;
     __syncthreads();
     int64_t carry = 0;
@@ -224,24 +334,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         const int nb = s < p.S ? blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) : 0;
         int64_t tile_total;
         const int64_t excl = carry + block_scan(nb, sh_scan, &tile_total) - nb;
+        if (blockIdx.x == 0 && s < p.S) p.prefix[s] = excl;
         if (nb > 0) {
 #pragma unroll
             for (int w = 0; w < kDecodeWarps; ++w) {
-                const int64_t lo = range_lo((int64_t)blockIdx.x * kDecodeWarps + w, total, nw);
-                const int64_t last = range_lo((int64_t)blockIdx.x * kDecodeWarps + w + 1, total, nw) - 1;
-                if (lo >= excl * Hkv && lo < (excl + nb) * Hkv) {
+                const int64_t ww = (int64_t)blockIdx.x * kDecodeWarps + w;
+                const int64_t lo = range_lo(ww, total, nw);
+                if (ww < nw && lo >= excl * Hkv && lo < (excl + nb) * Hkv) {
                     plan_s[w] = s;
                     plan_off[w] = (int)(lo - excl * Hkv);
                 }
-                if (last >= excl * Hkv && last < (excl + nb) * Hkv) {
-                    plan_s2[w] = s;
-                    plan_off2[w] = (int)(last - excl * Hkv);
-                }
+
             }
         }
         carry += tile_total;
     }
-    __syncthreads();
+    if (blockIdx.x == 0 && tid == 0) p.prefix[p.S] = total_nblk;
 
     // sequences with an empty context get all-zero rows
     for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
@@ -249,10 +357,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         for (int e = tid; e < p.Hq * D; e += blockDim.x) store_out<T>(p.out, p.out_dtype, (int64_t)s * p.Hq * D + e, 0.f);
     }
 
+    // every warp publishes its range word; the CTA then counts itself ready
+    // (thieves rob no warp before every CTA has published)
     const int64_t wg = (int64_t)blockIdx.x * kDecodeWarps + warp;
-    const int64_t lo_w = range_lo(wg, total, nw);
-    const int n = (int)(range_lo(wg + 1, total, nw) - lo_w);
-    if (n <= 0 || plan_s[warp] < 0) return;
+    const int64_t lo_w = wg < nw ? range_lo(wg, total, nw) : total;
+    const int n_own = wg < nw ? (int)(range_lo(wg + 1, total, nw) - lo_w) : 0;
+    if (lane == 0) p.ranges[wg] = rw_make(tag, 0, n_own);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) epoch_fetch_add(&p.ctl[0], p.epoch, 1);
 
     // ---- this warp's ring ----
     uint8_t *wring = ring + warp * STAGES * Sh::STAGE_BYTES;
@@ -268,363 +381,488 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     __syncwarp();
     const uint64_t policy = l2_policy_evict_first();
 
-    // Block order inside the range: if the range's last (sequence, KV head)
-    // segment continues into the next warp, that tail piece is streamed first,
-    // then the range from its start.  Both pieces of a split segment are then
-    // finished early in the kernel, so the warp that combines them does so
-    // while the other warps keep HBM busy, not at the very end.
-    const int s_head = plan_s[warp], off_head = plan_off[warp];
-    const int nb_head = blocks_of(p.context_lens, s_head, p.max_blocks, nullptr, nullptr);
-    const int s_last = plan_s2[warp];
-    const int nb_last = blocks_of(p.context_lens, s_last, p.max_blocks, nullptr, nullptr);
-    const int j_last = plan_off2[warp] % nb_last;
-    const int64_t t_start = lo_w + n - 1 - j_last;                  // flat start of the last segment
-    const int n_tail = (j_last < nb_last - 1 && t_start > lo_w) ? (int)(lo_w + n - t_start) : 0;
-
-    auto next_seq = [&](int s, int &nb_out, int *ctx_out) {
-        int nb;
-        do {
-            ++s;
-            nb = blocks_of(p.context_lens, s, p.max_blocks, nullptr, ctx_out);
-        } while (nb == 0);
-        nb_out = nb;
-        return s;
-    };
-    // consumer (c*) and producer (p*) cursors over (sequence, head, block)
-    int cs, c_ctx, c_nb, ch, cj;
-    auto seek_head = [&](int &s_, int &nb_, int &h_, int &j_, int *ctx_) {
-        s_ = s_head;
-        nb_ = blocks_of(p.context_lens, s_, p.max_blocks, nullptr, ctx_);
-        h_ = off_head / nb_;
-        j_ = off_head % nb_;
-    };
-    if (n_tail > 0) {
-        cs = s_last;
-        c_nb = blocks_of(p.context_lens, cs, p.max_blocks, nullptr, &c_ctx);
-        ch = plan_off2[warp] / c_nb;
-        cj = 0;
-    } else {
-        seek_head(cs, c_nb, ch, cj, &c_ctx);
-    }
-    int ps = cs, p_nb = c_nb, ph = ch, pj = cj;
-    bool started_mid = n_tail == 0 && cj != 0;
-    (void)nb_head;
-
-    auto table_entry = [&]() { return __ldg(p.block_tables + (int64_t)ps * p.max_blocks + pj); };
-    // move the producer from block k of the warp's order to block k + 1
-    auto advance_producer = [&](int k) {
-        if (k + 1 == n_tail) {
-            seek_head(ps, p_nb, ph, pj, nullptr);
-            return;
-        }
-        if (++pj == p_nb) {
-            pj = 0;
-            if (++ph == Hkv) {
-                ph = 0;
-                ps = next_seq(ps, p_nb, nullptr);
-            }
-        }
-    };
-    auto issue = [&](int stage, int blk) {
-        if (lane == 0) {
-            int row = (blk * Hkv + ph) * 16;
-            if (blk < 0 || blk >= p.num_blocks) {
-                set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                row = p.num_blocks * Hkv * 16;   // past the end: the load fills zeros
-            }
-            uint64_t *bar = &wbar[stage];
-            mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES);
-            uint8_t *kdst = wring + stage * Sh::STAGE_BYTES;
-            uint8_t *vdst = kdst + Sh::TILE_BYTES;
-#pragma unroll
-            for (int hf = 0; hf < Sh::HALVES; ++hf) {
-                tma_load_2d(kdst + hf * Sh::HALF_BYTES, &tk, hf * 64, row, bar, policy);
-                tma_load_2d(vdst + hf * Sh::HALF_BYTES, &tv, hf * 64, row, bar, policy);
-            }
-        }
-    };
-
-    // prologue: fill the ring
-    int pending = table_entry();
-    const int pro = n < STAGES ? n : STAGES;
-    for (int k = 0; k < pro; ++k) {
-        issue(k, pending);
-        if (k + 1 < n) {
-            advance_producer(k);
-            pending = table_entry();
-        }
-    }
-
     const int g = lane >> 2, t4 = lane & 3;
     const int mi = lane >> 3;
     const int ld_row = ((mi >> 1) << 3) + (lane & 7);          // token row this lane addresses
     const int ld_sw = ld_row & 7;                               // 128-byte swizzle phase of that row
     const uint32_t ring_addr = smem_addr(wring);
 
-    uint32_t qa[D / 16][4];
-    float acc[D / 16][NT][4];
-    float m_run[NT], l_run[NT];
-    bool seg_fresh = true;
+    uint32_t slot_base = 0;     // ring slots used by earlier pieces of work (phases continue)
+    bool steal_reserved = false;
 
-    const int G = p.G;
-    for (int i = 0; i < n; ++i) {
-        if (seg_fresh) {
-            // query fragments of (cs, ch): rows = heads of the group (padded to 16)
-            const uint32_t *qbase = reinterpret_cast<const uint32_t *>(
-                static_cast<const T *>(p.q) + ((int64_t)cs * p.Hq + (int64_t)ch * G) * D);
+    // Work: first the warp's own range (claimed in batches), then stolen pieces.
+    int64_t x0 = lo_w;          // flat start of the current work
+    int len = n_own;            // its length in blocks
+    bool own = true;
+    int s0 = plan_s[warp], off0 = plan_off[warp];
+    for (;;) {
+        if (len > 0 && s0 >= 0) {
+            // ---------------- stream [x0, x0 + len) ----------------
+            auto next_seq = [&](int s, int &nb_out, int *ctx_out) {
+                int nb;
+                do {
+                    ++s;
+                    nb = blocks_of(p.context_lens, s, p.max_blocks, nullptr, ctx_out);
+                } while (nb == 0);
+                nb_out = nb;
+                return s;
+            };
+            int cs = s0, c_ctx, c_nb, ch, cj;
+            c_nb = blocks_of(p.context_lens, cs, p.max_blocks, nullptr, &c_ctx);
+            ch = off0 / c_nb;
+            cj = off0 % c_nb;
+            int ps = cs, p_nb = c_nb, ph = ch, pj = cj;
+            auto table_entry = [&]() { return __ldg(p.block_tables + (int64_t)ps * p.max_blocks + pj); };
+            auto advance_producer = [&]() {
+                if (++pj == p_nb) {
+                    pj = 0;
+                    if (++ph == Hkv) {
+                        ph = 0;
+                        ps = next_seq(ps, p_nb, nullptr);
+                    }
+                }
+            };
+            auto issue = [&](uint32_t slot, int blk) {
+                if (lane == 0) {
+                    int row = (blk * Hkv + ph) * 16;
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                        row = p.num_blocks * Hkv * 16;   // past the end: the load fills zeros
+                    }
+                    const int stage = (int)(slot % STAGES);
+                    uint64_t *bar = &wbar[stage];
+                    mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES);
+                    uint8_t *kdst = wring + stage * Sh::STAGE_BYTES;
+                    uint8_t *vdst = kdst + Sh::TILE_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const int c0 = (kk * 16 + 2 * t4) >> 1;
-                qa[kk][0] = g < G ? __ldg(qbase + g * (D / 2) + c0) : 0u;
-                qa[kk][2] = g < G ? __ldg(qbase + g * (D / 2) + c0 + 4) : 0u;
-                if constexpr (NT == 1) {   // group of at most 8 heads: rows 8..15 are padding
-                    qa[kk][1] = 0u;
-                    qa[kk][3] = 0u;
-                } else {
-                    qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0) : 0u;
-                    qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0 + 4) : 0u;
+                    for (int hf = 0; hf < Sh::HALVES; ++hf) {
+                        tma_load_2d(kdst + hf * Sh::HALF_BYTES, &tk, hf * 64, row, bar, policy);
+                        tma_load_2d(vdst + hf * Sh::HALF_BYTES, &tv, hf * 64, row, bar, policy);
+                    }
+                }
+            };
+            auto wait_slot = [&](uint32_t slot, uint64_t limit) {
+                return mbar_wait(&wbar[slot % STAGES], (slot / STAGES) & 1u, limit);
+            };
+
+            // claims: blocks [0, limit) are this warp's; an own range asks for
+            // kClaimBatch more with one atomic add, a batch ahead of use
+            int limit = own ? 0 : len;
+            bool more = own;
+            unsigned long long claim = 0;
+            if (own && lane == 0) claim = atomicAdd(p.ranges + wg, (unsigned long long)kClaimBatch);
+
+            // prologue: fill the ring (loads run ahead of the claims; a load
+            // of a block that turns out not to be ours is only waited out)
+            int issued = 0;
+            int pending = table_entry();
+            const int pro = len < STAGES ? len : STAGES;
+            for (; issued < pro; ++issued) {
+                issue(slot_base + issued, pending);
+                if (issued + 1 < len) {
+                    advance_producer();
+                    pending = table_entry();
                 }
             }
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt)
-#pragma unroll
-                for (int pn = 0; pn < NT; ++pn)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[mt][pn][e] = 0.f;
-#pragma unroll
-            for (int pn = 0; pn < NT; ++pn) {
-                m_run[pn] = -INFINITY;
-                l_run[pn] = 0.f;
-            }
-            seg_fresh = false;
-        }
 
-        const int stage = i % STAGES;
-        const bool landed = mbar_wait(&wbar[stage], (uint32_t)((i / STAGES) & 1), kWaitLimitNs);
-        if (!__all_sync(0xffffffffu, landed)) {
-            set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
-            // let the copies this warp still has in flight land before leaving
-            for (int k = i + 1; k < n && k < i + STAGES; ++k)
-                mbar_wait(&wbar[k % STAGES], (uint32_t)((k / STAGES) & 1), kWaitLimitNs / 8);
-            return;
-        }
-        const uint32_t kbase = ring_addr + stage * Sh::STAGE_BYTES;
-        const uint32_t vbase = kbase + Sh::TILE_BYTES;
+            uint32_t qa[D / 16][4];
+            float acc[D / 16][NT][4];
+            float m_run[NT], l_run[NT];
+            bool seg_fresh = true;
+            int piece_j0 = cj, piece_n = 0;
 
-        // ---- pull the block's K and V fragments into registers, then hand the
-        // slot straight back to the TMA engine: the slot is held for the
-        // ldmatrix reads only, not for the whole block's arithmetic ----
-        uint32_t kf[D / 16][4], vf[D / 16][4];
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const int chunk = ((kk & 3) << 1) + (mi & 1);
-            const uint32_t off = (kk >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
-            ldsm_x4(kbase + off, kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
-            ldsm_x4_t(vbase + off, vf[kk][0], vf[kk][1], vf[kk][2], vf[kk][3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (i + STAGES < n) {
-            issue(stage, pending);
-            if (i + STAGES + 1 < n) {
-                advance_producer(i + STAGES);
-                pending = table_entry();
-            }
-        }
-
-        // ---- S = Q K^T over the 16 tokens of this block ----
-        float sacc[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
-        // two accumulator chains per n-tile (even / odd k-steps) halve the
-        // dependent MMA chain
-        float sacc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kk = 0; kk < D / 16; kk += 2) {
-            mma_16816<T>(sacc[0], qa[kk], kf[kk][0], kf[kk][1]);
-            mma_16816<T>(sacc[1], qa[kk], kf[kk][2], kf[kk][3]);
-            mma_16816<T>(sacc2[0], qa[kk + 1], kf[kk + 1][0], kf[kk + 1][1]);
-            mma_16816<T>(sacc2[1], qa[kk + 1], kf[kk + 1][2], kf[kk + 1][3]);
-        }
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
-
-        // ---- mask, online softmax (base 2) ----
-        const int lim = c_ctx - cj * 16;   // valid tokens in this block (>= 16: all)
-        float pr[2][4];
-        float alpha[NT];
-#pragma unroll
-        for (int pn = 0; pn < NT; ++pn) {
-            float x[2][2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = nt * 8 + 2 * t4 + e;
-                    x[nt][e] = tok < lim ? sacc[nt][pn * 2 + e] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, x[nt][e]);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run[pn], mx);
-            alpha[pn] = exp2_approx(m_run[pn] - m_new);
-            m_run[pn] = m_new;
-            float rs = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    pr[nt][pn * 2 + e] = exp2_approx(x[nt][e] - m_new);
-                    rs += pr[nt][pn * 2 + e];
-                }
-            l_run[pn] = l_run[pn] * alpha[pn] + rs;
-        }
-
-        // tokens beyond the context may hold anything (even NaN): clear their
-        // V values in the fragments so 0-weight x garbage cannot reach the
-        // accumulator.  Fragment registers 0/1 hold tokens 2*t4 (low half)
-        // and 2*t4+1 (high half); registers 2/3 the same tokens + 8.
-        if (lim < 16) {
-            const uint32_t m01 = (2 * t4 < lim ? 0x0000ffffu : 0u) | (2 * t4 + 1 < lim ? 0xffff0000u : 0u);
-            const uint32_t m23 = (2 * t4 + 8 < lim ? 0x0000ffffu : 0u) | (2 * t4 + 9 < lim ? 0xffff0000u : 0u);
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                vf[mt][0] &= m01;
-                vf[mt][1] &= m01;
-                vf[mt][2] &= m23;
-                vf[mt][3] &= m23;
-            }
-        }
-
-        // ---- rescale the accumulator (skipped when no row max moved, the
-        // common case once a range is under way), O^T += V^T P^T ----
-        bool moved = false;
-#pragma unroll
-        for (int pn = 0; pn < NT; ++pn) moved |= alpha[pn] != 1.f;
-        if (__any_sync(0xffffffffu, moved))
-#pragma unroll
-        for (int pn = 0; pn < NT; ++pn) {
-            const float a_lo = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4);
-            const float a_hi = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4 + 4);
-#pragma unroll
-            for (int mt = 0; mt < D / 16; ++mt) {
-                acc[mt][pn][0] *= a_lo;
-                acc[mt][pn][1] *= a_hi;
-                acc[mt][pn][2] *= a_lo;
-                acc[mt][pn][3] *= a_hi;
-            }
-        }
-        uint32_t pb0[NT][2], pb1[NT][2];
-#pragma unroll
-        for (int pn = 0; pn < NT; ++pn) {
-            pack2_split<T>(pr[0][pn * 2], pr[0][pn * 2 + 1], pb0[pn][0], pb0[pn][1]);
-            pack2_split<T>(pr[1][pn * 2], pr[1][pn * 2 + 1], pb1[pn][0], pb1[pn][1]);
-        }
-#pragma unroll
-        for (int mt = 0; mt < D / 16; ++mt) {
-#pragma unroll
-            for (int pn = 0; pn < NT; ++pn) {
-                mma_16816<T>(acc[mt][pn], vf[mt], pb0[pn][0], pb1[pn][0]);
-                mma_16816<T>(acc[mt][pn], vf[mt], pb0[pn][1], pb1[pn][1]);
-            }
-        }
-
-        // ---- end of a (sequence, head) range in this warp ----
-        const bool seg_done = cj == c_nb - 1;
-        if (seg_done || i == n - 1 || i == n_tail - 1) {
-            float lsum[NT];
-#pragma unroll
-            for (int pn = 0; pn < NT; ++pn) {
-                lsum[pn] = l_run[pn];
-                lsum[pn] += __shfl_xor_sync(0xffffffffu, lsum[pn], 1);
-                lsum[pn] += __shfl_xor_sync(0xffffffffu, lsum[pn], 2);
-            }
-            const int head0 = ch * G;
-            if (!started_mid && seg_done) {
-                // whole range in this warp: normalise and store
+            // closes the piece of (cs, ch) that ends with block cj of this warp
+            auto finish_piece = [&]() {
+                float lsum[NT];
 #pragma unroll
                 for (int pn = 0; pn < NT; ++pn) {
-                    const float inv_lo = 1.f / __shfl_sync(0xffffffffu, lsum[pn], 8 * t4);
-                    const float inv_hi = 1.f / __shfl_sync(0xffffffffu, lsum[pn], 8 * t4 + 4);
+                    lsum[pn] = l_run[pn];
+                    lsum[pn] += __shfl_xor_sync(0xffffffffu, lsum[pn], 1);
+                    lsum[pn] += __shfl_xor_sync(0xffffffffu, lsum[pn], 2);
+                }
+                const int head0 = ch * G;
+                if (piece_j0 == 0 && cj == c_nb - 1) {
+                    // the whole range in this piece: normalise and store
+#pragma unroll
+                    for (int pn = 0; pn < NT; ++pn) {
+                        const float inv_lo = 1.f / __shfl_sync(0xffffffffu, lsum[pn], 8 * t4);
+                        const float inv_hi = 1.f / __shfl_sync(0xffffffffu, lsum[pn], 8 * t4 + 4);
+                        const int ha = pn * 8 + 2 * t4, hb = ha + 1;
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            const int d0 = mt * 16 + g;
+                            if (ha < G) {
+                                const int64_t o = ((int64_t)cs * p.Hq + head0 + ha) * D;
+                                store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][0] * inv_lo);
+                                store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][2] * inv_lo);
+                            }
+                            if (hb < G) {
+                                const int64_t o = ((int64_t)cs * p.Hq + head0 + hb) * D;
+                                store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][1] * inv_hi);
+                                store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][3] * inv_hi);
+                            }
+                        }
+                    }
+                    return;
+                }
+                // one piece of a range: leave (m, l, acc) on the range's list
+                uint32_t ri = 0;
+                if (lane == 0) ri = epoch_fetch_add(&p.ctl[2], p.epoch, 1);
+                ri = __shfl_sync(0xffffffffu, ri, 0);
+                if (ri == 0u || (int)ri > p.pool_cap) {
+                    set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+                    return;
+                }
+                float *rec = p.part + (size_t)(ri - 1) * p.rec_floats;
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn) {
+                    const int hr = pn * 8 + g;
+                    if (t4 == 0 && hr < G) {
+                        rec[hr] = m_run[pn];
+                        rec[G + hr] = lsum[pn];
+                    }
+                    float *racc = rec + 2 * G;
                     const int ha = pn * 8 + 2 * t4, hb = ha + 1;
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
                         const int d0 = mt * 16 + g;
                         if (ha < G) {
-                            const int64_t o = ((int64_t)cs * p.Hq + head0 + ha) * D;
-                            store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][0] * inv_lo);
-                            store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][2] * inv_lo);
+                            racc[ha * D + d0] = acc[mt][pn][0];
+                            racc[ha * D + d0 + 8] = acc[mt][pn][2];
                         }
                         if (hb < G) {
-                            const int64_t o = ((int64_t)cs * p.Hq + head0 + hb) * D;
-                            store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][1] * inv_hi);
-                            store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][3] * inv_hi);
+                            racc[hb * D + d0] = acc[mt][pn][1];
+                            racc[hb * D + d0 + 8] = acc[mt][pn][3];
                         }
                     }
                 }
-            } else {
-                // part of a range shared with other warps: leave (m, l, acc)
-                float *rec = p.part + (size_t)(wg * 2 + (started_mid ? 0 : 1)) * Sh::REC;
-#pragma unroll
-                for (int pn = 0; pn < NT; ++pn) {
-                    if (t4 == 0) {
-                        rec[pn * 8 + g] = m_run[pn];
-                        rec[Sh::HP + pn * 8 + g] = lsum[pn];
-                    }
-                    float *racc = rec + 2 * Sh::HP;
-                    const int ha = pn * 8 + 2 * t4, hb = ha + 1;
-#pragma unroll
-                    for (int mt = 0; mt < D / 16; ++mt) {
-                        const int d0 = mt * 16 + g;
-                        racc[ha * D + d0] = acc[mt][pn][0];
-                        racc[hb * D + d0] = acc[mt][pn][1];
-                        racc[ha * D + d0 + 8] = acc[mt][pn][2];
-                        racc[hb * D + d0 + 8] = acc[mt][pn][3];
-                    }
-                }
-                // the warp that finishes the last piece of the range combines
-                // them; the counter update is a release (it publishes the
-                // record the lanes wrote before the __syncwarp) and an acquire
-                // (the last arriver then sees every other piece's record)
+                // publish: every lane's record stores, then lane 0 links the
+                // record and adds the piece's blocks to the range's counter
+                // (a release; the warp that completes the count acquires)
+                __threadfence();
                 __syncwarp();
-                const int64_t flat = i < n_tail ? t_start + i : lo_w + (i - n_tail);
-                const int64_t seg_lo = flat - cj, seg_hi = seg_lo + c_nb - 1;
-                const int64_t w0 = owner_of(seg_lo, total, nw), w1 = owner_of(seg_hi, total, nw);
-                uint32_t pieces = 0;
-                for (int64_t w = w0; w <= w1; ++w) pieces += range_lo(w + 1, total, nw) > range_lo(w, total, nw);
-                unsigned long long *ctr = p.arrivals + (size_t)cs * Hkv + ch;
-                uint32_t arrived = 0;
-                if (lane == 0) arrived = count_arrival(ctr, p.epoch);
-                arrived = __shfl_sync(0xffffffffu, arrived, 0);
-                if (arrived == pieces) {
+                const size_t seg = (size_t)cs * Hkv + ch;
+                uint32_t done = 0;
+                if (lane == 0) {
+                    const unsigned long long prev =
+                        atomicExch(p.seg_list + seg, ((unsigned long long)p.epoch << 32) | ri);
+                    const uint32_t nxt = (uint32_t)(prev >> 32) == p.epoch ? (uint32_t)prev : 0u;
+                    rec[2 * G + G * D] = __uint_as_float(nxt);
+                    rec[2 * G + G * D + 1] = __int_as_float(piece_j0);
+                    done = epoch_add(p.seg_done + seg, p.epoch, (uint32_t)piece_n);
+                }
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (done == (uint32_t)c_nb) {
                     __syncwarp();
-                    merge_pieces<T, D, NT>(p, w0, w1, total, nw, cs, ch, lane);
-                    if (lane == 0) atomicExch(ctr, 0ull);
-                } else if (arrived == 0) {
+                    merge_list<T, D, NT>(p, cs, ch, lane);
+                } else if (done == 0u) {
                     set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
                 }
-            }
-            started_mid = false;
-            seg_fresh = true;
-        }
-        // advance the consumer cursor
-        if (i + 1 == n_tail) {
-            seek_head(cs, c_nb, ch, cj, &c_ctx);
-            started_mid = cj != 0;
-        } else if (i + 1 < n) {
-            if (++cj == c_nb) {
-                cj = 0;
-                if (++ch == Hkv) {
-                    ch = 0;
-                    cs = next_seq(cs, c_nb, &c_ctx);
+            };
+
+            bool timed_out = false;
+            int i = 0;
+            for (; i < len; ++i) {
+                if (i == limit) {
+                    if (!more) break;
+                    // the batch claimed a batch ago: [b, min(b + batch, e)) is ours
+                    const unsigned long long c = __shfl_sync(0xffffffffu, claim, 0);
+                    const int b = rw_begin(c), e = rw_end(c);
+                    const int got = rw_tag(c) != tag ? 0 : max(0, min(kClaimBatch, e - b));
+                    limit += got;
+                    more = got == kClaimBatch && b + kClaimBatch < e;
+                    if (more && lane == 0) claim = atomicAdd(p.ranges + wg, (unsigned long long)kClaimBatch);
+                    if (got == 0) break;
+                }
+                if (seg_fresh) {
+                    // query fragments of (cs, ch): rows = heads of the group (padded to 16)
+                    const uint32_t *qbase = reinterpret_cast<const uint32_t *>(
+                        static_cast<const T *>(p.q) + ((int64_t)cs * p.Hq + (int64_t)ch * G) * D);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const int c0 = (kk * 16 + 2 * t4) >> 1;
+                        qa[kk][0] = g < G ? __ldg(qbase + g * (D / 2) + c0) : 0u;
+                        qa[kk][2] = g < G ? __ldg(qbase + g * (D / 2) + c0 + 4) : 0u;
+                        if constexpr (NT == 1) {   // group of at most 8 heads: rows 8..15 are padding
+                            qa[kk][1] = 0u;
+                            qa[kk][3] = 0u;
+                        } else {
+                            qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0) : 0u;
+                            qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0 + 4) : 0u;
+                        }
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+                        for (int pn = 0; pn < NT; ++pn)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) acc[mt][pn][e] = 0.f;
+#pragma unroll
+                    for (int pn = 0; pn < NT; ++pn) {
+                        m_run[pn] = -INFINITY;
+                        l_run[pn] = 0.f;
+                    }
+                    seg_fresh = false;
+                    piece_j0 = cj;
+                    piece_n = 0;
+                }
+
+                const uint32_t slot = slot_base + i;
+                if (!__all_sync(0xffffffffu, wait_slot(slot, kWaitLimitNs))) {
+                    timed_out = true;
+                    break;
+                }
+                const uint32_t kbase = ring_addr + (slot % STAGES) * Sh::STAGE_BYTES;
+                const uint32_t vbase = kbase + Sh::TILE_BYTES;
+
+                // ---- pull the block's K and V fragments into registers, then
+                // hand the slot straight back to the TMA engine ----
+                uint32_t kf[D / 16][4], vf[D / 16][4];
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const int chunk = ((kk & 3) << 1) + (mi & 1);
+                    const uint32_t off = (kk >> 2) * Sh::HALF_BYTES + ld_row * 128 + ((chunk ^ ld_sw) << 4);
+                    ldsm_x4(kbase + off, kf[kk][0], kf[kk][1], kf[kk][2], kf[kk][3]);
+                    ldsm_x4_t(vbase + off, vf[kk][0], vf[kk][1], vf[kk][2], vf[kk][3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (issued < len) {
+                    issue(slot_base + issued, pending);
+                    if (issued + 1 < len) {
+                        advance_producer();
+                        pending = table_entry();
+                    }
+                    ++issued;
+                }
+
+                // ---- S = Q K^T over the 16 tokens of this block ----
+                float sacc[2][4];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[nt][e] = 0.f;
+                // two accumulator chains per n-tile (even / odd k-steps) halve
+                // the dependent MMA chain
+                float sacc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                for (int kk = 0; kk < D / 16; kk += 2) {
+                    mma_16816<T>(sacc[0], qa[kk], kf[kk][0], kf[kk][1]);
+                    mma_16816<T>(sacc[1], qa[kk], kf[kk][2], kf[kk][3]);
+                    mma_16816<T>(sacc2[0], qa[kk + 1], kf[kk + 1][0], kf[kk + 1][1]);
+                    mma_16816<T>(sacc2[1], qa[kk + 1], kf[kk + 1][2], kf[kk + 1][3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[nt][e] += sacc2[nt][e];
+
+                // ---- mask, online softmax (base 2) ----
+                const int lim = c_ctx - cj * 16;   // valid tokens in this block (>= 16: all)
+                float pr[2][4];
+                float alpha[NT];
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn) {
+                    float x[2][2];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int tok = nt * 8 + 2 * t4 + e;
+                            x[nt][e] = tok < lim ? sacc[nt][pn * 2 + e] * p.scale_log2 : -INFINITY;
+                            mx = fmaxf(mx, x[nt][e]);
+                        }
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const float m_new = fmaxf(m_run[pn], mx);
+                    alpha[pn] = exp2_approx(m_run[pn] - m_new);
+                    m_run[pn] = m_new;
+                    float rs = 0.f;
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            pr[nt][pn * 2 + e] = exp2_approx(x[nt][e] - m_new);
+                            rs += pr[nt][pn * 2 + e];
+                        }
+                    l_run[pn] = l_run[pn] * alpha[pn] + rs;
+                }
+
+                // tokens beyond the context may hold anything (even NaN): clear
+                // their V values in the fragments so 0-weight x garbage cannot
+                // reach the accumulator.  Fragment registers 0/1 hold tokens
+                // 2*t4 (low half) and 2*t4+1 (high half); registers 2/3 the same
+                // tokens + 8.
+                if (lim < 16) {
+                    const uint32_t m01 = (2 * t4 < lim ? 0x0000ffffu : 0u) | (2 * t4 + 1 < lim ? 0xffff0000u : 0u);
+                    const uint32_t m23 = (2 * t4 + 8 < lim ? 0x0000ffffu : 0u) | (2 * t4 + 9 < lim ? 0xffff0000u : 0u);
+#pragma unroll
+                    for (int mt = 0; mt < D / 16; ++mt) {
+                        vf[mt][0] &= m01;
+                        vf[mt][1] &= m01;
+                        vf[mt][2] &= m23;
+                        vf[mt][3] &= m23;
+                    }
+                }
+
+                // ---- rescale the accumulator (skipped when no row max moved,
+                // the common case once a range is under way), O^T += V^T P^T ----
+                bool moved = false;
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn) moved |= alpha[pn] != 1.f;
+                if (__any_sync(0xffffffffu, moved))
+#pragma unroll
+                    for (int pn = 0; pn < NT; ++pn) {
+                        const float a_lo = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4);
+                        const float a_hi = __shfl_sync(0xffffffffu, alpha[pn], 8 * t4 + 4);
+#pragma unroll
+                        for (int mt = 0; mt < D / 16; ++mt) {
+                            acc[mt][pn][0] *= a_lo;
+                            acc[mt][pn][1] *= a_hi;
+                            acc[mt][pn][2] *= a_lo;
+                            acc[mt][pn][3] *= a_hi;
+                        }
+                    }
+                uint32_t pb0[NT][2], pb1[NT][2];
+#pragma unroll
+                for (int pn = 0; pn < NT; ++pn) {
+                    pack2_split<T>(pr[0][pn * 2], pr[0][pn * 2 + 1], pb0[pn][0], pb0[pn][1]);
+                    pack2_split<T>(pr[1][pn * 2], pr[1][pn * 2 + 1], pb1[pn][0], pb1[pn][1]);
+                }
+#pragma unroll
+                for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+                    for (int pn = 0; pn < NT; ++pn) {
+                        mma_16816<T>(acc[mt][pn], vf[mt], pb0[pn][0], pb1[pn][0]);
+                        mma_16816<T>(acc[mt][pn], vf[mt], pb0[pn][1], pb1[pn][1]);
+                    }
+                }
+                ++piece_n;
+
+                // ---- end of a (sequence, head) range ----
+                if (cj == c_nb - 1) {
+                    finish_piece();
+                    seg_fresh = true;
+                }
+                // advance the consumer cursor (the next block exists when it
+                // is inside this work)
+                if (i + 1 < len) {
+                    if (++cj == c_nb) {
+                        cj = 0;
+                        if (++ch == Hkv) {
+                            ch = 0;
+                            cs = next_seq(cs, c_nb, &c_ctx);
+                        }
+                    }
                 }
             }
+            if (!timed_out && !seg_fresh && piece_n > 0) {
+                // the work ended inside a range: cj was advanced past the last
+                // block taken, so step back to it before closing the piece
+                if (i < len) {
+                    if (cj == 0) {
+                        // cannot happen: a piece that ends at a range boundary
+                        // was closed above
+                    } else {
+                        --cj;
+                    }
+                }
+                finish_piece();
+                seg_fresh = true;
+            }
+            // loads issued but not consumed (speculative, or after a timeout)
+            // must land before their slots are reused or the warp leaves
+            for (int k = i + (timed_out ? 1 : 0); k < issued; ++k)
+                wait_slot(slot_base + k, timed_out ? kWaitLimitNs / 8 : kWaitLimitNs);
+            slot_base += issued;
+            if (timed_out) {
+                set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+                return;
+            }
         }
+
+        // ---------------- steal the far half of a busy warp's blocks ----------------
+        if (n_own == 0) return;   // a warp without a share of its own does not rob others
+        // nothing left to take: unclaimed work only shrinks, so once one full
+        // scan found no warp worth robbing, none will be again in this call
+        const unsigned long long kDrained = ((unsigned long long)p.epoch << 32) | 1ull;
+        if (ld_relaxed_u64(p.ctl + 3) == kDrained) return;
+        if (lane == 0 && !steal_reserved) {
+            // every CTA has published its words, and the steal budget allows
+            // one more piece (each steal can leave two partial records)
+            const unsigned long long rdy = ld_acquire_u64(p.ctl + 0);
+            const bool all_ready = (uint32_t)(rdy >> 32) == p.epoch && (uint32_t)rdy >= gridDim.x;
+            if (all_ready) {
+                const uint32_t r = epoch_fetch_add(&p.ctl[1], p.epoch, 1);
+                steal_reserved = r != 0u && (int)r <= p.steal_cap;
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, steal_reserved ? 1 : 0, 0)) return;
+        bool got = false;
+        for (int attempt = 0; attempt < 8 && !got; ++attempt) {
+            // every lane reads its share of the range words, eight at a time
+            int best = 0;
+            int64_t best_v = -1;
+            unsigned long long best_w = 0;
+            for (int64_t k0 = 0; k0 * 32 < nw; k0 += 8) {
+                unsigned long long w[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t v = (k0 + u) * 32 + lane;
+                    w[u] = v < nw ? ld_relaxed_u64(p.ranges + v) : 0ull;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t v = (k0 + u) * 32 + lane;
+                    const int rem = (v < nw && v != wg && rw_tag(w[u]) == tag) ? rw_end(w[u]) - rw_begin(w[u]) : 0;
+                    if (rem > best) {
+                        best = rem;
+                        best_v = v;
+                        best_w = w[u];
+                    }
+                }
+            }
+            // thieves spread over victims: each first tries the best candidate
+            // of a lane picked by its own index, and takes the overall best
+            // only when that one is too small
+            int top = best, top_lane = lane;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const int ob = __shfl_xor_sync(0xffffffffu, top, o);
+                const int ol = __shfl_xor_sync(0xffffffffu, top_lane, o);
+                if (ob > top || (ob == top && ol < top_lane)) {
+                    top = ob;
+                    top_lane = ol;
+                }
+            }
+            const int pick = (int)((wg * 7 + attempt) & 31);
+            const int picked = __shfl_sync(0xffffffffu, best, pick);
+            if (top >= kStealMin && picked >= kStealMin) top_lane = pick;
+            if (top < kStealMin) {
+                if (lane == 0) atomicExch(p.ctl + 3, kDrained);
+                break;
+            }
+            int start = 0, take = 0;
+            if (lane == top_lane) {
+                take = (best + 1) / 2;
+                start = rw_end(best_w) - take;
+                if (atomicCAS(p.ranges + best_v, best_w, rw_make(tag, rw_begin(best_w), start)) != best_w) take = 0;
+            }
+            take = __shfl_sync(0xffffffffu, take, top_lane);
+            start = __shfl_sync(0xffffffffu, start, top_lane);
+            const int64_t vv = __shfl_sync(0xffffffffu, best_v, top_lane);
+            if (take > 0) {
+                got = true;
+                x0 = range_lo(vv, total, nw) + start;
+                len = take;
+            }
+        }
+        if (!got) return;
+        steal_reserved = false;
+        own = false;
+        s0 = locate_seq(p, x0, lane);
+        off0 = (int)(x0 - __ldcg(p.prefix + s0) * Hkv);
     }
 }
 
@@ -645,23 +883,58 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
-static size_t decode_record_floats(int G, int head_dim) {
-    const int HP = G > 8 ? 16 : 8;
-    return (size_t)(2 * HP + HP * head_dim);
+// ---- workspace ----------------------------------------------------------------
+// [range counters S*Hkv x 8][range lists S*Hkv x 8][range words, one per warp]
+// [control words][prefix (S+1) x 8][partial records], each part 256-B aligned.
+// A partial record holds G maxima, G sums, G x head_dim accumulators, a link
+// and the piece's first block.
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static int record_floats(int G, int head_dim) { return (2 * G + G * head_dim + 2 + 3) & ~3; }
+
+struct DecodeLayout {
+    size_t seg_done, seg_list, ranges, ctl, prefix, part, fixed;
+};
+
+static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
+    DecodeLayout L;
+    size_t o = 0;
+    L.seg_done = o;
+    o += align256((size_t)S * Hkv * 8);
+    L.seg_list = o;
+    o += align256((size_t)S * Hkv * 8);
+    L.ranges = o;
+    o += align256((size_t)total_warps * 8);
+    L.ctl = o;
+    o += 256;
+    L.prefix = o;
+    o += align256((size_t)(S + 1) * 8);
+    L.part = o;
+    L.fixed = o;
+    return L;
 }
 
-// Workspace: [arrival counters, S * Hkv x 8 B, padded to 256 B][partial records].
-static size_t arrivals_bytes(int S, int Hkv) { return ((size_t)S * Hkv * 8 + 255) & ~size_t(255); }
-
-static size_t workspace_bytes_for(int S, int Hkv, int G, int head_dim, int total_warps) {
-    return arrivals_bytes(S, Hkv) + (size_t)2 * total_warps * decode_record_floats(G, head_dim) * sizeof(float);
-}
+// records: two per warp for its own range (the pieces at its ends) plus two
+// per steal; the recommended size allows four steals per warp
+static size_t records_min(int total_warps) { return (size_t)2 * total_warps; }
+static size_t records_recommended(int total_warps) { return (size_t)10 * total_warps; }
 
 static uint32_t next_epoch() {
     static std::atomic<uint32_t> epoch{0};
     uint32_t e = ++epoch;
     if (e == 0) e = ++epoch;
     return e;
+}
+
+size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
+    int sms = 0;
+    if (current_sm_count(&sms) != PKV_OK) return 0;
+    const int nw = sms * kDecodeWarps;
+    const int G = num_q_heads / num_kv_heads;
+    return decode_layout(num_seqs, num_kv_heads, nw).fixed +
+           records_min(nw) * (size_t)record_floats(G, head_dim) * sizeof(float);
 }
 
 }  // namespace pkv
@@ -671,7 +944,10 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
     int sms = 0;
     if (current_sm_count(&sms) != PKV_OK) return 0;
-    return workspace_bytes_for(num_seqs, num_kv_heads, num_q_heads / num_kv_heads, head_dim, sms * kDecodeWarps);
+    const int nw = sms * kDecodeWarps;
+    const int G = num_q_heads / num_kv_heads;
+    return decode_layout(num_seqs, num_kv_heads, nw).fixed +
+           records_recommended(nw) * (size_t)record_floats(G, head_dim) * sizeof(float);
 }
 
 extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
@@ -707,8 +983,12 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     if (grid > sms) grid = sms;
     if (grid < 1) grid = 1;
     const int total_warps = grid * kDecodeWarps;
-    if (workspace_bytes < workspace_bytes_for(num_seqs, num_kv_heads, G, head_dim, total_warps))
-        return PKV_ERR_WORKSPACE;
+    // range offsets are 24-bit fields
+    if (upper / total_warps + 1 >= kMaxWarpBlocks) return PKV_ERR_UNSUPPORTED;
+    const DecodeLayout lay = decode_layout(num_seqs, num_kv_heads, total_warps);
+    const size_t rec_bytes = (size_t)record_floats(G, head_dim) * sizeof(float);
+    if (workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) return PKV_ERR_WORKSPACE;
+    const size_t cap = (workspace_bytes - lay.fixed) / rec_bytes;
 
     CUtensorMap tk, tv;
     rc = encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
@@ -716,13 +996,18 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     rc = encode_cache_map(&tv, v_cache, num_blocks, num_kv_heads, block_size, head_dim);
     if (rc != PKV_OK) return rc;
 
+    char *ws = static_cast<char *>(workspace);
     DecodeParams prm;
     prm.out = out;
     prm.q = q;
     prm.block_tables = block_tables;
     prm.context_lens = context_lens;
-    prm.arrivals = static_cast<unsigned long long *>(workspace);
-    prm.part = reinterpret_cast<float *>(static_cast<char *>(workspace) + arrivals_bytes(num_seqs, num_kv_heads));
+    prm.seg_done = reinterpret_cast<unsigned long long *>(ws + lay.seg_done);
+    prm.seg_list = reinterpret_cast<unsigned long long *>(ws + lay.seg_list);
+    prm.ranges = reinterpret_cast<unsigned long long *>(ws + lay.ranges);
+    prm.ctl = reinterpret_cast<unsigned long long *>(ws + lay.ctl);
+    prm.prefix = reinterpret_cast<long long *>(ws + lay.prefix);
+    prm.part = reinterpret_cast<float *>(ws + lay.part);
     prm.dev_status = dev_status;
     prm.S = num_seqs;
     prm.max_blocks = max_blocks_per_seq;
@@ -733,6 +1018,13 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.out_dtype = out_dtype;
     prm.total_warps = total_warps;
+    prm.rec_floats = record_floats(G, head_dim);
+    prm.pool_cap = cap > (size_t)INT32_MAX ? INT32_MAX : (int)cap;
+    prm.steal_cap = (int)((prm.pool_cap - records_min(total_warps)) / 2);
+    // PKV_DETERMINISTIC=1: no stealing, so the split of every range is fixed
+    // by the contexts alone and the output bits repeat from call to call
+    const char *det = std::getenv("PKV_DETERMINISTIC");
+    if (det && det[0] == '1') prm.steal_cap = 0;
     prm.epoch = next_epoch();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const bool wide = G > 8;

@@ -68,7 +68,7 @@ extern "C" int pkv_paged_decode_attention_static(void *out, const void *q, const
     // The existing entry point validates everything else; only the scratch
     // capacity is checked here.
     if (num_seqs > 0 && num_kv_heads > 0 && num_q_heads > 0 && num_q_heads % num_kv_heads == 0) {
-        const size_t need = pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim);
+        const size_t need = pkv::decode_workspace_min(num_seqs, num_q_heads, num_kv_heads, head_dim);
         if (need > kScratchBytes) {
             pkv::set_error_message("pkv_paged_decode_attention_static: shape needs more than PKV_STATIC_SCRATCH_BYTES");
             return PKV_ERR_WORKSPACE;

@@ -21,6 +21,10 @@ void set_error_message(const char *msg);
 // SM count of the current device (cached per device).  PKV_OK or an error.
 int current_sm_count(int *num_sms);
 
+// Smallest workspace pkv_paged_decode_attention accepts for this shape (two
+// partial records per warp; no room left for stolen pieces).
+size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
+
 // Encodes a 2-D TMA descriptor over a paged cache viewed as
 // [num_blocks * num_kv_heads * block_size rows][head_dim elements] of 16-bit
 // elements, with a box of 64 elements x block_size rows and 128-byte swizzle.
