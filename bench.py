@@ -353,23 +353,26 @@ def run_mixed(args):
     }
 
 
-def run_trace_bench(args):
-    """The continuous-batching trace: 1000 requests, Poisson(20) arrivals per
+def trace_line(args, n, NB, policy="continuous", outputs="geometric"):
+    """The continuous-batching trace: n requests, Poisson(20) arrivals per
     step, prompts lognormal (mean 512, sigma 1, clipped 8..4096), outputs
-    geometric (mean 256), max batch 256, 8192-token budget, 512-token prefill
-    chunks, a pool of 200k 16-token blocks, preemption by recompute; every
-    step runs append + prefill chunks + decode for 32 layers of the 8B shape.
-    The 32 layers rotate over 4 physical caches (52 GB) so the trace fits in
-    HBM; every layer still streams its full context."""
+    geometric (or lognormal) with mean 256, max batch 256, 8192-token budget,
+    512-token prefill chunks, a pool of NB 16-token blocks, preemption by
+    recompute; every step runs append + prefill chunks + decode for 32 layers
+    of the 8B shape.  The 32 layers rotate over 4 physical caches so the trace
+    fits in HBM; every layer still streams its full context."""
     import torch
+    from paged_kv_cache_tables_gb300 import _binding
     from paged_kv_cache_tables_gb300.engine import PagedEngine, run_trace
     from synth import SEEDS
     from synth.trace import make_fill, make_requests, pick_rows
     torch.cuda.set_device(0)
     seed = SEEDS["trace"]
-    n, L, R, NB = args.trace_requests, args.trace_layers, args.trace_caches, args.trace_pool
-    arrival, prompt, eos = make_requests(seed, n=n)
-    eng = PagedEngine(NB, num_layers=L, num_caches=R, initial_order=np.random.default_rng(seed).permutation(NB))
+    L, R = args.trace_layers, args.trace_caches
+    arrival, prompt, eos = make_requests(seed, n=n, outputs=outputs)
+    pol = {"continuous": _binding.SCHED_CONTINUOUS, "static": _binding.SCHED_STATIC}[policy]
+    eng = PagedEngine(NB, num_layers=L, num_caches=R, initial_order=np.random.default_rng(seed).permutation(NB),
+                      policy=pol)
     rng = np.random.default_rng(seed + 1)
     clk = ClockSampler(0)
     with clk:
@@ -401,6 +404,15 @@ def run_trace_bench(args):
             big_steps += 1
     gen = sum(min(int(eos[i]), 4096, 8192 - int(prompt[i])) for i in range(n))
     lat = np.array([res["finish_step"][i] - int(arrival[i]) for i in range(n)])
+    # time to first token: in engine steps, and in device time from the start
+    # of the arrival step to the end of the first token's step
+    step_ms = np.zeros(max(s["step"] for s in steps) + 1)
+    for s_ in steps:
+        step_ms[s_["step"]] = s_["device_ms"]
+    cum = np.concatenate([[0.0], np.cumsum(step_ms)])
+    ft = res["first_token_step"]
+    ttft_steps = np.array([ft[i] - int(arrival[i]) for i in range(n)], dtype=np.float64)
+    ttft_ms = np.array([cum[ft[i] + 1] - cum[int(arrival[i])] for i in range(n)])
     dev_s = res["stream_ms"] / 1e3
     # oracle check of the sampled layer-0 rows, and the oracle's own time on them
     import oracle
@@ -420,9 +432,9 @@ def run_trace_bench(args):
             checked += 1
     line = {
         "metric": "continuous-batching trace: output tokens/s and aggregate paged-attention KV GB/s",
-        "workload": "trace: %d requests, Poisson(20)/step, prompt lognormal mean 512 clip 8-4096, output geometric "
+        "workload": "trace: %d requests, Poisson(20)/step, prompt lognormal mean 512 clip 8-4096, output %s "
                     "mean 256, max batch 256, budget 8192, chunk 512, pool %d blocks, %d layers (8B shape) over %d "
-                    "physical caches" % (n, NB, L, R),
+                    "physical caches, %s batching" % (n, outputs, NB, L, R, policy),
         "engine_steps": len(steps), "wall_s": round(res["wall_s"], 3), "stream_s": round(dev_s, 3),
         "host_sched_ms_per_step": round(st["host_ms"] / max(1, st["steps"]), 4),
         "host_ms_per_step": round(eng.host_ms / max(1, len(steps)), 4),
@@ -438,12 +450,38 @@ def run_trace_bench(args):
         "preemptions": st["preemptions"], "preemption_rate": round(st["preemptions"] / max(1, st["steps"]), 4),
         "avg_running_batch": round(st["sum_running"] / max(1, st["steps"]), 2),
         "latency_steps_p50": float(np.percentile(lat, 50)), "latency_steps_p99": float(np.percentile(lat, 99)),
+        "ttft_steps_mean": round(float(ttft_steps.mean()), 2), "ttft_ms_mean": round(float(ttft_ms.mean()), 3),
         "upload_bytes_per_step": int(eng.upload_bytes / max(1, len(steps))),
         "oracle_check": {"rows": checked, "max_abs_err": worst, "every": "50th engine step, layer 0",
                          "oracle_s": round(t_or, 2), "oracle_keys_per_s": round(keys / max(t_or, 1e-9), 1)},
         "clocks": clk.summary(),
     }
-    print(json.dumps(line))
+    return line
+
+
+def run_trace_bench(args):
+    print(json.dumps(trace_line(args, args.trace_requests, args.trace_pool)))
+
+
+def run_batching_bench(args):
+    """Static against continuous batching on one synthetic trace: 500 requests
+    with lognormal output lengths, the rest as in the trace workload.  Both runs
+    use the same engine, kernels and pool; only the admission policy differs."""
+    n = args.trace_requests if args.trace_requests != 1000 else 500
+    st = trace_line(args, n, args.trace_pool, policy="static", outputs="lognormal")
+    co = trace_line(args, n, args.trace_pool, policy="continuous", outputs="lognormal")
+    keep = ["engine_steps", "wall_s", "output_tokens", "output_tokens_per_s", "avg_running_batch", "ttft_steps_mean",
+            "ttft_ms_mean", "latency_steps_p50", "latency_steps_p99", "preemptions", "oracle_check", "clocks"]
+    print(json.dumps({
+        "metric": "static vs continuous batching: output tokens/s and mean time to first token",
+        "workload": "%d requests, Poisson(20)/step, prompt lognormal mean 512, output lognormal mean 256 (sigma 1), "
+                    "max batch 256, budget 8192, chunk 512, pool %d blocks, %d layers (8B shape)"
+                    % (n, args.trace_pool, args.trace_layers),
+        "static": {k: st[k] for k in keep}, "continuous": {k: co[k] for k in keep},
+        "throughput_ratio": round(co["output_tokens_per_s"] / st["output_tokens_per_s"], 3),
+        "ttft_ratio_static_over_continuous": round(st["ttft_ms_mean"] / co["ttft_ms_mean"], 3),
+    }))
+
 
 
 def run_pkv(args):
@@ -569,7 +607,8 @@ def main():
     ap.add_argument("--mixed-prior", type=int, default=-1,
                     help="give every prefill chunk this prior context instead of U{0..4096} (profiling)")
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace"])
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching"],
+                    help="trace: the continuous-batching trace; batching: static vs continuous on one trace")
     ap.add_argument("--trace-requests", type=int, default=1000)
     ap.add_argument("--trace-layers", type=int, default=32)
     ap.add_argument("--trace-caches", type=int, default=4)
@@ -581,6 +620,9 @@ def main():
         args.warmup = 3
     if args.workload == "trace":
         run_trace_bench(args)
+        return
+    if args.workload == "batching":
+        run_batching_bench(args)
         return
     if args.only_mixed:
         import torch

@@ -283,7 +283,17 @@ typedef struct pkv_sched_config {
     int chunk;                  /* max prefill tokens per request per step */
     int max_model_len;          /* max prompt + generated tokens */
     const int32_t *initial_order; /* NULL or a permutation of [0, num_blocks) (copied) */
+    int policy;                 /* PKV_SCHED_CONTINUOUS (0) or PKV_SCHED_STATIC (1) */
 } pkv_sched_config;
+
+/* Admission policies.  Continuous: the rules above, every step ("Continuous
+ * Batching" §4-5).  Static: the baseline that page's opening section
+ * describes -- a batch of up to max_batch waiting requests is admitted only
+ * when nothing runs, and runs until its last request retires; its prefill
+ * chunks still take the token budget step by step.  Everything else (block
+ * accounting, growth, preemption, retirement) is the same. */
+#define PKV_SCHED_CONTINUOUS 0
+#define PKV_SCHED_STATIC 1
 
 /* Arrays are owned by the scheduler and valid until the next pkv_sched_step
  * or pkv_sched_destroy on the same scheduler. */

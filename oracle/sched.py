@@ -113,7 +113,9 @@ def cdiv(a: int, b: int) -> int:
 class Scheduler:
     def __init__(self, num_blocks: int, block_size: int = 16, max_batch: int = 256,
                  max_num_batched_tokens: int = 8192, chunk: int = 512, max_model_len: int = 8192,
-                 initial_order=None):
+                 initial_order=None, policy: str = "continuous"):
+        assert policy in ("continuous", "static")
+        self.policy = policy
         self.bs = block_size
         self.pool = BlockPool(num_blocks, initial_order)
         self.max_batch = max_batch
@@ -175,8 +177,13 @@ class Scheduler:
             scheduled.append((r, q))
             budget -= q
             i += 1
-        # admit waiting requests, first come first served
-        while self.waiting and len(self.running) < self.max_batch and budget > 0:
+        # admit waiting requests, first come first served.  Static batching
+        # ("Continuous Batching", opening section): a new batch only when
+        # nothing runs, filled to max_batch whatever the token budget; the
+        # members' prefill chunks then take the budget step by step.
+        static = self.policy == "static"
+        may_admit = not static or not self.running
+        while may_admit and self.waiting and len(self.running) < self.max_batch and (static or budget > 0):
             r = self.waiting[0]
             got = self._try_alloc(cdiv(r.length, self.bs))
             if got is None:
@@ -186,8 +193,9 @@ class Scheduler:
             r.state = "running"
             self.running.append(r)
             q = min(r.length, self.chunk, budget)
-            scheduled.append((r, q))
-            budget -= q
+            if q > 0:
+                scheduled.append((r, q))
+                budget -= q
         self.sum_running += len(self.running)
         meta = self._emit(scheduled) if scheduled else None
         # the iteration ran: advance, emit a token where the context caught up, retire

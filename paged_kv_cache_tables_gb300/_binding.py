@@ -45,7 +45,10 @@ class StepMeta(ctypes.Structure):
 class SchedConfig(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_num_batched_tokens", ctypes.c_int), ("chunk", ctypes.c_int), ("max_model_len", ctypes.c_int),
-                ("initial_order", ctypes.POINTER(ctypes.c_int32))]
+                ("initial_order", ctypes.POINTER(ctypes.c_int32)), ("policy", ctypes.c_int)]
+
+
+SCHED_CONTINUOUS, SCHED_STATIC = 0, 1
 
 
 class SchedStats(ctypes.Structure):
@@ -237,10 +240,11 @@ class Scheduler:
     """pkv_sched_*: the native iteration-level scheduler (host only)."""
 
     def __init__(self, num_blocks, block_size=16, max_batch=256, max_num_batched_tokens=8192, chunk=512,
-                 max_model_len=8192, initial_order=None):
+                 max_model_len=8192, initial_order=None, policy=SCHED_CONTINUOUS):
         L = lib()
         self._keep = None
-        cfg = SchedConfig(num_blocks, block_size, max_batch, max_num_batched_tokens, chunk, max_model_len, None)
+        cfg = SchedConfig(num_blocks, block_size, max_batch, max_num_batched_tokens, chunk, max_model_len, None,
+                          policy)
         if initial_order is not None:
             self._keep = np.ascontiguousarray(initial_order, dtype=np.int32)
             cfg.initial_order = self._keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))

@@ -244,8 +244,12 @@ int pkv_sched::step(pkv_step_meta *out) {
         budget -= q;
         ++i;
     }
-    // 2. admission, first come first served
-    while (!waiting.empty() && (int)running.size() < cfg.max_batch && budget > 0) {
+    // 2. admission, first come first served; under the static policy only
+    // when nothing runs, and then a whole batch whatever the token budget
+    // (its members' prefill chunks are scheduled as the budget allows)
+    const bool is_static = cfg.policy == PKV_SCHED_STATIC;
+    const bool may_admit = !is_static || running.empty();
+    while (may_admit && !waiting.empty() && (int)running.size() < cfg.max_batch && (is_static || budget > 0)) {
         const int idx = waiting.front();
         Request &r = reqs[idx];
         got.clear();
@@ -256,8 +260,10 @@ int pkv_sched::step(pkv_step_meta *out) {
         running.push_back(idx);
         ++stats.admitted;
         const int q = std::min(std::min(r.length(), cfg.chunk), budget);
-        scheduled.emplace_back(idx, q);
-        budget -= q;
+        if (q > 0) {
+            scheduled.emplace_back(idx, q);
+            budget -= q;
+        }
     }
     stats.sum_running += (int64_t)running.size();
     if (!scheduled.empty()) {
@@ -296,7 +302,7 @@ extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
     if (!config) return nullptr;
     const pkv_sched_config &c = *config;
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.max_batch <= 0 || c.max_num_batched_tokens <= 0 ||
-        c.chunk <= 0 || c.max_model_len <= 1)
+        c.chunk <= 0 || c.max_model_len <= 1 || (c.policy != PKV_SCHED_CONTINUOUS && c.policy != PKV_SCHED_STATIC))
         return nullptr;
     pkv_sched *s = new (std::nothrow) pkv_sched();
     if (!s) return nullptr;

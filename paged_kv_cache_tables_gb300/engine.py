@@ -25,7 +25,7 @@ from . import _binding as B
 class PagedEngine:
     def __init__(self, num_blocks, num_layers=32, num_caches=4, Hq=32, Hkv=8, d=128, dtype="bf16",
                  max_batch=256, max_num_batched_tokens=8192, chunk=512, max_model_len=8192, initial_order=None,
-                 device="cuda"):
+                 device="cuda", policy=B.SCHED_CONTINUOUS):
         import torch
         self.torch = torch
         self.L, self.R = num_layers, num_caches
@@ -33,7 +33,7 @@ class PagedEngine:
         self.NB = num_blocks
         self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
         self.sched = B.Scheduler(num_blocks, 16, max_batch, max_num_batched_tokens, chunk, max_model_len,
-                                 initial_order=initial_order)
+                                 initial_order=initial_order, policy=policy)
         self.max_blocks = self.sched.max_blocks
         self.max_T = max_num_batched_tokens
         self.max_S = max_batch
@@ -173,6 +173,7 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
                 idx = torch.tensor([r[0] for r in rows], device=out.device)
                 samples.append((rows, out.index_select(0, idx).float().to("cpu")))
 
+    first_token = {}
     t_wall = time.perf_counter()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -187,6 +188,12 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
         if info is not None:
             for rid in info["finished"]:
                 finish_step[int(rid)] = step
+            # a request emits its first token after the step in which its
+            # context first covers the whole prompt
+            for rid, c in zip(info["seq_rids"], info["context_lens"]):
+                rid = int(rid)
+                if rid not in first_token and c >= prompt[rid]:
+                    first_token[rid] = step
             steps.append({"step": step, "S": info["S"], "T": info["T"], "P": info["P"],
                           "context_lens": info["context_lens"], "q_lens": info["q_lens"], "events": info["events"]})
         if nxt >= n and len(finish_step) == n:
@@ -196,5 +203,5 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
     for s in steps:   # device time of each step's layer launches
         e = s.pop("events")
         s["device_ms"] = e[0].elapsed_time(e[1])
-    return {"steps": steps, "finish_step": finish_step, "wall_s": time.perf_counter() - t_wall,
+    return {"steps": steps, "finish_step": finish_step, "first_token_step": first_token, "wall_s": time.perf_counter() - t_wall,
             "stream_ms": ev0.elapsed_time(ev1), "samples": samples}

@@ -59,8 +59,11 @@ def token_rows(rids, pos, tag: int, width: int, dtype: str = "bf16") -> np.ndarr
 
 
 def make_requests(seed: int, n: int = 1000, rate: float = 20.0, prompt_mean: float = 512.0,
-                  sigma: float = 1.0, out_mean: float = 256.0, pmin: int = 8, pmax: int = 4096):
-    """Returns arrival_step, prompt_len, eos_after (int64 arrays of length n)."""
+                  sigma: float = 1.0, out_mean: float = 256.0, pmin: int = 8, pmax: int = 4096,
+                  outputs: str = "geometric"):
+    """Returns arrival_step, prompt_len, eos_after (int64 arrays of length n).
+    Output lengths are geometric with mean out_mean, or (outputs="lognormal")
+    lognormal with mean out_mean and the prompts' sigma, at least 1."""
     rng = np.random.Generator(np.random.PCG64(seed))
     arrival = np.empty(n, dtype=np.int64)
     k, step = 0, 0
@@ -72,7 +75,13 @@ def make_requests(seed: int, n: int = 1000, rate: float = 20.0, prompt_mean: flo
         step += 1
     mu = np.log(prompt_mean) - sigma * sigma / 2
     prompt = np.clip(np.rint(rng.lognormal(mu, sigma, size=n)), pmin, pmax).astype(np.int64)
-    eos = rng.geometric(1.0 / out_mean, size=n).astype(np.int64)
+    if outputs == "geometric":
+        eos = rng.geometric(1.0 / out_mean, size=n).astype(np.int64)
+    elif outputs == "lognormal":
+        mo = np.log(out_mean) - sigma * sigma / 2
+        eos = np.maximum(np.rint(rng.lognormal(mo, sigma, size=n)), 1).astype(np.int64)
+    else:
+        raise ValueError(outputs)
     return arrival, prompt, eos
 
 

@@ -8,6 +8,7 @@ import pytest
 import sched_golden
 from oracle.sched import Scheduler as PyScheduler
 from paged_kv_cache_tables_gb300 import BlockPool, PkvError, Scheduler
+from paged_kv_cache_tables_gb300._binding import SCHED_CONTINUOUS, SCHED_STATIC
 
 
 class _Adapter:
@@ -45,11 +46,12 @@ def test_native_scheduler_reproduces_hand_worked_trace(path):
                     max_num_batched_tokens=c["budget"], chunk=c["chunk"], max_model_len=c["max_model_len"]), path)
 
 
-def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fail_every=0):
+def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fail_every=0, policy="continuous"):
     rng = np.random.default_rng(seed)
     order = rng.permutation(NB)
-    py = PyScheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order)
-    nat = Scheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order)
+    py = PyScheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order, policy=policy)
+    nat = Scheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order,
+                    policy={"continuous": SCHED_CONTINUOUS, "static": SCHED_STATIC}[policy])
     arrivals = sorted((int(rng.integers(0, 60)), rid, int(rng.integers(1, 200)), int(rng.integers(1, 120)),
                        int(rng.geometric(1 / 30))) for rid in range(n))
     i = 0
@@ -89,6 +91,18 @@ def test_native_matches_python_restatement_step_by_step(seed):
 def test_native_matches_python_under_memory_pressure_and_injected_failures(seed):
     py = run_both(100 + seed, NB=40, fail_every=7)
     assert py.n_preemptions > 0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_native_matches_python_static_policy(seed):
+    run_both(200 + seed, policy="static")
+    py = run_both(300 + seed, NB=40, fail_every=7, policy="static")
+    assert py.n_preemptions > 0
+
+
+def test_native_rejects_unknown_policy():
+    with pytest.raises(ValueError):
+        Scheduler(16, policy=7)
 
 
 def test_pool_stack_order_and_all_or_nothing():

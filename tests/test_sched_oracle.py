@@ -162,3 +162,56 @@ def test_injected_alloc_failure_preempts_lifo_and_recompute_reaches_same_state()
         sched.step()
     assert [r.generated for r in sorted(sched.finished, key=lambda r: r.rid)] == [40, 40, 40]
     assert sched.pool.free_count() == 64
+
+
+def _finish_steps(policy):
+    """A (prompt 3, EOS after 2), B (prompt 2, EOS after 4), C (prompt 1, EOS
+    after 1), all waiting at step 0, max_batch 2, no chunking.  Worked by hand:
+    both policies admit A and B at step 0; A retires after step 1 and B after
+    step 3.  Continuous admission puts C into A's freed slot at step 2 (it
+    retires there); static batching holds C until the batch has drained and
+    admits it at step 4."""
+    s = Scheduler(64, 16, max_batch=2, max_num_batched_tokens=100, chunk=100, max_model_len=64, policy=policy)
+    for rid, prompt, eos in ((0, 3, 2), (1, 2, 4), (2, 1, 1)):
+        s.add(rid, prompt, 10, eos)
+    done = {}
+    for step in range(20):
+        m = s.step()
+        if m is not None:
+            for rid in m.finished_rids:
+                done[int(rid)] = step
+        if s.idle():
+            break
+    return done
+
+
+def test_static_batching_holds_new_requests_until_the_batch_drains():
+    assert _finish_steps("continuous") == {0: 1, 1: 3, 2: 2}
+    assert _finish_steps("static") == {0: 1, 1: 3, 2: 4}
+
+
+def test_static_batching_admits_only_when_idle():
+    """Static policy: a step that starts with anything running admits
+    nobody; a step that starts idle admits min(max_batch, waiting)."""
+    rng = np.random.default_rng(11)
+    s = Scheduler(400, 16, max_batch=6, max_num_batched_tokens=64, chunk=32, max_model_len=256, policy="static")
+    arrivals = sorted((int(rng.integers(0, 30)), rid, int(rng.integers(1, 100)), int(rng.geometric(1 / 20)))
+                      for rid in range(40))
+    i, batches = 0, 0
+    for step in range(3000):
+        while i < len(arrivals) and arrivals[i][0] <= step:
+            _, rid, p, eos = arrivals[i]
+            s.add(rid, p, 50, eos)
+            i += 1
+        running_before = len(s.running)
+        waiting_before = {r.rid for r in s.waiting}
+        s.step()
+        admitted = waiting_before - {r.rid for r in s.waiting}
+        if running_before:
+            assert not admitted, "step %d admitted into a running batch" % step
+        elif waiting_before:
+            assert len(admitted) == min(6, len(waiting_before)), step
+            batches += 1
+        if i == len(arrivals) and s.idle():
+            break
+    assert s.idle() and len(s.finished) == 40 and batches >= 40 // 6
