@@ -240,42 +240,81 @@ def run_reference(args):
 
 def run_e2e(args, ws, st, q, kn, vn, slots, bt, cl, out, kc, vc, work, status, stream, scale, step_bytes, K):
     """Same step through the public API with inputs in pinned host memory:
-    every step copies its inputs host->device and its output device->host."""
+    every step copies its inputs host->device and its output device->host.
+    As a serving engine would, the transfers run on a copy stream and overlap
+    the neighbouring steps' kernels: each step's inputs (one packed pinned
+    buffer, one copy, on an input-copy stream) go into one of two device input
+    sets, its kernels wait for them, and its output (one of two) is read back
+    on an output-copy stream once they are done."""
     import torch
     import paged_kv_cache_tables_gb300 as pkv
-    pin = lambda t: t.cpu().pin_memory()
-    h_q, h_kn, h_vn = pin(q), pin(kn), pin(vn)
-    h_slots, h_bt, h_cl = pin(slots), pin(bt), pin(cl)
-    h_out = torch.empty_like(out, device="cpu").pin_memory()
-    d_q, d_kn, d_vn = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
-    d_slots, d_bt, d_cl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_bt, h_cl))
-    d2h = h_out.numel() * h_out.element_size()
+    parts = [q, kn, vn, slots, bt, cl]
+    nbytes = [t.numel() * t.element_size() for t in parts]
+    offs = [0]
+    for n in nbytes:
+        offs.append((offs[-1] + n + 255) // 256 * 256)
+    total = offs[-1]
+    h_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for t, o, n in zip(parts, offs, nbytes):
+        h_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    h2d = sum(nbytes)
+    d2h = out.numel() * out.element_size()
 
-    def e2e_step():
-        for dst, src in ((d_q, h_q), (d_kn, h_kn), (d_vn, h_vn), (d_slots, h_slots), (d_bt, h_bt), (d_cl, h_cl)):
-            dst.copy_(src, non_blocking=True)
+    def views(buf):
+        return [buf[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, nbytes)]
+    d_in = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(2)]
+    d_views = [views(b) for b in d_in]
+    d_out = [torch.empty_like(out) for _ in range(2)]
+    h_out = [torch.empty_like(out, device="cpu").pin_memory() for _ in range(2)]
+    copy_in, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of the set are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # kernels of the set have finished
+    ev_back = [torch.cuda.Event() for _ in range(2)]   # output of the set is back on the host
+    for e in ev_done + ev_back:
+        e.record(stream)
+
+    def e2e_step(k):
+        i = k & 1
+        # inputs: the set's previous kernels must be done with it
+        copy_in.wait_event(ev_done[i])
+        with torch.cuda.stream(copy_in):
+            d_in[i].copy_(h_in, non_blocking=True)
+        ev_in[i].record(copy_in)
+        # kernels: after their inputs, and after the previous read-back of this output
+        stream.wait_event(ev_in[i])
+        stream.wait_event(ev_back[i])
+        d_q, d_kn, d_vn, d_slots, d_bt, d_cl = d_views[i]
         pkv.kv_append(d_kn, d_vn, d_slots, kc, vc, dev_status=status, stream=stream)
-        pkv.paged_decode_attention(out, d_q, kc, vc, d_bt, d_cl, scale=scale, workspace=work, dev_status=status,
-                                   stream=stream)
-        h_out.copy_(out, non_blocking=True)
+        pkv.paged_decode_attention(d_out[i], d_q, kc, vc, d_bt, d_cl, scale=scale, workspace=work,
+                                   dev_status=status, stream=stream)
+        ev_done[i].record(stream)
+        # result back to the host (a stream of its own, so that the next
+        # step's input copy does not queue behind it)
+        copy_out.wait_event(ev_done[i])
+        with torch.cuda.stream(copy_out):
+            h_out[i].copy_(d_out[i], non_blocking=True)
+        ev_back[i].record(copy_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for k in range(args.warmup):
+        e2e_step(k)
     torch.cuda.synchronize()
     barrier(ws)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(K):
-        e2e_step()
+    for k in range(K):
+        e2e_step(k)
+    # the timed region ends when the last result is on the host
+    stream.wait_event(ev_back[(K - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws) / K
     e2e_value = step_bytes * ws / (e2e_ms * 1e-3) / 1e9
+    # the read-back is the step's real output
+    if not torch.equal(h_out[(K - 1) & 1], d_out[(K - 1) & 1].cpu()):
+        raise RuntimeError("e2e: output read back differs from the device copy")
     return e2e_value, e2e_ms, h2d, d2h
-
 
 
 def run_mixed(args):
