@@ -284,6 +284,7 @@ typedef struct pkv_sched_config {
     int max_model_len;          /* max prompt + generated tokens */
     const int32_t *initial_order; /* NULL or a permutation of [0, num_blocks) (copied) */
     int policy;                 /* PKV_SCHED_CONTINUOUS (0) or PKV_SCHED_STATIC (1) */
+    int prefix_caching;         /* 1: share full prompt pages between requests added with tokens */
 } pkv_sched_config;
 
 /* Admission policies.  Continuous: the rules above, every step ("Continuous
@@ -326,8 +327,25 @@ typedef struct pkv_sched_stats {
     int waiting;
     int free_blocks;
     double host_ms;         /* wall time spent inside pkv_sched_step */
+    int64_t prefix_hit_blocks; /* blocks taken from the prefix cache at admissions */
+    int cached_blocks;      /* pages registered in the prefix cache now */
 } pkv_sched_stats;
 
+/* Prefix caching ("Project 17" Step 8 "Prefix caching"; "Continuous Batching"
+ * §7 names the gain).  For requests added with their prompt tokens
+ * (pkv_sched_add_tokens) and prefix_caching = 1:
+ *   - a full page (block_size tokens) of a prompt is registered once its K/V
+ *     are computed, keyed by the block holding the preceding page and its own
+ *     tokens (which identifies the whole page-aligned prefix, as the page's
+ *     tuple key does); it is registered only if that preceding page is;
+ *   - at admission the longest chain of registered pages matching the prompt
+ *     is taken, covering at most prompt_len - 1 tokens (at least one prompt
+ *     token is always computed, so a request never writes into a page it
+ *     shares); those blocks join the request's block table with their
+ *     reference counts raised, and its computed length starts past them;
+ *   - a block returns to the free list when its last holder retires or is
+ *     preempted, and its cache entry goes with it.
+ * Block tables then carry shared block ids; the kernels need no change. */
 pkv_sched *pkv_sched_create(const pkv_sched_config *config);
 void pkv_sched_destroy(pkv_sched *sched);
 /* Queue a request.  eos_after >= 1 is the output length at which it emits
@@ -335,6 +353,10 @@ void pkv_sched_destroy(pkv_sched *sched);
  * max_tokens < 1, eos_after < 1 or a duplicate rid.  A request needing more
  * blocks than the pool holds is accepted but never admitted. */
 int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int max_tokens, int eos_after);
+/* As pkv_sched_add, with the prompt's token ids (copied; prompt_len of them)
+ * so that the request can share prompt pages through the prefix cache. */
+int pkv_sched_add_tokens(pkv_sched *sched, int64_t rid, const int32_t *tokens, int prompt_len, int max_tokens,
+                         int eos_after);
 /* One engine step.  Returns the number of scheduled sequences (0 = nothing to
  * run; *out then has num_seqs = 0), or a negative status. */
 int pkv_sched_step(pkv_sched *sched, pkv_step_meta *out);

@@ -31,6 +31,15 @@ Sources and the reading taken where they differ:
   returning blocks"); blocks are freed immediately (§1 lifecycle diagram).
 * Context length of a scheduled sequence counts its tokens appended this step
   (tiny-vllm part 7 "Uploading the active arrays to the GPU").
+* Prefix caching ("Project 17" Step 8, PrefixCache.find_prefix_match: the
+  longest page-aligned prefix of the prompt found in the cache, its pages'
+  reference counts raised).  Readings where the page is silent: a full prompt
+  page is registered once its K/V are computed, keyed by (block of the
+  preceding page, its own tokens) -- the same prefix identity as the page's
+  tuple of all tokens up to it -- and only if that preceding page is the
+  registered one; a match covers at most prompt_len - 1 tokens, so one prompt
+  token is always computed and no request writes into a shared page; a block
+  is freed when no request holds it, and leaves the cache then.
 
 Emitted per step: prefill chunks (more than one new token) first, then decode
 sequences (exactly one new token), each group in scheduling order.
@@ -82,6 +91,9 @@ class Request:
     generated: int = 0
     num_computed: int = 0          # tokens whose K/V are in the cache
     blocks: List[int] = field(default_factory=list)
+    tokens: Optional[list] = None  # prompt token ids (None: no prefix sharing)
+    registered: int = 0            # leading prompt pages registered in the prefix cache
+    reg_stopped: bool = False
     state: str = "waiting"         # waiting | running | finished
     arrival_step: int = 0
     finish_step: int = -1
@@ -113,9 +125,14 @@ def cdiv(a: int, b: int) -> int:
 class Scheduler:
     def __init__(self, num_blocks: int, block_size: int = 16, max_batch: int = 256,
                  max_num_batched_tokens: int = 8192, chunk: int = 512, max_model_len: int = 8192,
-                 initial_order=None, policy: str = "continuous"):
+                 initial_order=None, policy: str = "continuous", prefix_caching: bool = False):
         assert policy in ("continuous", "static")
         self.policy = policy
+        self.prefix_caching = prefix_caching
+        self.cache = {}          # (block of the preceding page or -1, page tokens) -> block
+        self.key_of = {}         # block -> its cache key
+        self.refcount = {}       # block -> number of requests holding it
+        self.prefix_hit_blocks = 0
         self.bs = block_size
         self.pool = BlockPool(num_blocks, initial_order)
         self.max_batch = max_batch
@@ -130,17 +147,76 @@ class Scheduler:
         self.n_preemptions = 0
         self.sum_running = 0
 
-    def add(self, rid: int, prompt_len: int, max_tokens: int, eos_after: int) -> None:
+    def add(self, rid: int, prompt_len: int, max_tokens: int, eos_after: int, tokens=None) -> None:
         # A request that needs more blocks than the pool holds is accepted but
         # never admitted (it stays at the head of the queue).
         if prompt_len < 1 or prompt_len >= self.max_model_len or max_tokens < 1 or eos_after < 1:
             raise ValueError("bad request")
-        self.waiting.append(Request(rid, prompt_len, max_tokens, eos_after, arrival_step=self.step_no))
+        if tokens is not None:
+            tokens = [int(t) for t in tokens]
+            assert len(tokens) == prompt_len
+        self.waiting.append(Request(rid, prompt_len, max_tokens, eos_after, tokens=tokens,
+                                    arrival_step=self.step_no))
+
+    # ---- blocks with reference counts, and the prefix cache
+    def _alloc(self, n: int):
+        got = self._try_alloc(n)
+        if got is not None:
+            for b in got:
+                self.refcount[b] = 1
+        return got
+
+    def _release(self, r: Request) -> None:
+        for b in r.blocks:
+            self.refcount[b] -= 1
+            if self.refcount[b] == 0:
+                del self.refcount[b]
+                self.pool.free([b])
+                if b in self.key_of:
+                    del self.cache[self.key_of.pop(b)]
+        r.blocks = []
+
+    def _page(self, r: Request, k: int):
+        return tuple(r.tokens[k * self.bs:(k + 1) * self.bs])
+
+    def find_prefix_match(self, r: Request) -> list:
+        """Blocks of the longest chain of registered pages matching r's
+        prompt, covering at most prompt_len - 1 tokens."""
+        if not self.prefix_caching or r.tokens is None:
+            return []
+        chain, parent = [], -1
+        for k in range((r.prompt_len - 1) // self.bs):
+            b = self.cache.get((parent, self._page(r, k)))
+            if b is None:
+                break
+            chain.append(b)
+            parent = b
+        return chain
+
+    def _register(self, r: Request) -> None:
+        if not self.prefix_caching or r.tokens is None or r.reg_stopped:
+            return
+        full = min(r.num_computed, r.prompt_len) // self.bs
+        while r.registered < full:
+            k = r.registered
+            parent = -1 if k == 0 else r.blocks[k - 1]
+            if k > 0 and parent not in self.key_of:
+                r.reg_stopped = True
+                return
+            key = (parent, self._page(r, k))
+            if key not in self.cache:
+                self.cache[key] = r.blocks[k]
+                self.key_of[r.blocks[k]] = key
+            elif self.cache[key] != r.blocks[k]:
+                r.reg_stopped = True
+                return
+            r.registered += 1
 
     def _preempt(self, r: Request) -> None:
-        self.pool.free(r.blocks)
-        r.blocks = []
+        self._release(r)
         r.num_computed = 0
+        r.registered = 0
+        r.reg_stopped = False
         r.state = "waiting"
         r.preemptions += 1
         self.running.remove(r)
@@ -162,7 +238,7 @@ class Scheduler:
             r = self.running[i]
             q = min(r.length - r.num_computed, self.chunk, budget)
             need = cdiv(r.num_computed + q, self.bs) - len(r.blocks)
-            got = [] if need <= 0 else self._try_alloc(need)
+            got = [] if need <= 0 else self._alloc(need)
             preempted_self = False
             while got is None:
                 victim = self.running[-1]
@@ -170,7 +246,7 @@ class Scheduler:
                 if victim is r:
                     preempted_self = True
                     break
-                got = self._try_alloc(need)
+                got = self._alloc(need)
             if preempted_self:
                 continue
             r.blocks.extend(got)
@@ -185,14 +261,21 @@ class Scheduler:
         may_admit = not static or not self.running
         while may_admit and self.waiting and len(self.running) < self.max_batch and (static or budget > 0):
             r = self.waiting[0]
-            got = self._try_alloc(cdiv(r.length, self.bs))
+            chain = self.find_prefix_match(r)
+            got = self._alloc(cdiv(r.length, self.bs) - len(chain))
             if got is None:
                 break
             self.waiting.popleft()
-            r.blocks = got
+            for b in chain:
+                self.refcount[b] += 1
+            r.blocks = chain + got
+            r.num_computed = len(chain) * self.bs
+            r.registered = len(chain)
+            r.reg_stopped = False
+            self.prefix_hit_blocks += len(chain)
             r.state = "running"
             self.running.append(r)
-            q = min(r.length, self.chunk, budget)
+            q = min(r.length - r.num_computed, self.chunk, budget)
             if q > 0:
                 scheduled.append((r, q))
                 budget -= q
@@ -202,12 +285,12 @@ class Scheduler:
         done = []
         for r, q in scheduled:
             r.num_computed += q
+            self._register(r)
             if r.num_computed == r.length:
                 r.generated += 1
                 if (r.generated >= r.eos_after or r.generated >= r.max_tokens
                         or r.length >= self.max_model_len):
-                    self.pool.free(r.blocks)
-                    r.blocks = []
+                    self._release(r)
                     r.state = "finished"
                     r.finish_step = self.step_no
                     self.running.remove(r)
@@ -256,4 +339,6 @@ class Scheduler:
             "finished": len(self.finished),
             "preemptions": self.n_preemptions,
             "sum_running": self.sum_running,
+            "prefix_hit_blocks": self.prefix_hit_blocks,
+            "cached_blocks": len(self.cache),
         }

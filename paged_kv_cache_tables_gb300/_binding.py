@@ -45,7 +45,8 @@ class StepMeta(ctypes.Structure):
 class SchedConfig(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_num_batched_tokens", ctypes.c_int), ("chunk", ctypes.c_int), ("max_model_len", ctypes.c_int),
-                ("initial_order", ctypes.POINTER(ctypes.c_int32)), ("policy", ctypes.c_int)]
+                ("initial_order", ctypes.POINTER(ctypes.c_int32)), ("policy", ctypes.c_int),
+                ("prefix_caching", ctypes.c_int)]
 
 
 SCHED_CONTINUOUS, SCHED_STATIC = 0, 1
@@ -55,7 +56,8 @@ class SchedStats(ctypes.Structure):
     _fields_ = [("steps", ctypes.c_int64), ("preemptions", ctypes.c_int64), ("admitted", ctypes.c_int64),
                 ("finished", ctypes.c_int64), ("sum_running", ctypes.c_int64), ("tokens", ctypes.c_int64),
                 ("prefill_tokens", ctypes.c_int64), ("running", ctypes.c_int), ("waiting", ctypes.c_int),
-                ("free_blocks", ctypes.c_int), ("host_ms", ctypes.c_double)]
+                ("free_blocks", ctypes.c_int), ("host_ms", ctypes.c_double), ("prefix_hit_blocks", ctypes.c_int64),
+                ("cached_blocks", ctypes.c_int)]
 
 
 def lib():
@@ -86,6 +88,7 @@ def lib():
         "pkv_sched_create": ([ctypes.POINTER(SchedConfig)], P),
         "pkv_sched_destroy": ([P], None),
         "pkv_sched_add": ([P, I64, I, I, I], I),
+        "pkv_sched_add_tokens": ([P, I64, P, I, I, I], I),
         "pkv_sched_step": ([P, ctypes.POINTER(StepMeta)], I),
         "pkv_sched_get_stats": ([P, ctypes.POINTER(SchedStats)], I),
         "pkv_sched_inject_alloc_failure": ([P, I64], I),
@@ -240,11 +243,11 @@ class Scheduler:
     """pkv_sched_*: the native iteration-level scheduler (host only)."""
 
     def __init__(self, num_blocks, block_size=16, max_batch=256, max_num_batched_tokens=8192, chunk=512,
-                 max_model_len=8192, initial_order=None, policy=SCHED_CONTINUOUS):
+                 max_model_len=8192, initial_order=None, policy=SCHED_CONTINUOUS, prefix_caching=False):
         L = lib()
         self._keep = None
         cfg = SchedConfig(num_blocks, block_size, max_batch, max_num_batched_tokens, chunk, max_model_len, None,
-                          policy)
+                          policy, 1 if prefix_caching else 0)
         if initial_order is not None:
             self._keep = np.ascontiguousarray(initial_order, dtype=np.int32)
             cfg.initial_order = self._keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
@@ -258,8 +261,15 @@ class Scheduler:
             _lib.pkv_sched_destroy(self._h)
             self._h = None
 
-    def add(self, rid, prompt_len, max_tokens, eos_after):
-        _check("pkv_sched_add", lib().pkv_sched_add(self._h, rid, prompt_len, max_tokens, eos_after))
+    def add(self, rid, prompt_len, max_tokens, eos_after, tokens=None):
+        if tokens is None:
+            _check("pkv_sched_add", lib().pkv_sched_add(self._h, rid, prompt_len, max_tokens, eos_after))
+            return
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        if t.shape != (prompt_len,):
+            raise ValueError("tokens must hold prompt_len ids")
+        _check("pkv_sched_add_tokens", lib().pkv_sched_add_tokens(self._h, rid, t.ctypes.data_as(ctypes.c_void_p),
+                                                                  prompt_len, max_tokens, eos_after))
 
     def step_raw(self):
         """One step; returns the raw StepMeta (arrays valid until the next step)."""

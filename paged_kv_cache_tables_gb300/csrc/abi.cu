@@ -26,6 +26,16 @@ int cuda_fail_driver(int cu_result, const char *what) {
 
 void set_error_message(const char *msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 
+bool first_on_device(unsigned long long *flag_bits) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return true;
+    const unsigned long long bit = 1ull << dev;
+    // races only repeat an idempotent attribute call
+    if (__atomic_load_n(flag_bits, __ATOMIC_ACQUIRE) & bit) return false;
+    __atomic_fetch_or(flag_bits, bit, __ATOMIC_ACQ_REL);
+    return true;
+}
+
 int current_sm_count(int *num_sms) {
     static int cached[64] = {0};
     int dev = 0;

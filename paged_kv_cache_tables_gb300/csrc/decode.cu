@@ -870,12 +870,11 @@ template <typename T, int D, int NT>
 static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
                          cudaStream_t stream) {
     using Sh = DecodeShape<D, NT>;
-    static bool attr_set = false;   // per instantiation; idempotent if raced
-    if (!attr_set) {
+    static unsigned long long attr_set = 0;   // per instantiation and device
+    if (first_on_device(&attr_set)) {
         cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
-        attr_set = true;
     }
     cudaError_t e = launch_pdl(paged_decode_kernel<T, D, NT>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES,
                                stream, prm, tk, tv);

@@ -14,6 +14,7 @@
 #include <cstring>
 #include <deque>
 #include <new>
+#include <string>
 #include <unordered_map>
 #include <vector>
 
@@ -127,6 +128,9 @@ struct Request {
     int num_computed = 0;     // tokens whose K/V are in the cache
     State state = WAITING;
     std::vector<int32_t> blocks;
+    std::vector<int32_t> tokens;   // prompt token ids (empty: no prefix sharing)
+    int registered = 0;            // leading prompt pages registered in the prefix cache
+    bool reg_stopped = false;      // a page of this prompt is held by another block
     int length() const { return prompt_len + generated; }
 };
 
@@ -143,6 +147,82 @@ struct pkv_sched {
     std::vector<int> running;          // request indices, admission order
     std::deque<int> waiting;
     pkv_sched_stats stats{};
+    // prefix cache: page key -> block, and each block's key (empty: none);
+    // reference count of each block = requests whose tables hold it
+    std::unordered_map<std::string, int32_t> cache;
+    std::vector<std::string> key_of;
+    std::vector<int> ref;
+
+    bool caching() const { return cfg.prefix_caching != 0; }
+
+    std::string page_key(int32_t parent, const int32_t *toks) const {
+        std::string k(sizeof(int32_t) * (1 + cfg.block_size), '\0');
+        std::memcpy(&k[0], &parent, sizeof(int32_t));
+        std::memcpy(&k[sizeof(int32_t)], toks, sizeof(int32_t) * cfg.block_size);
+        return k;
+    }
+
+    // fresh blocks: owned by one request
+    bool alloc_blocks(int n, std::vector<int32_t> &got) {
+        if (!pool.alloc(n, got)) return false;
+        for (int32_t b : got) ref[b] = 1;
+        return true;
+    }
+
+    // drop one holder of each block, in table order; a block nobody holds
+    // goes back to the free list and out of the prefix cache
+    void release_blocks(std::vector<int32_t> &blocks) {
+        for (int32_t b : blocks) {
+            if (--ref[b] > 0) continue;
+            pool.release(std::vector<int32_t>(1, b));
+            if (!key_of[b].empty()) {
+                cache.erase(key_of[b]);
+                key_of[b].clear();
+            }
+        }
+        blocks.clear();
+    }
+
+    // the registered pages matching the start of r's prompt, at most
+    // (prompt_len - 1) / block_size of them
+    void prefix_match(const Request &r, std::vector<int32_t> &chain) const {
+        chain.clear();
+        if (!caching() || r.tokens.empty()) return;
+        const int bs = cfg.block_size;
+        const int pages = (r.prompt_len - 1) / bs;
+        int32_t parent = -1;
+        for (int k = 0; k < pages; ++k) {
+            auto it = cache.find(page_key(parent, r.tokens.data() + (size_t)k * bs));
+            if (it == cache.end()) break;
+            chain.push_back(it->second);
+            parent = it->second;
+        }
+    }
+
+    // register r's prompt pages whose K/V are now computed
+    void register_pages(Request &r) {
+        if (!caching() || r.tokens.empty() || r.reg_stopped) return;
+        const int bs = cfg.block_size;
+        const int full = std::min(r.num_computed, r.prompt_len) / bs;
+        while (r.registered < full) {
+            const int k = r.registered;
+            const int32_t parent = k == 0 ? -1 : r.blocks[k - 1];
+            if (k > 0 && key_of[parent].empty()) {   // its prefix is not the registered one
+                r.reg_stopped = true;
+                return;
+            }
+            std::string key = page_key(parent, r.tokens.data() + (size_t)k * bs);
+            auto it = cache.find(key);
+            if (it == cache.end()) {
+                cache.emplace(key, r.blocks[k]);
+                key_of[r.blocks[k]] = std::move(key);
+            } else if (it->second != r.blocks[k]) {  // another block holds this page
+                r.reg_stopped = true;
+                return;
+            }
+            ++r.registered;
+        }
+    }
 
     // emitted arrays (valid until the next step)
     std::vector<int64_t> seq_rids, slot_mapping, token_rids, finished_rids;
@@ -150,9 +230,10 @@ struct pkv_sched {
 
     void preempt(int idx) {
         Request &r = reqs[idx];
-        pool.release(r.blocks);
-        r.blocks.clear();
+        release_blocks(r.blocks);
         r.num_computed = 0;
+        r.registered = 0;
+        r.reg_stopped = false;
         r.state = WAITING;
         running.erase(std::find(running.begin(), running.end(), idx));
         waiting.push_front(idx);
@@ -226,7 +307,7 @@ int pkv_sched::step(pkv_step_meta *out) {
         const int q = std::min(std::min(r.length() - r.num_computed, cfg.chunk), budget);
         const int need = cdiv(r.num_computed + q, bs) - (int)r.blocks.size();
         got.clear();
-        bool ok = need <= 0 || pool.alloc(need, got);
+        bool ok = need <= 0 || alloc_blocks(need, got);
         bool self = false;
         while (!ok) {
             const int victim = running.back();
@@ -236,7 +317,7 @@ int pkv_sched::step(pkv_step_meta *out) {
                 break;
             }
             got.clear();
-            ok = pool.alloc(need, got);
+            ok = alloc_blocks(need, got);
         }
         if (self) continue;   // r was the last running request; the loop ends
         r.blocks.insert(r.blocks.end(), got.begin(), got.end());
@@ -249,17 +330,25 @@ int pkv_sched::step(pkv_step_meta *out) {
     // (its members' prefill chunks are scheduled as the budget allows)
     const bool is_static = cfg.policy == PKV_SCHED_STATIC;
     const bool may_admit = !is_static || running.empty();
+    std::vector<int32_t> chain;
     while (may_admit && !waiting.empty() && (int)running.size() < cfg.max_batch && (is_static || budget > 0)) {
         const int idx = waiting.front();
         Request &r = reqs[idx];
+        prefix_match(r, chain);
         got.clear();
-        if (!pool.alloc(cdiv(r.length(), bs), got)) break;
+        if (!alloc_blocks(cdiv(r.length(), bs) - (int)chain.size(), got)) break;
         waiting.pop_front();
-        r.blocks = got;
+        for (int32_t b : chain) ++ref[b];
+        r.blocks = chain;
+        r.blocks.insert(r.blocks.end(), got.begin(), got.end());
+        r.num_computed = (int)chain.size() * bs;
+        r.registered = (int)chain.size();
+        r.reg_stopped = false;
+        stats.prefix_hit_blocks += (int64_t)chain.size();
         r.state = RUNNING;
         running.push_back(idx);
         ++stats.admitted;
-        const int q = std::min(std::min(r.length(), cfg.chunk), budget);
+        const int q = std::min(std::min(r.length() - r.num_computed, cfg.chunk), budget);
         if (q > 0) {
             scheduled.emplace_back(idx, q);
             budget -= q;
@@ -279,12 +368,12 @@ int pkv_sched::step(pkv_step_meta *out) {
         r.num_computed += x.second;
         stats.tokens += x.second;
         if (x.second > 1) stats.prefill_tokens += x.second;
+        register_pages(r);
         if (r.num_computed == r.length()) {
             ++r.generated;
             if (r.generated >= r.eos_after || r.generated >= r.max_tokens ||
                 r.length() >= cfg.max_model_len) {
-                pool.release(r.blocks);
-                r.blocks.clear();
+                release_blocks(r.blocks);
                 r.state = FINISHED;
                 running.erase(std::find(running.begin(), running.end(), x.first));
                 ++stats.finished;
@@ -302,7 +391,8 @@ extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
     if (!config) return nullptr;
     const pkv_sched_config &c = *config;
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.max_batch <= 0 || c.max_num_batched_tokens <= 0 ||
-        c.chunk <= 0 || c.max_model_len <= 1 || (c.policy != PKV_SCHED_CONTINUOUS && c.policy != PKV_SCHED_STATIC))
+        c.chunk <= 0 || c.max_model_len <= 1 || (c.policy != PKV_SCHED_CONTINUOUS && c.policy != PKV_SCHED_STATIC) ||
+        (c.prefix_caching != 0 && c.prefix_caching != 1))
         return nullptr;
     pkv_sched *s = new (std::nothrow) pkv_sched();
     if (!s) return nullptr;
@@ -313,6 +403,8 @@ extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
         return nullptr;
     }
     s->max_blocks = cdiv(c.max_model_len, c.block_size);
+    s->key_of.assign(c.num_blocks, std::string());
+    s->ref.assign(c.num_blocks, 0);
     return s;
 }
 
@@ -335,6 +427,15 @@ extern "C" int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int 
     return PKV_OK;
 }
 
+extern "C" int pkv_sched_add_tokens(pkv_sched *sched, int64_t rid, const int32_t *tokens, int prompt_len,
+                                    int max_tokens, int eos_after) {
+    if (!tokens) return PKV_ERR_INVALID_ARG;
+    const int rc = pkv_sched_add(sched, rid, prompt_len, max_tokens, eos_after);
+    if (rc != PKV_OK) return rc;
+    sched->reqs.back().tokens.assign(tokens, tokens + prompt_len);
+    return PKV_OK;
+}
+
 extern "C" int pkv_sched_step(pkv_sched *sched, pkv_step_meta *out) {
     if (!sched || !out) return PKV_ERR_INVALID_ARG;
     auto t0 = std::chrono::steady_clock::now();
@@ -350,6 +451,7 @@ extern "C" int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out)
     out->running = (int)sched->running.size();
     out->waiting = (int)sched->waiting.size();
     out->free_blocks = (int)sched->pool.free_list.size();
+    out->cached_blocks = (int)sched->cache.size();
     return PKV_OK;
 }
 

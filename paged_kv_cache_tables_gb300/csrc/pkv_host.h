@@ -21,6 +21,11 @@ void set_error_message(const char *msg);
 // SM count of the current device (cached per device).  PKV_OK or an error.
 int current_sm_count(int *num_sms);
 
+// Per-device "done once" flags (kernel attributes are set per device): true
+// the first time this is called for (flag, current device), false after.
+// Devices 0..63; beyond that it always returns true (setting again is harmless).
+bool first_on_device(unsigned long long *flag_bits);
+
 // Smallest workspace pkv_paged_decode_attention accepts for this shape (two
 // partial records per warp; no room left for stolen pieces).
 size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);

@@ -464,24 +464,28 @@ template <typename T, int D>
 int launch_prefill_tc(const PrefillTcParams &prm, const CUtensorMap &tk, const CUtensorMap &tv,
                       const CUtensorMap &tq, int grid, cudaStream_t stream) {
     using Sh = TcShape<D>;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e);
-        // the register split inside the kernel waits for registers that only
-        // exist if the compiled count is the one it was sized for
+    // the register split inside the kernel waits for registers that only
+    // exist if the compiled count is the one it was sized for: check it
+    // (once; the answer does not change) and refuse to launch otherwise
+    static int regs_ok = 0;   // 0 unknown, 1 as sized, -1 not
+    if (regs_ok == 0) {
         cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, paged_prefill_tc_kernel<T, D>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, paged_prefill_tc_kernel<T, D>);
         if (e != cudaSuccess) return cuda_fail(e);
-        if (fa.numRegs != kTcLaunchRegs) {
+        regs_ok = fa.numRegs == kTcLaunchRegs ? 1 : -1;
+        if (regs_ok < 0) {
             char msg[128];
             std::snprintf(msg, sizeof msg, "prefill kernel compiled to %d registers per thread, its split needs %d",
                           fa.numRegs, kTcLaunchRegs);
             set_error_message(msg);
-            return PKV_ERR_UNSUPPORTED;
         }
-        attr_set = true;
+    }
+    if (regs_ok < 0) return PKV_ERR_UNSUPPORTED;
+    static unsigned long long attr_set = 0;   // per instantiation and device
+    if (first_on_device(&attr_set)) {
+        cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e);
     }
     cudaError_t e = launch_pdl(paged_prefill_tc_kernel<T, D>, dim3(grid), dim3(kTcThreads), Sh::SMEM_BYTES, stream,
                                prm, tk, tv, tq);

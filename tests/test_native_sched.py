@@ -93,6 +93,63 @@ def test_native_matches_python_under_memory_pressure_and_injected_failures(seed)
     assert py.n_preemptions > 0
 
 
+def run_both_prefix(seed, NB=140, fail_every=0, policy="continuous"):
+    """Native vs Python with prefix caching on a trace of requests from a few
+    groups sharing page-aligned prompt heads (some prompts are a head alone)."""
+    from test_sched_oracle import shared_prefix_trace
+    rng = np.random.default_rng(seed)
+    trace = shared_prefix_trace(rng, 70)
+    order = rng.permutation(NB)
+    py = PyScheduler(NB, 16, 10, 160, 48, 320, initial_order=order, policy=policy, prefix_caching=True)
+    nat = Scheduler(NB, 16, 10, 160, 48, 320, initial_order=order, prefix_caching=True,
+                    policy={"continuous": SCHED_CONTINUOUS, "static": SCHED_STATIC}[policy])
+    i = 0
+    for step in range(5000):
+        while i < len(trace) and trace[i][0] <= step:
+            _, rid, toks, mt, eos = trace[i]
+            py.add(rid, len(toks), mt, eos, tokens=toks)
+            nat.add(rid, len(toks), mt, eos, tokens=toks)
+            i += 1
+        if fail_every and step % fail_every == 3:
+            py.pool.fail_at = py.pool.alloc_calls + 1
+            nat.inject_alloc_failure(1)
+        a = py.step()
+        b = nat.step()
+        assert (a is None) == (b is None), "step %d" % step
+        if a is not None:
+            for k in ["seq_rids", "q_lens", "context_lens", "cu_seqlens", "block_tables", "slot_mapping",
+                      "token_rids", "token_pos"]:
+                assert np.array_equal(getattr(a, k), b[k]), "step %d field %s" % (step, k)
+            assert np.array_equal(a.finished_rids, b["finished_rids"]), "step %d finished" % step
+        sa, sb = py.stats(), nat.stats()
+        for k in ["free_blocks", "running", "waiting", "finished", "preemptions", "prefix_hit_blocks",
+                  "cached_blocks"]:
+            assert sa[k] == sb[k], "step %d stat %s: %s vs %s" % (step, k, sa[k], sb[k])
+        if i == len(trace) and py.idle():
+            break
+    assert py.idle() and nat.stats()["free_blocks"] == NB and nat.stats()["cached_blocks"] == 0
+    return py
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_native_prefix_cache_matches_python(seed):
+    py = run_both_prefix(400 + seed)
+    assert py.prefix_hit_blocks > 0
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_native_prefix_cache_matches_python_under_pressure(seed):
+    py = run_both_prefix(500 + seed, NB=50, fail_every=7)
+    assert py.n_preemptions > 0 and py.prefix_hit_blocks > 0
+    run_both_prefix(600 + seed, NB=60, policy="static")
+
+
+def test_native_add_tokens_checks_length():
+    s = Scheduler(16, prefix_caching=True)
+    with pytest.raises(ValueError):
+        s.add(1, 5, 4, 4, tokens=[1, 2, 3])
+
+
 @pytest.mark.parametrize("seed", range(3))
 def test_native_matches_python_static_policy(seed):
     run_both(200 + seed, policy="static")

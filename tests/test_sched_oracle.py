@@ -215,3 +215,114 @@ def test_static_batching_admits_only_when_idle():
         if i == len(arrivals) and s.idle():
             break
     assert s.idle() and len(s.finished) == 40 and batches >= 40 // 6
+
+
+def test_prefix_cache_hand_worked_trace():
+    """Block size 4, pool [0..19] popped from the end, no chunking.
+    A: prompt 1..10, EOS after 3.  B: prompt 1..8, 50, 51, 52 (its first two
+    pages equal A's), EOS after 2, arriving at step 2.  Worked by hand:
+    step 0: A admitted with blocks 19, 18, 17, prefills 10 tokens; its two
+            full pages are registered: (-1, 1-4) -> 19, (19, 5-8) -> 18.
+    step 1: A decodes (position 10, block 17).
+    step 2: B matches both pages (2 pages <= (11 - 1) // 4): blocks 19, 18 shared,
+            one new block 16, computed length 8, prefill of 3 tokens at slots
+            64, 65, 66; A decodes position 11 (slot 17 * 4 + 3 = 71), emits its
+            third token and retires: 19 and 18 are still held by B, 17 is freed.
+    step 3: B decodes and retires: 19, 18, 16 freed in table order; the cache
+            empties."""
+    s = Scheduler(20, 4, max_batch=4, max_num_batched_tokens=100, chunk=100, max_model_len=64, prefix_caching=True)
+    s.add(0, 10, 10, 3, tokens=list(range(1, 11)))
+    m0 = s.step()
+    assert m0.block_tables[0, :3].tolist() == [19, 18, 17] and int(m0.q_lens[0]) == 10
+    assert s.stats()["cached_blocks"] == 2
+    s.step()
+    s.add(1, 11, 10, 2, tokens=list(range(1, 9)) + [50, 51, 52])
+    m2 = s.step()
+    assert m2.seq_rids.tolist() == [1, 0]                    # B's prefill chunk first
+    assert m2.q_lens.tolist() == [3, 1] and m2.context_lens.tolist() == [11, 12]
+    assert m2.block_tables[0, :3].tolist() == [19, 18, 16]
+    assert m2.slot_mapping.tolist() == [64, 65, 66, 71]
+    assert m2.finished_rids.tolist() == [0]
+    assert s.stats()["prefix_hit_blocks"] == 2
+    m3 = s.step()
+    assert m3.finished_rids.tolist() == [1]
+    assert s.idle() and s.stats()["cached_blocks"] == 0
+    assert s.pool.free_list == list(range(16)) + [17, 19, 18, 16]
+    # C's prompt is exactly A's two registered pages: only one page may be
+    # taken, so that the last prompt page is computed (in a block of its own)
+    c = Scheduler(20, 4, max_batch=4, max_num_batched_tokens=100, chunk=100, max_model_len=64, prefix_caching=True)
+    c.add(0, 10, 10, 9, tokens=list(range(1, 11)))
+    c.step()
+    c.add(2, 8, 10, 2, tokens=list(range(1, 9)))
+    mc = c.step()
+    assert mc.seq_rids.tolist() == [2, 0] and mc.q_lens.tolist() == [4, 1] and mc.context_lens.tolist() == [8, 11]
+    assert mc.block_tables[0, :2].tolist() == [19, 16]
+    # without the cache B recomputes everything in three fresh blocks
+    n = Scheduler(20, 4, max_batch=4, max_num_batched_tokens=100, chunk=100, max_model_len=64)
+    n.add(0, 10, 10, 3, tokens=list(range(1, 11)))
+    n.step()
+    n.step()
+    n.add(1, 11, 10, 2, tokens=list(range(1, 9)) + [50, 51, 52])
+    m = n.step()
+    assert m.q_lens.tolist() == [11, 1] and m.block_tables[0, :3].tolist() == [16, 15, 14]
+
+
+def shared_prefix_trace(rng, n, groups=4, prefix_pages=(1, 6), bs=16, tail=(0, 60), eos_mean=20):
+    """Requests from a few groups: each group's prompts start with the same
+    tokens (a whole number of pages), then a request's own tokens."""
+    heads = [list(rng.integers(1000, 2000, size=int(rng.integers(*prefix_pages)) * bs)) for _ in range(groups)]
+    out = []
+    for rid in range(n):
+        g = int(rng.integers(0, groups))
+        toks = heads[g] + list(rng.integers(3000, 4000, size=int(rng.integers(*tail))))
+        out.append((int(rng.integers(0, 50)), rid, toks, int(rng.integers(1, 60)), int(rng.geometric(1 / eos_mean))))
+    return sorted(out, key=lambda x: (x[0], x[1]))
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_prefix_cache_invariants(seed):
+    """With sharing: no emitted slot lands in a block two requests hold; each
+    block's count equals its holders; free + held = pool; every request emits
+    the same tokens as without sharing; the pool and cache are empty at the end."""
+    rng = np.random.default_rng(seed)
+    trace = shared_prefix_trace(rng, 60)
+    runs = {}
+    for caching in (False, True):
+        s = Scheduler(120, 16, max_batch=10, max_num_batched_tokens=160, chunk=48, max_model_len=256,
+                      prefix_caching=caching)
+        i, prefill, computed = 0, 0, {}
+        for step in range(5000):
+            while i < len(trace) and trace[i][0] <= step:
+                _, rid, toks, mt, eos = trace[i]
+                s.add(rid, len(toks), mt, eos, tokens=toks)
+                i += 1
+            m = s.step()
+            if m is not None:
+                # holders when the step was emitted: the scheduled sequences'
+                # tables, and the running requests that were not scheduled
+                held = {}
+                scheduled = set(int(x) for x in m.seq_rids)
+                rows = [row[row >= 0] for row in m.block_tables]
+                rows += [np.array(r.blocks) for r in s.running if r.rid not in scheduled]
+                for row in rows:
+                    for b in row:
+                        held[int(b)] = held.get(int(b), 0) + 1
+                prefill += int(m.q_lens[m.q_lens > 1].sum())
+                for slot in m.slot_mapping:
+                    assert held[int(slot) // 16] == 1, "step %d writes a shared block" % step
+                for rid, q in zip(m.seq_rids, m.q_lens):
+                    computed[int(rid)] = computed.get(int(rid), 0) + int(q)
+            for r in s.running:
+                for b in r.blocks:
+                    assert s.refcount[b] == sum(b in x.blocks for x in s.running)
+            held_now = set(b for r in s.running for b in r.blocks)
+            assert len(held_now) + s.pool.free_count() == 120
+            if i == len(trace) and s.idle():
+                break
+        assert s.idle() and s.pool.free_count() == 120 and not s.cache
+        # every emitted token needs at least one token computed in its step
+        for r in s.finished:
+            assert computed[r.rid] >= r.generated, r.rid
+        runs[caching] = ({r.rid: r.generated for r in s.finished}, prefill, s.prefix_hit_blocks)
+    assert runs[True][0] == runs[False][0]
+    assert runs[True][2] > 0 and runs[True][1] < runs[False][1]
