@@ -392,7 +392,7 @@ def run_mixed(args):
     }
 
 
-def trace_line(args, n, NB, policy="continuous", outputs="geometric"):
+def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=False, caching=False):
     """The continuous-batching trace: n requests, Poisson(20) arrivals per
     step, prompts lognormal (mean 512, sigma 1, clipped 8..4096), outputs
     geometric (or lognormal) with mean 256, max batch 256, 8192-token budget,
@@ -404,19 +404,24 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric"):
     from paged_kv_cache_tables_gb300 import _binding
     from paged_kv_cache_tables_gb300.engine import PagedEngine, run_trace
     from synth import SEEDS
-    from synth.trace import make_fill, make_requests, pick_rows
+    from synth.trace import content_keys, make_fill, make_requests, make_shared_requests, pick_rows
     torch.cuda.set_device(0)
     seed = SEEDS["trace"]
     L, R = args.trace_layers, args.trace_caches
-    arrival, prompt, eos = make_requests(seed, n=n, outputs=outputs)
+    tokens, row_keys = None, None
+    if shared:
+        arrival, prompt, eos, tokens, head_len, group = make_shared_requests(seed, n=n)
+        row_keys = lambda r, p: content_keys(r, p, head_len, group)
+    else:
+        arrival, prompt, eos = make_requests(seed, n=n, outputs=outputs)
     pol = {"continuous": _binding.SCHED_CONTINUOUS, "static": _binding.SCHED_STATIC}[policy]
     eng = PagedEngine(NB, num_layers=L, num_caches=R, initial_order=np.random.default_rng(seed).permutation(NB),
-                      policy=pol)
+                      policy=pol, prefix_caching=caching, row_keys=row_keys)
     rng = np.random.default_rng(seed + 1)
     clk = ClockSampler(0)
     with clk:
         res = run_trace(eng, arrival, prompt, eos, max_tokens=4096, fill=make_fill(), sample_every=50,
-                        pick=lambda info: pick_rows(info, rng, n_decode=1, n_prefill=1))
+                        pick=lambda info: pick_rows(info, rng, n_decode=1, n_prefill=1), tokens=tokens)
     if int(eng.status.item()) != 0:
         raise RuntimeError("device status %d in the trace" % int(eng.status.item()))
     st = eng.sched.stats()
@@ -460,7 +465,8 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric"):
     for rows, vals in res["samples"]:
         for (row, rid, pos), got in zip(rows, vals.numpy()):
             t0 = time.perf_counter()
-            ref = layer0_row(rid, pos, Hq, Hkv, d)
+            ref = layer0_row(rid, pos, Hq, Hkv, d, keys=None if row_keys is None else
+                             (lambda ps, r=rid: row_keys(np.full(len(ps), r), ps)))
             t_or += time.perf_counter() - t0
             keys += pos + 1
             err = np.abs(got.astype(np.float64) - ref)
@@ -490,6 +496,7 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric"):
         "avg_running_batch": round(st["sum_running"] / max(1, st["steps"]), 2),
         "latency_steps_p50": float(np.percentile(lat, 50)), "latency_steps_p99": float(np.percentile(lat, 99)),
         "ttft_steps_mean": round(float(ttft_steps.mean()), 2), "ttft_ms_mean": round(float(ttft_ms.mean()), 3),
+        "prefill_tokens": st["prefill_tokens"], "prefix_hit_blocks": st["prefix_hit_blocks"],
         "upload_bytes_per_step": int(eng.upload_bytes / max(1, len(steps))),
         "oracle_check": {"rows": checked, "max_abs_err": worst, "every": "50th engine step, layer 0",
                          "oracle_s": round(t_or, 2), "oracle_keys_per_s": round(keys / max(t_or, 1e-9), 1)},
@@ -500,6 +507,29 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric"):
 
 def run_trace_bench(args):
     print(json.dumps(trace_line(args, args.trace_requests, args.trace_pool)))
+
+
+def run_prefix_bench(args):
+    """Prefix caching on a sharing-heavy trace: 1000 requests in 8 groups whose
+    prompts share a head (lognormal, mean 1024 tokens, whole pages) followed by
+    their own tail (lognormal, mean 128), outputs geometric with mean 256; the
+    same engine with and without the prefix cache."""
+    n = args.trace_requests
+    off = trace_line(args, n, args.trace_pool, shared=True, caching=False)
+    on = trace_line(args, n, args.trace_pool, shared=True, caching=True)
+    keep = ["engine_steps", "wall_s", "output_tokens", "output_tokens_per_s", "prefill_tokens", "prefix_hit_blocks",
+            "avg_running_batch", "ttft_steps_mean", "ttft_ms_mean", "latency_steps_p50", "latency_steps_p99",
+            "preemptions", "oracle_check", "clocks"]
+    print(json.dumps({
+        "metric": "prefix caching: output tokens/s, prefill tokens and mean time to first token",
+        "workload": "%d requests in 8 groups sharing a prompt head (lognormal mean 1024, whole pages) + own tail "
+                    "(lognormal mean 128), outputs geometric mean 256, Poisson(20)/step, max batch 256, budget 8192, "
+                    "chunk 512, pool %d blocks, %d layers (8B shape)" % (n, args.trace_pool, args.trace_layers),
+        "no_cache": {k: off[k] for k in keep}, "cache": {k: on[k] for k in keep},
+        "throughput_ratio": round(on["output_tokens_per_s"] / off["output_tokens_per_s"], 3),
+        "prefill_token_ratio": round(off["prefill_tokens"] / max(1, on["prefill_tokens"]), 3),
+        "ttft_ratio_no_cache_over_cache": round(off["ttft_ms_mean"] / on["ttft_ms_mean"], 3),
+    }))
 
 
 def run_batching_bench(args):
@@ -646,8 +676,9 @@ def main():
     ap.add_argument("--mixed-prior", type=int, default=-1,
                     help="give every prefill chunk this prior context instead of U{0..4096} (profiling)")
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching"],
-                    help="trace: the continuous-batching trace; batching: static vs continuous on one trace")
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching", "prefix"],
+                    help="trace: the continuous-batching trace; batching: static vs continuous on one trace; "
+                         "prefix: with and without the prefix cache on a sharing-heavy trace")
     ap.add_argument("--trace-requests", type=int, default=1000)
     ap.add_argument("--trace-layers", type=int, default=32)
     ap.add_argument("--trace-caches", type=int, default=4)
@@ -662,6 +693,9 @@ def main():
         return
     if args.workload == "batching":
         run_batching_bench(args)
+        return
+    if args.workload == "prefix":
+        run_prefix_bench(args)
         return
     if args.only_mixed:
         import torch

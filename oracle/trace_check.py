@@ -14,15 +14,19 @@ from synth.trace import kv_tag, q_tag, token_rows
 from . import decode
 
 
-def layer0_row(rid, pos, Hq, Hkv, d, dtype="bf16"):
+def layer0_row(rid, pos, Hq, Hkv, d, dtype="bf16", keys=None):
+    """keys(positions) -> the row keys of the request's tokens (default: the
+    request id; a shared prompt head uses its group's key)."""
     n = pos + 1
     nb = -(-n // 16)
-    ks = token_rows(np.full(n, rid), np.arange(n), kv_tag(0, "k"), Hkv * d, dtype).reshape(n, Hkv, d)
-    vs = token_rows(np.full(n, rid), np.arange(n), kv_tag(0, "v"), Hkv * d, dtype).reshape(n, Hkv, d)
+    kk = np.full(n, rid) if keys is None else keys(np.arange(n))
+    ks = token_rows(kk, np.arange(n), kv_tag(0, "k"), Hkv * d, dtype).reshape(n, Hkv, d)
+    vs = token_rows(kk, np.arange(n), kv_tag(0, "v"), Hkv * d, dtype).reshape(n, Hkv, d)
     kc = np.full((nb * 16, Hkv, d), NAN_BITS[dtype], np.uint16)
     vc = kc.copy()
     kc[:n], vc[:n] = ks, vs
     kc = kc.reshape(nb, 16, Hkv, d).transpose(0, 2, 1, 3).copy()
     vc = vc.reshape(nb, 16, Hkv, d).transpose(0, 2, 1, 3).copy()
-    q = token_rows(np.array([rid]), np.array([pos]), q_tag(0), Hq * d, dtype).reshape(1, Hq, d)
+    qk = np.array([rid]) if keys is None else keys(np.array([pos]))
+    q = token_rows(qk, np.array([pos]), q_tag(0), Hq * d, dtype).reshape(1, Hq, d)
     return decode(q, kc, vc, np.arange(nb, dtype=np.int32)[None], np.array([n], np.int32), dtype)[0]

@@ -25,7 +25,7 @@ from . import _binding as B
 class PagedEngine:
     def __init__(self, num_blocks, num_layers=32, num_caches=4, Hq=32, Hkv=8, d=128, dtype="bf16",
                  max_batch=256, max_num_batched_tokens=8192, chunk=512, max_model_len=8192, initial_order=None,
-                 device="cuda", policy=B.SCHED_CONTINUOUS):
+                 device="cuda", policy=B.SCHED_CONTINUOUS, prefix_caching=False, row_keys=None):
         import torch
         self.torch = torch
         self.L, self.R = num_layers, num_caches
@@ -33,7 +33,10 @@ class PagedEngine:
         self.NB = num_blocks
         self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
         self.sched = B.Scheduler(num_blocks, 16, max_batch, max_num_batched_tokens, chunk, max_model_len,
-                                 initial_order=initial_order, policy=policy)
+                                 initial_order=initial_order, policy=policy, prefix_caching=prefix_caching)
+        # row_keys(token_rids, token_pos) -> int64 keys handed to `fill` in
+        # place of the request ids (a caller whose rows depend on content)
+        self.row_keys = row_keys
         self.max_blocks = self.sched.max_blocks
         self.max_T = max_num_batched_tokens
         self.max_S = max_batch
@@ -65,8 +68,8 @@ class PagedEngine:
         self.wait_ms = 0.0      # host time spent waiting for a staging buffer
         self.upload_bytes = 0
 
-    def add(self, rid, prompt_len, max_tokens, eos_after):
-        self.sched.add(rid, prompt_len, max_tokens, eos_after)
+    def add(self, rid, prompt_len, max_tokens, eos_after, tokens=None):
+        self.sched.add(rid, prompt_len, max_tokens, eos_after, tokens=tokens)
 
     def step(self, fill, on_layer_done=None):
         """One engine step.  Returns None when nothing was scheduled, else a
@@ -89,7 +92,8 @@ class PagedEngine:
         self.wait_ms += waited
         h64, h32 = self.h_i64[buf].numpy(), self.h_i32[buf].numpy()
         h64[:T] = arr(m.slot_mapping, T)
-        h64[T:2 * T] = arr(m.token_rids, T)
+        h64[T:2 * T] = (arr(m.token_rids, T) if self.row_keys is None
+                        else self.row_keys(arr(m.token_rids, T), arr(m.token_pos, T)))
         o = 0
         h32[o:o + T] = arr(m.token_pos, T); o += T
         h32[o:o + S] = arr(m.context_lens, S); o += S
@@ -151,7 +155,8 @@ class PagedEngine:
         return info
 
 
-def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pick=None, max_steps=1000000):
+def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pick=None, max_steps=1000000,
+              tokens=None):
     """Drive `engine` through a request trace: request i is added at engine
     step arrival[i]; steps run until every request has finished.  On every
     `sample_every`-th engine step, pick(info) names (output row, rid,
@@ -181,7 +186,7 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
     for step in range(max_steps):
         while nxt < n and arrival[order[nxt]] <= step:
             i = int(order[nxt])
-            engine.add(i, int(prompt[i]), int(max_tokens), int(eos[i]))
+            engine.add(i, int(prompt[i]), int(max_tokens), int(eos[i]), tokens=None if tokens is None else tokens[i])
             nxt += 1
         state["sample"] = bool(sample_every) and pick is not None and len(steps) % sample_every == 0
         info = engine.step(fill, on_layer_done=on_layer)

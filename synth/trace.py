@@ -85,6 +85,54 @@ def make_requests(seed: int, n: int = 1000, rate: float = 20.0, prompt_mean: flo
     return arrival, prompt, eos
 
 
+GROUP_KEY_BASE = 0x80000000   # content keys of shared prompt heads (request ids stay below)
+
+
+def make_shared_requests(seed: int, n: int = 1000, rate: float = 20.0, groups: int = 8,
+                         head_mean: float = 1024.0, tail_mean: float = 128.0, sigma: float = 1.0,
+                         out_mean: float = 256.0, bs: int = 16, pmax: int = 4096):
+    """A sharing-heavy trace: every request belongs to one of `groups` groups
+    whose prompts start with the same head (lognormal length with mean
+    head_mean, rounded down to whole pages of bs tokens, at least one page),
+    followed by the request's own tail (lognormal, mean tail_mean, at least 1
+    token); prompts clipped to pmax.  Returns arrival, prompt_len, eos_after,
+    tokens (list of int32 arrays), head_len and group (int64 arrays)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    arrival = np.empty(n, dtype=np.int64)
+    k, step = 0, 0
+    while k < n:
+        m = int(rng.poisson(rate))
+        take = min(m, n - k)
+        arrival[k:k + take] = step
+        k += take
+        step += 1
+    mh = np.log(head_mean) - sigma * sigma / 2
+    heads_len = np.maximum(np.floor(rng.lognormal(mh, sigma, size=groups) / bs), 1).astype(np.int64) * bs
+    heads_len = np.minimum(heads_len, (pmax // 2) // bs * bs)
+    heads = [rng.integers(1, 1 << 20, size=int(h), dtype=np.int64).astype(np.int32) for h in heads_len]
+    group = rng.integers(0, groups, size=n).astype(np.int64)
+    mt = np.log(tail_mean) - sigma * sigma / 2
+    tail = np.maximum(np.rint(rng.lognormal(mt, sigma, size=n)), 1).astype(np.int64)
+    eos = rng.geometric(1.0 / out_mean, size=n).astype(np.int64)
+    tokens, prompt, head_len = [], np.empty(n, np.int64), np.empty(n, np.int64)
+    for i in range(n):
+        t = min(int(tail[i]), pmax - int(heads_len[group[i]]))
+        own = rng.integers(1 << 20, 1 << 30, size=t, dtype=np.int64).astype(np.int32)
+        tokens.append(np.concatenate([heads[group[i]], own]))
+        prompt[i] = len(tokens[-1])
+        head_len[i] = heads_len[group[i]]
+    return arrival, prompt, eos, tokens, head_len, group
+
+
+def content_keys(rids, pos, head_len, group):
+    """Key of the row of token (rids[i], pos[i]): inside its request's shared
+    head the group's key (the same prefix has the same K/V whichever request
+    computed it), else the request id."""
+    rids = np.asarray(rids, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    return np.where(pos < head_len[rids], GROUP_KEY_BASE + group[rids], rids)
+
+
 # ---------------------------------------------------------------- GPU generator
 
 _lib = None

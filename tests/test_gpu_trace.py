@@ -77,3 +77,46 @@ def test_trace_under_memory_pressure_preempts_and_recomputes_exactly(cuda_lib, s
     assert st["free_blocks"] == 96
     assert int(eng.status.item()) == 0
     assert check_samples(res) >= 10
+
+
+def run_shared(n, NB, caching, seed, layers=2, max_batch=16, budget=256, chunk=64, mml=1024):
+    from synth.trace import content_keys, make_shared_requests
+    arrival, prompt, eos, tokens, head_len, group = make_shared_requests(
+        seed, n=n, rate=6, groups=3, head_mean=96, tail_mean=30, out_mean=10, pmax=mml // 2)
+    eng = PagedEngine(NB, num_layers=layers, num_caches=2, Hq=HQ, Hkv=HKV, d=D, max_batch=max_batch,
+                      max_num_batched_tokens=budget, chunk=chunk, max_model_len=mml,
+                      initial_order=np.random.default_rng(seed).permutation(NB), prefix_caching=caching,
+                      row_keys=lambda r, p: content_keys(r, p, head_len, group))
+    rng = np.random.default_rng(seed + 1)
+    res = run_trace(eng, arrival, prompt, eos, max_tokens=mml, fill=make_fill(), sample_every=3,
+                    pick=lambda info: pick_rows(info, rng), tokens=tokens)
+    checked = 0
+    for rows, vals in res["samples"]:
+        for (row, rid, pos), got in zip(rows, vals.numpy()):
+            ref = layer0_row(rid, pos, HQ, HKV, D, keys=lambda ps, r=rid: content_keys(np.full(len(ps), r), ps,
+                                                                                       head_len, group))
+            assert_close(got, ref, "bf16", what="rid %d pos %d" % (rid, pos))
+            checked += 1
+    return eng, res, checked
+
+
+def test_prefix_cached_trace_reads_shared_pages_correctly(cuda_lib, synth_gpu):
+    """Requests sharing prompt heads: with prefix caching their block tables
+    point at the same physical pages, written once; every sampled row still
+    equals the oracle on the request's own (content-keyed) rows."""
+    eng, res, checked = run_shared(48, 4096, True, seed=21)
+    st = eng.sched.stats()
+    assert len(res["finish_step"]) == 48 and int(eng.status.item()) == 0
+    assert st["prefix_hit_blocks"] > 20 and st["cached_blocks"] == 0 and st["free_blocks"] == 4096
+    assert checked >= 20
+    # the same trace without sharing computes more prefill tokens
+    eng2, _, _ = run_shared(48, 4096, False, seed=21)
+    assert eng2.sched.stats()["prefill_tokens"] > st["prefill_tokens"]
+
+
+def test_prefix_cached_trace_under_memory_pressure(cuda_lib, synth_gpu):
+    eng, res, checked = run_shared(40, 60, True, seed=23, budget=512, chunk=128, mml=512)
+    st = eng.sched.stats()
+    assert len(res["finish_step"]) == 40 and int(eng.status.item()) == 0
+    assert st["preemptions"] > 0 and st["prefix_hit_blocks"] > 0 and st["free_blocks"] == 60
+    assert checked >= 10
