@@ -371,6 +371,30 @@ def run_mixed(args):
         raise RuntimeError("device status %d in the mixed step" % int(status.item()))
     ms = lambda a, b: statistics.mean(evs[k][a].elapsed_time(evs[k][b]) for k in range(K))
     step_ms, app_ms, pre_ms, dec_ms = ms(0, 3), ms(0, 1), ms(1, 2), ms(2, 3)
+
+    # the same step through the mixed entry point: prefill and decode side by
+    # side on split SMs (the split picked from the host copies of the metadata)
+    out2 = torch.empty_like(out)
+    cu_h, cl_h = st.cu_seqlens[:p + 1].astype(np.int32), st.context_lens.astype(np.int32)
+    d_sms = pkv.mixed_split(torch.cuda.get_device_properties(0).multi_processor_count, cu_h, p, cl_h, st.Hq,
+                            st.Hkv, st.d)
+
+    def fused():
+        pkv.kv_append(kn, vn, slots, kc, vc, dev_status=status, stream=stream)
+        pkv.paged_mixed_attention(out2, q, cu_p, p, max_q, kc, vc, bt, cl, workspace=work, cu_seqlens_host=cu_h,
+                                  context_lens_host=cl_h, dev_status=status, stream=stream)
+    for _ in range(args.warmup):
+        fused()
+    torch.cuda.synchronize()
+    fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in fe:
+        a.record(stream)
+        fused()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the side-by-side mixed step" % int(status.item()))
+    fused_ms = statistics.mean(a.elapsed_time(b) for a, b in fe)
     flops = prefill_flops(st.context_lens[:p], st.q_lens[:p], st.Hq, st.d)
     dbytes = decode_bytes(st.context_lens[p:], st.Hq, st.Hkv, st.d)
     tpeak, tkind = load_tensor_peak()
@@ -380,7 +404,11 @@ def run_mixed(args):
         "workload": "mixed: %d prefill chunks x 512 (prior %s) + 248 decodes (ctx U{256..4096}), 32/8 heads, "
                     "d 128, bf16; append of %d tokens first"
                     % (p, "U{0..4096}" if args.mixed_prior < 0 else args.mixed_prior, st.T),
-        "steps": K, "ms_per_step": round(step_ms, 4),
+        "steps": K, "ms_per_step": round(fused_ms, 4),
+        "sequential_ms_per_step": round(step_ms, 4),
+        "side_by_side": {"ms_per_step": round(fused_ms, 4), "decode_sms": d_sms,
+                         "note": "append, then pkv_paged_mixed_attention: decode on decode_sms SMs, prefill on the "
+                                 "rest, concurrently; the kernel timings below are the sequential run"},
         "kv_append_ms": round(app_ms, 4),
         "prefill": {"ms": round(pre_ms, 4), "gflop": round(flops / 1e9, 2), "tflops": round(tfl, 1),
                     "roofline": {"bound": "tensor", "achieved": round(tfl, 1), "peak": tpeak, "unit": "TFLOP/s",

@@ -184,6 +184,48 @@ int pkv_paged_prefill_attention(void *out, const void *q, const int32_t *cu_seql
                                 int *dev_status, void *stream);
 
 /*
+ * pkv_paged_mixed_attention -- the attention of one mixed engine step, prefill
+ * chunks and decodes in one batch ("Continuous Batching" §5 "Mixed batching
+ * (prefill + decode in one step)"), with the two kernels side by side.
+ *
+ * Layout as the scheduler emits it: the first num_prefill sequences are
+ * prefill chunks (rows [0, prefill_tokens) of q/out, cu_seqlens with
+ * num_prefill + 1 entries, prefill_tokens = cu_seqlens[num_prefill]), the
+ * next num_decode sequences are decodes (one row each, rows prefill_tokens
+ * onward); block_tables and context_lens hold num_prefill + num_decode rows.
+ * Results equal pkv_paged_prefill_attention on the first part and
+ * pkv_paged_decode_attention on the second (workspace as for decode, sized
+ * for num_decode sequences).
+ *
+ * The decode kernel runs on decode_sms SMs and the prefill kernel on the
+ * others, on a library-owned side stream forked from and joined back into
+ * `stream` with events (one per device, created on first use; the fork and
+ * join of concurrent calls are serialised).  decode_sms <= 0 picks the split:
+ * from pkv_mixed_split when cu_seqlens_host and context_lens_host (host
+ * copies of the same arrays, num_prefill + 1 and num_prefill + num_decode
+ * entries) are given, else 3/5 of the SMs.  The pages describe no such
+ * overlap; it exists because prefill is bound by the tensor cores and decode
+ * by HBM.
+ */
+int pkv_paged_mixed_attention(void *out, const void *q, const int32_t *cu_seqlens, int num_prefill,
+                              int prefill_tokens, int max_q_len, int num_decode, const void *k_cache,
+                              const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int num_blocks, int num_q_heads, int num_kv_heads,
+                              int head_dim, int block_size, float scale, int dtype, int out_dtype, void *workspace,
+                              size_t workspace_bytes, const int32_t *cu_seqlens_host,
+                              const int32_t *context_lens_host, int decode_sms, int *dev_status, void *stream);
+
+/*
+ * The SMs pkv_paged_mixed_attention gives the decode kernel for a step (host
+ * arrays as above): the split that balances the two kernels' times under a
+ * model of their per-SM rates on GB300 -- prefill ~7 TFLOP/s of algorithmic
+ * work per SM, decode ~55 GB/s per SM up to 6.2 TB/s in total.  num_sms when
+ * there is no prefill, 0 when there is no decode.  Pure host code.
+ */
+int pkv_mixed_split(int num_sms, const int32_t *cu_seqlens, int num_prefill, const int32_t *context_lens,
+                    int num_decode, int num_q_heads, int num_kv_heads, int head_dim, int elem_bytes);
+
+/*
  * pkv_paged_decode_attention_static -- the same decode attention, for callers
  * that cannot allocate device memory.  The pages describe no counterpart:
  * this entry point exists only for the memory model of some callers.

@@ -78,6 +78,9 @@ def lib():
         "pkv_paged_decode_attention": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, SZ, P, P], I),
         "pkv_paged_prefill_attention": ([P, P, P, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, P], I),
         "pkv_paged_decode_attention_static": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P], I),
+        "pkv_paged_mixed_attention": ([P, P, P, I, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, SZ, P, P, I, P, P],
+                                      I),
+        "pkv_mixed_split": ([I, P, I, P, I, I, I, I, I], I),
         "pkv_pool_create": ([I, P], P),
         "pkv_pool_destroy": ([P], None),
         "pkv_pool_alloc": ([P, I, P], I),
@@ -194,6 +197,54 @@ def paged_prefill_attention(out, q, cu_seqlens, max_q_len, k_cache, v_cache, blo
         _dev(context_lens, "context_lens", torch.int32, 1), NB, Hq, Hkv, d, bs, float(scale), _dtype_code(q),
         _dtype_code(out), _status_ptr(dev_status), _stream(stream))
     _check("pkv_paged_prefill_attention", st)
+
+
+def paged_mixed_attention(out, q, cu_seqlens, num_prefill, max_q_len, k_cache, v_cache, block_tables, context_lens,
+                          scale=None, workspace=None, cu_seqlens_host=None, context_lens_host=None, decode_sms=0,
+                          dev_status=None, stream=None):
+    """pkv_paged_mixed_attention: rows [0, cu_seqlens[num_prefill]) of q/out are
+    the prefill chunks, the rest one decode row each; block_tables and
+    context_lens hold the prefill sequences first.  Host copies of cu_seqlens
+    and context_lens (numpy int32) let the library pick the SM split."""
+    import torch
+    L = lib()
+    T, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    S = context_lens.shape[0]
+    num_decode = S - num_prefill
+    if cu_seqlens_host is not None:
+        cu_seqlens_host = np.ascontiguousarray(cu_seqlens_host, dtype=np.int32)
+        prefill_tokens = int(cu_seqlens_host[num_prefill])
+    else:
+        prefill_tokens = T - num_decode
+    if context_lens_host is not None:
+        context_lens_host = np.ascontiguousarray(context_lens_host, dtype=np.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(max(16, decode_workspace_size(num_decode, Hq, Hkv, d)), dtype=torch.uint8,
+                                device=q.device)
+    hp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    st = L.pkv_paged_mixed_attention(
+        _dev(out, "out", ndim=3), _dev(q, "q", ndim=3), _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), num_prefill,
+        prefill_tokens, int(max_q_len), num_decode, _dev(k_cache, "k_cache", q.dtype, 4),
+        _dev(v_cache, "v_cache", q.dtype, 4), _dev(block_tables, "block_tables", torch.int32, 2),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32, 1), NB, Hq, Hkv, d, bs, float(scale),
+        _dtype_code(q), _dtype_code(out), _dev(workspace, "workspace"), workspace.numel(), hp(cu_seqlens_host),
+        hp(context_lens_host), int(decode_sms), _status_ptr(dev_status), _stream(stream))
+    _check("pkv_paged_mixed_attention", st)
+
+
+def mixed_split(num_sms, cu_seqlens, num_prefill, context_lens, num_q_heads, num_kv_heads, head_dim, elem_bytes=2):
+    """pkv_mixed_split on host arrays: the SMs the decode kernel gets."""
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    r = lib().pkv_mixed_split(num_sms, cu.ctypes.data_as(ctypes.c_void_p), num_prefill,
+                              cl.ctypes.data_as(ctypes.c_void_p), len(cl) - num_prefill, num_q_heads, num_kv_heads,
+                              head_dim, elem_bytes)
+    if r < 0:
+        raise PkvError("pkv_mixed_split", r)
+    return r
 
 
 # ------------------------------------------------------------ host pool / scheduler

@@ -17,7 +17,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpkv.so")
 
-SOURCES = ["abi.cu", "append.cu", "decode.cu", "decode_static.cu", "prefill.cu", "prefill_tc.cu", "host_sched.cpp"]
+SOURCES = ["abi.cu", "append.cu", "decode.cu", "decode_static.cu", "prefill.cu", "prefill_tc.cu", "mixed.cu",
+           "host_sched.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -949,13 +949,14 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
            records_recommended(nw) * (size_t)record_floats(G, head_dim) * sizeof(float);
 }
 
-extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
-                                          const int32_t *block_tables, int max_blocks_per_seq,
-                                          const int32_t *context_lens, int num_seqs, int num_blocks,
-                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                          float scale, int dtype, int out_dtype, void *workspace,
-                                          size_t workspace_bytes, int *dev_status, void *stream) {
-    using namespace pkv;
+namespace pkv {
+
+// The decode entry point with the grid capped at max_sms CTAs (0: one per SM).
+int decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                     int num_blocks, int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                     int dtype, int out_dtype, void *workspace, size_t workspace_bytes, int *dev_status,
+                     cudaStream_t stream, int max_sms) {
     if (num_seqs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
         return PKV_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
@@ -980,6 +981,7 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     const int64_t upper = (int64_t)num_seqs * num_kv_heads * max_blocks_per_seq;
     int grid = (int)((upper + kDecodeWarps - 1) / kDecodeWarps);
     if (grid > sms) grid = sms;
+    if (max_sms > 0 && grid > max_sms) grid = max_sms;
     if (grid < 1) grid = 1;
     const int total_warps = grid * kDecodeWarps;
     // range offsets are 24-bit fields
@@ -1025,7 +1027,7 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     const char *det = std::getenv("PKV_DETERMINISTIC");
     if (det && det[0] == '1') prm.steal_cap = 0;
     prm.epoch = next_epoch();
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t st = stream;
     const bool wide = G > 8;
     if (dtype == PKV_DTYPE_BF16) {
         if (head_dim == 128)
@@ -1039,4 +1041,17 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
                     : launch_decode<__half, 128, 1>(prm, tk, tv, grid, st);
     return wide ? launch_decode<__half, 64, 2>(prm, tk, tv, grid, st)
                 : launch_decode<__half, 64, 1>(prm, tk, tv, grid, st);
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *context_lens, int num_seqs, int num_blocks,
+                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          float scale, int dtype, int out_dtype, void *workspace,
+                                          size_t workspace_bytes, int *dev_status, void *stream) {
+    return pkv::decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                 num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype,
+                                 workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), 0);
 }

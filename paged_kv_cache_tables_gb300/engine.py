@@ -129,6 +129,10 @@ class PagedEngine:
         pwork, nwork = self.work.data_ptr(), self.work.numel()
         dt = B.DTYPE_BF16 if self.tdt == torch.bfloat16 else B.DTYPE_F16
         scale = 1.0 / float(np.sqrt(self.d))
+        # host copies of cu_seqlens and context lengths (the scheduler's arrays,
+        # valid until its next step) let the library split the SMs
+        hcu = ctypes.cast(m.cu_seqlens, ctypes.c_void_p) if P else None
+        hctx = ctypes.cast(m.context_lens, ctypes.c_void_p) if P else None
         kc = [t.data_ptr() for t in self.k_cache]
         vc = [t.data_ptr() for t in self.v_cache]
         NB, Hq, Hkv, d = self.NB, self.Hq, self.Hkv, self.d
@@ -139,10 +143,15 @@ class PagedEngine:
             cid = layer % self.R
             fill(layer, cid, q, k, v, trids, tpos)
             rc = L.pkv_kv_append(pk, pv, pslots, T, kc[cid], vc[cid], NB, 16, Hkv, d, dt, pst, pstream)
-            if rc == B.PKV_OK and P:
+            if rc == B.PKV_OK and P and S > P:
+                # prefill chunks and decodes side by side on split SMs
+                rc = L.pkv_paged_mixed_attention(pout, pq, pcu, P, t1, max_q, S - P, kc[cid], vc[cid], ptab, MB, pctx,
+                                                 NB, Hq, Hkv, d, 16, scale, dt, dt, pwork, nwork, hcu, hctx, 0, pst,
+                                                 pstream)
+            elif rc == B.PKV_OK and P:
                 rc = L.pkv_paged_prefill_attention(pout, pq, pcu, P, max_q, t1, kc[cid], vc[cid], ptab, MB, pctx, NB,
                                                    Hq, Hkv, d, 16, scale, dt, dt, pst, pstream)
-            if rc == B.PKV_OK and S > P:
+            elif rc == B.PKV_OK and S > P:
                 rc = L.pkv_paged_decode_attention(pout + t1 * row_q, pq + t1 * row_q, kc[cid], vc[cid],
                                                   ptab + P * MB * 4, MB, pctx + P * 4, S - P, NB, Hq, Hkv, d, 16,
                                                   scale, dt, dt, pwork, nwork, pst, pstream)

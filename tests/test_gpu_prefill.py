@@ -129,3 +129,37 @@ def test_prefill_flags_a_chunk_longer_than_its_context(cuda_lib):
     torch.cuda.synchronize()
     assert int(ds.status.item()) & 16
     assert torch.all(out[:5] == 0)    # the bad chunk's rows were not written
+
+
+@pytest.mark.parametrize("decode_sms", [0, 24, 130])
+def test_mixed_entry_side_by_side_matches_oracle(cuda_lib, decode_sms):
+    """pkv_paged_mixed_attention on the mixed step (prefill and decode kernels
+    on split SMs, the split picked from host metadata or forced): the prefill
+    rows are the bits of the plain prefill call, and sampled rows of both parts
+    match the oracle."""
+    from paged_kv_cache_tables_gb300 import paged_mixed_attention
+    st = make_step("mixed")
+    ds = DeviceStep(st)
+    kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
+    p = st.n_prefill
+    t1 = int(st.cu_seqlens[p])
+    out = torch.full((st.T, st.Hq, st.d), float("nan"), dtype=torch.float32, device="cuda")
+    paged_mixed_attention(out, ds.q, ds.cu_seqlens[:p + 1], p, 512, ds.k_cache, ds.v_cache, ds.block_tables,
+                          ds.context_lens, cu_seqlens_host=st.cu_seqlens[:p + 1], context_lens_host=st.context_lens,
+                          decode_sms=decode_sms, dev_status=ds.status)
+    pre = torch.empty((t1, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    paged_prefill_attention(pre, ds.q[:t1], ds.cu_seqlens[:p + 1], 512, ds.k_cache, ds.v_cache,
+                            ds.block_tables[:p], ds.context_lens[:p], dev_status=ds.status)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) == 0
+    assert torch.equal(out[:t1], pre)
+    assert np.all(np.isfinite(out.cpu().numpy()))
+    kc, vc = oracle_after_append(st)
+    rows = [(c, i) for c in range(p) for i in (0, 300, 511)]
+    ref = sampled_prefill_reference(st, kc, vc, rows)
+    got = np.stack([out_to_f64(out[int(st.cu_seqlens[c]) + i]) for c, i in rows])
+    assert_close(got, ref, "fp32", what="mixed entry prefill rows")
+    pick = [0, 7, 123, 247]
+    q_d, bt_d, cl_d = st.decode_part()
+    refd = oracle.decode(q_d[pick], kc, vc, bt_d[pick], cl_d[pick], st.dtype)
+    assert_close(out_to_f64(out[t1:])[pick], refd, "fp32", what="mixed entry decode rows")
