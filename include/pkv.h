@@ -105,6 +105,23 @@ int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int
                   int head_dim, int dtype, int *dev_status, void *stream);
 
 /*
+ * pkv_copy_blocks -- copy whole cache blocks by index pairs, for preemption by
+ * swap ("Continuous Batching" §5 "Preemption": copy the victim's KV blocks to
+ * CPU memory, later copy them back).  For every i < num_pairs, the
+ * block_bytes bytes of block pairs[2i] of src go to block pairs[2i+1] of dst.
+ *   dst, src   [dst_blocks] / [src_blocks] blocks of block_bytes each, 16-B
+ *              aligned; device memory or pinned host memory (the GPU reads
+ *              and writes the latter directly); one call per cache array
+ *              (a K or a V cache of one layer)
+ *   pairs      device-accessible int32 [num_pairs][2] (source, destination)
+ *   block_bytes  multiple of 16 (Hkv * block_size * head_dim * element size)
+ * An index out of range skips that pair and sets PKV_DEV_BAD_BLOCK_ID.
+ * Destinations must be distinct within a call (else one writer wins).
+ */
+int pkv_copy_blocks(void *dst, int64_t dst_blocks, const void *src, int64_t src_blocks, const int32_t *pairs,
+                    int num_pairs, int64_t block_bytes, int *dev_status, void *stream);
+
+/*
  * Bytes of device workspace pkv_paged_decode_attention should be given on the
  * current device for these head counts and head_dim (independent of the
  * contexts).  The call also accepts less, down to two partial records per
@@ -327,7 +344,24 @@ typedef struct pkv_sched_config {
     const int32_t *initial_order; /* NULL or a permutation of [0, num_blocks) (copied) */
     int policy;                 /* PKV_SCHED_CONTINUOUS (0) or PKV_SCHED_STATIC (1) */
     int prefix_caching;         /* 1: share full prompt pages between requests added with tokens */
+    int preemption;             /* PKV_PREEMPT_RECOMPUTE (0) or PKV_PREEMPT_SWAP (1) */
+    int swap_blocks;            /* host slots for swapped-out blocks (PKV_PREEMPT_SWAP) */
 } pkv_sched_config;
+
+/* Preemption ("Continuous Batching" §5 "Preemption").  Recompute: the
+ * victim's blocks are freed and it is re-prefilled later.  Swap: the blocks
+ * holding its computed tokens are copied to host slots, the device blocks are
+ * freed, and when it is admitted again (it waits at the front of the queue)
+ * fresh device blocks are allocated, the host slots copied back and its
+ * computed length restored -- nothing is recomputed.  A victim whose blocks
+ * do not fit in the free host slots is recomputed instead.  The copies are
+ * the caller's: each step lists them (pkv_step_meta swap_out / swap_in) and
+ * they must run before the step's kernels, all swap-outs before the
+ * swap-ins (a block freed by a swap-out may be refilled by a swap-in of the
+ * same step).  A host slot freed by a swap-in is reused from the next step
+ * on. */
+#define PKV_PREEMPT_RECOMPUTE 0
+#define PKV_PREEMPT_SWAP 1
 
 /* Admission policies.  Continuous: the rules above, every step ("Continuous
  * Batching" §4-5).  Static: the baseline that page's opening section
@@ -355,6 +389,10 @@ typedef struct pkv_step_meta {
     const int32_t *token_pos;     /* [num_tokens] position of every new token in its request */
     int num_finished;             /* requests retired at the end of this step */
     const int64_t *finished_rids; /* [num_finished] their ids, in scheduling order */
+    int num_swap_out;             /* blocks to copy device -> host before this step's kernels */
+    const int32_t *swap_out;      /* [num_swap_out][2]: device block, host slot */
+    int num_swap_in;              /* blocks to copy host -> device, after the swap-outs */
+    const int32_t *swap_in;       /* [num_swap_in][2]: host slot, device block */
 } pkv_step_meta;
 
 typedef struct pkv_sched_stats {
@@ -371,6 +409,9 @@ typedef struct pkv_sched_stats {
     double host_ms;         /* wall time spent inside pkv_sched_step */
     int64_t prefix_hit_blocks; /* blocks taken from the prefix cache at admissions */
     int cached_blocks;      /* pages registered in the prefix cache now */
+    int64_t swapped_out_blocks; /* blocks copied to host slots */
+    int64_t swapped_in_blocks;  /* blocks copied back */
+    int free_swap_slots;    /* host slots free now (including those usable from the next step) */
 } pkv_sched_stats;
 
 /* Prefix caching ("Project 17" Step 8 "Prefix caching"; "Continuous Batching"

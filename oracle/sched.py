@@ -40,6 +40,14 @@ Sources and the reading taken where they differ:
   registered one; a match covers at most prompt_len - 1 tokens, so one prompt
   token is always computed and no request writes into a shared page; a block
   is freed when no request holds it, and leaves the cache then.
+* Preemption by swap ("Continuous Batching" §5 "Preemption", SWAP: copy the
+  victim's KV blocks to CPU memory, free the GPU blocks, copy back later).
+  Readings: only the blocks holding computed tokens are copied, to host slots
+  taken from a stack; a victim they do not fit is recomputed instead; the
+  swapped request keeps its computed length and waits at the front of the
+  queue; when admitted again it gets fresh blocks (no prefix match) and its
+  slots are copied back into the first of them; a slot freed by a swap-in is
+  reused from the next step on (the step's copies run swap-outs first).
 
 Emitted per step: prefill chunks (more than one new token) first, then decode
 sequences (exactly one new token), each group in scheduling order.
@@ -94,6 +102,7 @@ class Request:
     tokens: Optional[list] = None  # prompt token ids (None: no prefix sharing)
     registered: int = 0            # leading prompt pages registered in the prefix cache
     reg_stopped: bool = False
+    slots: List[int] = field(default_factory=list)   # host slots of its swapped-out blocks
     state: str = "waiting"         # waiting | running | finished
     arrival_step: int = 0
     finish_step: int = -1
@@ -116,6 +125,8 @@ class StepMeta:
     token_pos: np.ndarray          # int32 [T]
     num_prefill: int
     finished_rids: np.ndarray = None   # int64: requests retired at the end of this step
+    swap_out: np.ndarray = None        # int32 [n, 2]: device block -> host slot, before the kernels
+    swap_in: np.ndarray = None         # int32 [n, 2]: host slot -> device block, after the swap-outs
 
 
 def cdiv(a: int, b: int) -> int:
@@ -125,9 +136,16 @@ def cdiv(a: int, b: int) -> int:
 class Scheduler:
     def __init__(self, num_blocks: int, block_size: int = 16, max_batch: int = 256,
                  max_num_batched_tokens: int = 8192, chunk: int = 512, max_model_len: int = 8192,
-                 initial_order=None, policy: str = "continuous", prefix_caching: bool = False):
+                 initial_order=None, policy: str = "continuous", prefix_caching: bool = False,
+                 preemption: str = "recompute", swap_blocks: int = 0):
         assert policy in ("continuous", "static")
+        assert preemption in ("recompute", "swap")
         self.policy = policy
+        self.preemption = preemption
+        self.swap_free = list(range(swap_blocks - 1, -1, -1))   # a stack: slot 0 first
+        self.swap_free_next = []
+        self.swap_out_pairs, self.swap_in_pairs = [], []
+        self.swapped_out_blocks = self.swapped_in_blocks = 0
         self.prefix_caching = prefix_caching
         self.cache = {}          # (block of the preceding page or -1, page tokens) -> block
         self.key_of = {}         # block -> its cache key
@@ -213,8 +231,16 @@ class Scheduler:
             r.registered += 1
 
     def _preempt(self, r: Request) -> None:
+        keep = cdiv(r.num_computed, self.bs)        # blocks holding computed tokens
+        if self.preemption == "swap" and 0 < keep <= len(self.swap_free):
+            for k in range(keep):
+                slot = self.swap_free.pop()
+                r.slots.append(slot)
+                self.swap_out_pairs.append((r.blocks[k], slot))
+            self.swapped_out_blocks += keep
+        else:
+            r.num_computed = 0
         self._release(r)
-        r.num_computed = 0
         r.registered = 0
         r.reg_stopped = False
         r.state = "waiting"
@@ -231,6 +257,9 @@ class Scheduler:
 
     def step(self) -> Optional[StepMeta]:
         budget = self.budget
+        self.swap_free.extend(self.swap_free_next)
+        self.swap_free_next = []
+        self.swap_out_pairs, self.swap_in_pairs = [], []
         scheduled = []
         # running requests first, in admission order
         i = 0
@@ -261,7 +290,8 @@ class Scheduler:
         may_admit = not static or not self.running
         while may_admit and self.waiting and len(self.running) < self.max_batch and (static or budget > 0):
             r = self.waiting[0]
-            chain = self.find_prefix_match(r)
+            swapped = bool(r.slots)
+            chain = [] if swapped else self.find_prefix_match(r)
             got = self._alloc(cdiv(r.length, self.bs) - len(chain))
             if got is None:
                 break
@@ -269,8 +299,16 @@ class Scheduler:
             for b in chain:
                 self.refcount[b] += 1
             r.blocks = chain + got
-            r.num_computed = len(chain) * self.bs
-            r.registered = len(chain)
+            if swapped:
+                # the host slots go back into the first blocks
+                self.swap_in_pairs.extend(zip(r.slots, r.blocks))
+                self.swapped_in_blocks += len(r.slots)
+                self.swap_free_next.extend(r.slots)
+                r.slots = []
+                r.registered = 0
+            else:
+                r.num_computed = len(chain) * self.bs
+                r.registered = len(chain)
             r.reg_stopped = False
             self.prefix_hit_blocks += len(chain)
             r.state = "running"
@@ -296,8 +334,12 @@ class Scheduler:
                     self.running.remove(r)
                     self.finished.append(r)
                     done.append(r.rid)
+        if meta is None and (self.swap_out_pairs or self.swap_in_pairs):
+            meta = self._emit([])
         if meta is not None:
             meta.finished_rids = np.array(done, dtype=np.int64)
+            meta.swap_out = np.array(self.swap_out_pairs, dtype=np.int32).reshape(-1, 2)
+            meta.swap_in = np.array(self.swap_in_pairs, dtype=np.int32).reshape(-1, 2)
         self.step_no += 1
         return meta
 
@@ -341,4 +383,7 @@ class Scheduler:
             "sum_running": self.sum_running,
             "prefix_hit_blocks": self.prefix_hit_blocks,
             "cached_blocks": len(self.cache),
+            "swapped_out_blocks": self.swapped_out_blocks,
+            "swapped_in_blocks": self.swapped_in_blocks,
+            "free_swap_slots": len(self.swap_free) + len(self.swap_free_next),
         }

@@ -4,8 +4,9 @@ The work happens in ``libpkv.so`` (CUDA kernels for sm_103a plus a C++ host
 block pool and scheduler); this package only binds it.  Public names mirror
 the C ABI in ``include/pkv.h``.
 """
-from ._binding import (BlockPool, PkvError, Scheduler, decode_workspace_size, kv_append, lib, mixed_split,
+from ._binding import (BlockPool, PkvError, Scheduler, copy_blocks, decode_workspace_size, kv_append, lib,
+                       mixed_split,
                        paged_decode_attention, paged_mixed_attention, paged_prefill_attention)
 
-__all__ = ["BlockPool", "PkvError", "Scheduler", "decode_workspace_size", "kv_append", "lib", "mixed_split",
+__all__ = ["BlockPool", "PkvError", "Scheduler", "copy_blocks", "decode_workspace_size", "kv_append", "lib", "mixed_split",
            "paged_decode_attention", "paged_mixed_attention", "paged_prefill_attention"]

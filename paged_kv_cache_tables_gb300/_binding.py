@@ -39,17 +39,20 @@ class StepMeta(ctypes.Structure):
                 ("cu_seqlens", ctypes.POINTER(ctypes.c_int32)), ("block_tables", ctypes.POINTER(ctypes.c_int32)),
                 ("slot_mapping", ctypes.POINTER(ctypes.c_int64)), ("token_rids", ctypes.POINTER(ctypes.c_int64)),
                 ("token_pos", ctypes.POINTER(ctypes.c_int32)), ("num_finished", ctypes.c_int),
-                ("finished_rids", ctypes.POINTER(ctypes.c_int64))]
+                ("finished_rids", ctypes.POINTER(ctypes.c_int64)), ("num_swap_out", ctypes.c_int),
+                ("swap_out", ctypes.POINTER(ctypes.c_int32)), ("num_swap_in", ctypes.c_int),
+                ("swap_in", ctypes.POINTER(ctypes.c_int32))]
 
 
 class SchedConfig(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int), ("block_size", ctypes.c_int), ("max_batch", ctypes.c_int),
                 ("max_num_batched_tokens", ctypes.c_int), ("chunk", ctypes.c_int), ("max_model_len", ctypes.c_int),
                 ("initial_order", ctypes.POINTER(ctypes.c_int32)), ("policy", ctypes.c_int),
-                ("prefix_caching", ctypes.c_int)]
+                ("prefix_caching", ctypes.c_int), ("preemption", ctypes.c_int), ("swap_blocks", ctypes.c_int)]
 
 
 SCHED_CONTINUOUS, SCHED_STATIC = 0, 1
+PREEMPT_RECOMPUTE, PREEMPT_SWAP = 0, 1
 
 
 class SchedStats(ctypes.Structure):
@@ -57,7 +60,8 @@ class SchedStats(ctypes.Structure):
                 ("finished", ctypes.c_int64), ("sum_running", ctypes.c_int64), ("tokens", ctypes.c_int64),
                 ("prefill_tokens", ctypes.c_int64), ("running", ctypes.c_int), ("waiting", ctypes.c_int),
                 ("free_blocks", ctypes.c_int), ("host_ms", ctypes.c_double), ("prefix_hit_blocks", ctypes.c_int64),
-                ("cached_blocks", ctypes.c_int)]
+                ("cached_blocks", ctypes.c_int), ("swapped_out_blocks", ctypes.c_int64),
+                ("swapped_in_blocks", ctypes.c_int64), ("free_swap_slots", ctypes.c_int)]
 
 
 def lib():
@@ -81,6 +85,7 @@ def lib():
         "pkv_paged_mixed_attention": ([P, P, P, I, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, SZ, P, P, I, P, P],
                                       I),
         "pkv_mixed_split": ([I, P, I, P, I, I, I, I, I], I),
+        "pkv_copy_blocks": ([P, I64, P, I64, P, I, I64, P, P], I),
         "pkv_pool_create": ([I, P], P),
         "pkv_pool_destroy": ([P], None),
         "pkv_pool_alloc": ([P, I, P], I),
@@ -235,6 +240,25 @@ def paged_mixed_attention(out, q, cu_seqlens, num_prefill, max_q_len, k_cache, v
     _check("pkv_paged_mixed_attention", st)
 
 
+def copy_blocks(dst, src, pairs, dev_status=None, stream=None):
+    """pkv_copy_blocks: dst, src [blocks, ...] tensors (CUDA or pinned CPU) with
+    equal block shapes; pairs int32 [n, 2] (source block, destination block),
+    on the device or pinned."""
+    import torch
+    if dst.shape[1:] != src.shape[1:] or dst.dtype != src.dtype:
+        raise ValueError("dst and src must hold blocks of one shape and dtype")
+    for name, t in (("dst", dst), ("src", src), ("pairs", pairs)):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError("%s must be contiguous, on the GPU or pinned" % name)
+    if pairs.dtype != torch.int32 or pairs.dim() != 2 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int32 [n, 2]")
+    block_bytes = dst[0].numel() * dst.element_size()
+    st = lib().pkv_copy_blocks(ctypes.c_void_p(dst.data_ptr()), dst.shape[0], ctypes.c_void_p(src.data_ptr()),
+                               src.shape[0], ctypes.c_void_p(pairs.data_ptr()), pairs.shape[0], block_bytes,
+                               _status_ptr(dev_status), _stream(stream))
+    _check("pkv_copy_blocks", st)
+
+
 def mixed_split(num_sms, cu_seqlens, num_prefill, context_lens, num_q_heads, num_kv_heads, head_dim, elem_bytes=2):
     """pkv_mixed_split on host arrays: the SMs the decode kernel gets."""
     cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
@@ -294,11 +318,12 @@ class Scheduler:
     """pkv_sched_*: the native iteration-level scheduler (host only)."""
 
     def __init__(self, num_blocks, block_size=16, max_batch=256, max_num_batched_tokens=8192, chunk=512,
-                 max_model_len=8192, initial_order=None, policy=SCHED_CONTINUOUS, prefix_caching=False):
+                 max_model_len=8192, initial_order=None, policy=SCHED_CONTINUOUS, prefix_caching=False,
+                 preemption=PREEMPT_RECOMPUTE, swap_blocks=0):
         L = lib()
         self._keep = None
         cfg = SchedConfig(num_blocks, block_size, max_batch, max_num_batched_tokens, chunk, max_model_len, None,
-                          policy, 1 if prefix_caching else 0)
+                          policy, 1 if prefix_caching else 0, preemption, swap_blocks)
         if initial_order is not None:
             self._keep = np.ascontiguousarray(initial_order, dtype=np.int32)
             cfg.initial_order = self._keep.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
@@ -331,13 +356,16 @@ class Scheduler:
         return meta
 
     def step(self):
-        """One step; returns a dict of numpy copies of the metadata, or None."""
+        """One step; returns a dict of numpy copies of the metadata, or None
+        when nothing was scheduled or copied."""
         m = self.step_raw()
-        if m.num_seqs == 0:
+        if m.num_seqs == 0 and m.num_swap_out == 0 and m.num_swap_in == 0:
             return None
         S, T, MB = m.num_seqs, m.num_tokens, m.max_blocks
 
         def arr(ptr, n, dt):
+            if n == 0:   # nothing scheduled (a step that only swapped): the pointers may be null
+                return np.zeros(0, dt)
             return np.ctypeslib.as_array(ptr, shape=(n,)).astype(dt, copy=True)
 
         return {
@@ -348,6 +376,10 @@ class Scheduler:
             "token_pos": arr(m.token_pos, T, np.int32), "num_prefill": m.num_prefill,
             "finished_rids": arr(m.finished_rids, m.num_finished, np.int64) if m.num_finished else
             np.zeros(0, np.int64),
+            "swap_out": arr(m.swap_out, 2 * m.num_swap_out, np.int32).reshape(-1, 2) if m.num_swap_out else
+            np.zeros((0, 2), np.int32),
+            "swap_in": arr(m.swap_in, 2 * m.num_swap_in, np.int32).reshape(-1, 2) if m.num_swap_in else
+            np.zeros((0, 2), np.int32),
         }
 
     def stats(self):

@@ -73,3 +73,50 @@ extern "C" int pkv_kv_append(const void *k, const void *v, const int64_t *slot_m
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
+
+// ---------------------------------------------------------------- block copies
+
+namespace pkv {
+
+// One CTA per (src, dst) pair: copies block_vec 16-byte vectors from block
+// pairs[2i] of src to block pairs[2i+1] of dst (device or pinned host memory:
+// both are addressed directly).
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
+                                                          const int32_t *__restrict__ pairs, int num_pairs,
+                                                          int64_t block_vec, int64_t src_blocks, int64_t dst_blocks,
+                                                          int *dev_status) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    for (int i = blockIdx.x; i < num_pairs; i += gridDim.x) {
+        const int64_t s = __ldg(pairs + 2 * i), d = __ldg(pairs + 2 * i + 1);
+        if (s < 0 || s >= src_blocks || d < 0 || d >= dst_blocks) {
+            if (threadIdx.x == 0) set_status(dev_status, PKV_DEV_BAD_BLOCK_ID);
+            continue;
+        }
+        const uint4 *from = src + s * block_vec;
+        uint4 *to = dst + d * block_vec;
+        for (int64_t v = threadIdx.x; v < block_vec; v += blockDim.x) to[v] = from[v];
+    }
+}
+
+}  // namespace pkv
+
+extern "C" int pkv_copy_blocks(void *dst, int64_t dst_blocks, const void *src, int64_t src_blocks,
+                               const int32_t *pairs, int num_pairs, int64_t block_bytes, int *dev_status,
+                               void *stream) {
+    using namespace pkv;
+    if (num_pairs < 0 || block_bytes <= 0 || dst_blocks <= 0 || src_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (num_pairs == 0) return PKV_OK;
+    if (!dst || !src || !pairs) return PKV_ERR_INVALID_ARG;
+    if (block_bytes % 16 != 0 || !aligned(dst, 16) || !aligned(src, 16) || !aligned(pairs, 4))
+        return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    int rc = current_sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    const int grid = num_pairs < sms * 4 ? num_pairs : sms * 4;
+    cudaError_t e = launch_pdl(copy_blocks_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                               static_cast<uint4 *>(dst), static_cast<const uint4 *>(src), pairs, num_pairs,
+                               (int64_t)(block_bytes / 16), src_blocks, dst_blocks, dev_status);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? PKV_OK : cuda_fail(e);
+}

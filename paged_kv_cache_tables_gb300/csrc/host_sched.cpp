@@ -131,6 +131,7 @@ struct Request {
     std::vector<int32_t> tokens;   // prompt token ids (empty: no prefix sharing)
     int registered = 0;            // leading prompt pages registered in the prefix cache
     bool reg_stopped = false;      // a page of this prompt is held by another block
+    std::vector<int32_t> slots;    // host slots holding its swapped-out blocks, in table order
     int length() const { return prompt_len + generated; }
 };
 
@@ -152,6 +153,9 @@ struct pkv_sched {
     std::unordered_map<std::string, int32_t> cache;
     std::vector<std::string> key_of;
     std::vector<int> ref;
+    // swap space: free host slots (a stack) and slots freed this step, usable
+    // from the next one; the step's copies
+    std::vector<int32_t> swap_free, swap_free_next, swap_out_pairs, swap_in_pairs;
 
     bool caching() const { return cfg.prefix_caching != 0; }
 
@@ -230,8 +234,21 @@ struct pkv_sched {
 
     void preempt(int idx) {
         Request &r = reqs[idx];
+        const int keep = cdiv(r.num_computed, cfg.block_size);   // blocks holding computed tokens
+        if (cfg.preemption == PKV_PREEMPT_SWAP && keep > 0 && keep <= (int)swap_free.size()) {
+            // swap: copy the computed blocks to host slots, keep the progress
+            for (int k = 0; k < keep; ++k) {
+                const int32_t slot = swap_free.back();
+                swap_free.pop_back();
+                r.slots.push_back(slot);
+                swap_out_pairs.push_back(r.blocks[k]);
+                swap_out_pairs.push_back(slot);
+            }
+            stats.swapped_out_blocks += keep;
+        } else {
+            r.num_computed = 0;
+        }
         release_blocks(r.blocks);
-        r.num_computed = 0;
         r.registered = 0;
         r.reg_stopped = false;
         r.state = WAITING;
@@ -295,6 +312,11 @@ void pkv_sched::emit(const std::vector<std::pair<int, int>> &scheduled, pkv_step
 
 int pkv_sched::step(pkv_step_meta *out) {
     const int bs = cfg.block_size;
+    // host slots freed by last step's swap-ins can be reused now
+    swap_free.insert(swap_free.end(), swap_free_next.begin(), swap_free_next.end());
+    swap_free_next.clear();
+    swap_out_pairs.clear();
+    swap_in_pairs.clear();
     int budget = cfg.max_num_batched_tokens;
     std::vector<std::pair<int, int>> scheduled;
     std::vector<int32_t> got;
@@ -334,15 +356,32 @@ int pkv_sched::step(pkv_step_meta *out) {
     while (may_admit && !waiting.empty() && (int)running.size() < cfg.max_batch && (is_static || budget > 0)) {
         const int idx = waiting.front();
         Request &r = reqs[idx];
-        prefix_match(r, chain);
+        const bool swapped = !r.slots.empty();
+        if (swapped)
+            chain.clear();
+        else
+            prefix_match(r, chain);
         got.clear();
         if (!alloc_blocks(cdiv(r.length(), bs) - (int)chain.size(), got)) break;
         waiting.pop_front();
         for (int32_t b : chain) ++ref[b];
         r.blocks = chain;
         r.blocks.insert(r.blocks.end(), got.begin(), got.end());
-        r.num_computed = (int)chain.size() * bs;
-        r.registered = (int)chain.size();
+        if (swapped) {
+            // swap in: the host slots go back to the first blocks; the
+            // computed length is the one it had
+            for (size_t k = 0; k < r.slots.size(); ++k) {
+                swap_in_pairs.push_back(r.slots[k]);
+                swap_in_pairs.push_back(r.blocks[k]);
+            }
+            stats.swapped_in_blocks += (int64_t)r.slots.size();
+            swap_free_next.insert(swap_free_next.end(), r.slots.begin(), r.slots.end());
+            r.slots.clear();
+            r.registered = 0;
+        } else {
+            r.num_computed = (int)chain.size() * bs;
+            r.registered = (int)chain.size();
+        }
         r.reg_stopped = false;
         stats.prefix_hit_blocks += (int64_t)chain.size();
         r.state = RUNNING;
@@ -383,6 +422,10 @@ int pkv_sched::step(pkv_step_meta *out) {
     }
     out->num_finished = (int)finished_rids.size();
     out->finished_rids = finished_rids.data();
+    out->num_swap_out = (int)swap_out_pairs.size() / 2;
+    out->swap_out = swap_out_pairs.data();
+    out->num_swap_in = (int)swap_in_pairs.size() / 2;
+    out->swap_in = swap_in_pairs.data();
     ++stats.steps;
     return (int)scheduled.size();
 }
@@ -392,7 +435,8 @@ extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
     const pkv_sched_config &c = *config;
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.max_batch <= 0 || c.max_num_batched_tokens <= 0 ||
         c.chunk <= 0 || c.max_model_len <= 1 || (c.policy != PKV_SCHED_CONTINUOUS && c.policy != PKV_SCHED_STATIC) ||
-        (c.prefix_caching != 0 && c.prefix_caching != 1))
+        (c.prefix_caching != 0 && c.prefix_caching != 1) ||
+        (c.preemption != PKV_PREEMPT_RECOMPUTE && c.preemption != PKV_PREEMPT_SWAP) || c.swap_blocks < 0)
         return nullptr;
     pkv_sched *s = new (std::nothrow) pkv_sched();
     if (!s) return nullptr;
@@ -405,6 +449,8 @@ extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
     s->max_blocks = cdiv(c.max_model_len, c.block_size);
     s->key_of.assign(c.num_blocks, std::string());
     s->ref.assign(c.num_blocks, 0);
+    // host slots popped from the end: slot 0 first
+    for (int i = c.swap_blocks - 1; i >= 0; --i) s->swap_free.push_back(i);
     return s;
 }
 
@@ -452,6 +498,7 @@ extern "C" int pkv_sched_get_stats(const pkv_sched *sched, pkv_sched_stats *out)
     out->waiting = (int)sched->waiting.size();
     out->free_blocks = (int)sched->pool.free_list.size();
     out->cached_blocks = (int)sched->cache.size();
+    out->free_swap_slots = (int)(sched->swap_free.size() + sched->swap_free_next.size());
     return PKV_OK;
 }
 

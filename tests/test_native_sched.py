@@ -8,7 +8,7 @@ import pytest
 import sched_golden
 from oracle.sched import Scheduler as PyScheduler
 from paged_kv_cache_tables_gb300 import BlockPool, PkvError, Scheduler
-from paged_kv_cache_tables_gb300._binding import SCHED_CONTINUOUS, SCHED_STATIC
+from paged_kv_cache_tables_gb300._binding import PREEMPT_RECOMPUTE, PREEMPT_SWAP, SCHED_CONTINUOUS, SCHED_STATIC
 
 
 class _Adapter:
@@ -46,12 +46,16 @@ def test_native_scheduler_reproduces_hand_worked_trace(path):
                     max_num_batched_tokens=c["budget"], chunk=c["chunk"], max_model_len=c["max_model_len"]), path)
 
 
-def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fail_every=0, policy="continuous"):
+def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fail_every=0, policy="continuous",
+             swap_blocks=0):
     rng = np.random.default_rng(seed)
     order = rng.permutation(NB)
-    py = PyScheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order, policy=policy)
+    mode = "swap" if swap_blocks else "recompute"
+    py = PyScheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order, policy=policy, preemption=mode,
+                     swap_blocks=swap_blocks)
     nat = Scheduler(NB, 16, max_batch, budget, chunk, mml, initial_order=order,
-                    policy={"continuous": SCHED_CONTINUOUS, "static": SCHED_STATIC}[policy])
+                    policy={"continuous": SCHED_CONTINUOUS, "static": SCHED_STATIC}[policy],
+                    preemption=PREEMPT_SWAP if swap_blocks else PREEMPT_RECOMPUTE, swap_blocks=swap_blocks)
     arrivals = sorted((int(rng.integers(0, 60)), rid, int(rng.integers(1, 200)), int(rng.integers(1, 120)),
                        int(rng.geometric(1 / 30))) for rid in range(n))
     i = 0
@@ -73,8 +77,10 @@ def run_both(seed, n=80, NB=96, max_batch=12, budget=160, chunk=48, mml=320, fai
                 assert np.array_equal(getattr(a, k), b[k]), "step %d field %s" % (step, k)
             assert a.num_prefill == b["num_prefill"]
             assert np.array_equal(a.finished_rids, b["finished_rids"]), "step %d finished" % step
+            assert np.array_equal(a.swap_out, b["swap_out"]) and np.array_equal(a.swap_in, b["swap_in"]), step
         sa, sb = py.stats(), nat.stats()
-        for k in ["free_blocks", "running", "waiting", "finished", "preemptions", "sum_running"]:
+        for k in ["free_blocks", "running", "waiting", "finished", "preemptions", "sum_running",
+                  "swapped_out_blocks", "swapped_in_blocks", "free_swap_slots"]:
             assert sa[k] == sb[k], "step %d stat %s" % (step, k)
         if i == len(arrivals) and py.idle():
             break
@@ -93,16 +99,18 @@ def test_native_matches_python_under_memory_pressure_and_injected_failures(seed)
     assert py.n_preemptions > 0
 
 
-def run_both_prefix(seed, NB=140, fail_every=0, policy="continuous"):
+def run_both_prefix(seed, NB=140, fail_every=0, policy="continuous", swap_blocks=0):
     """Native vs Python with prefix caching on a trace of requests from a few
     groups sharing page-aligned prompt heads (some prompts are a head alone)."""
     from test_sched_oracle import shared_prefix_trace
     rng = np.random.default_rng(seed)
     trace = shared_prefix_trace(rng, 70)
     order = rng.permutation(NB)
-    py = PyScheduler(NB, 16, 10, 160, 48, 320, initial_order=order, policy=policy, prefix_caching=True)
+    py = PyScheduler(NB, 16, 10, 160, 48, 320, initial_order=order, policy=policy, prefix_caching=True,
+                     preemption="swap" if swap_blocks else "recompute", swap_blocks=swap_blocks)
     nat = Scheduler(NB, 16, 10, 160, 48, 320, initial_order=order, prefix_caching=True,
-                    policy={"continuous": SCHED_CONTINUOUS, "static": SCHED_STATIC}[policy])
+                    policy={"continuous": SCHED_CONTINUOUS, "static": SCHED_STATIC}[policy],
+                    preemption=PREEMPT_SWAP if swap_blocks else PREEMPT_RECOMPUTE, swap_blocks=swap_blocks)
     i = 0
     for step in range(5000):
         while i < len(trace) and trace[i][0] <= step:
@@ -121,9 +129,10 @@ def run_both_prefix(seed, NB=140, fail_every=0, policy="continuous"):
                       "token_rids", "token_pos"]:
                 assert np.array_equal(getattr(a, k), b[k]), "step %d field %s" % (step, k)
             assert np.array_equal(a.finished_rids, b["finished_rids"]), "step %d finished" % step
+            assert np.array_equal(a.swap_out, b["swap_out"]) and np.array_equal(a.swap_in, b["swap_in"]), step
         sa, sb = py.stats(), nat.stats()
         for k in ["free_blocks", "running", "waiting", "finished", "preemptions", "prefix_hit_blocks",
-                  "cached_blocks"]:
+                  "cached_blocks", "swapped_out_blocks", "swapped_in_blocks", "free_swap_slots"]:
             assert sa[k] == sb[k], "step %d stat %s: %s vs %s" % (step, k, sa[k], sb[k])
         if i == len(trace) and py.idle():
             break
@@ -142,6 +151,16 @@ def test_native_prefix_cache_matches_python_under_pressure(seed):
     py = run_both_prefix(500 + seed, NB=50, fail_every=7)
     assert py.n_preemptions > 0 and py.prefix_hit_blocks > 0
     run_both_prefix(600 + seed, NB=60, policy="static")
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_native_swap_preemption_matches_python(seed):
+    py = run_both(700 + seed, NB=40, swap_blocks=30)
+    assert py.swapped_out_blocks > 0
+    py = run_both(710 + seed, NB=40, fail_every=7, swap_blocks=12)    # slots run out: some recompute
+    assert py.swapped_out_blocks > 0
+    py = run_both_prefix(720 + seed, NB=50, fail_every=5, swap_blocks=20)
+    assert py.n_preemptions > 0
 
 
 def test_native_add_tokens_checks_length():

@@ -326,3 +326,79 @@ def test_prefix_cache_invariants(seed):
         runs[caching] = ({r.rid: r.generated for r in s.finished}, prefill, s.prefix_hit_blocks)
     assert runs[True][0] == runs[False][0]
     assert runs[True][2] > 0 and runs[True][1] < runs[False][1]
+
+
+def _swap_trace(preemption):
+    s = Scheduler(6, 4, max_batch=4, max_num_batched_tokens=100, chunk=100, max_model_len=64,
+                  preemption=preemption, swap_blocks=10)
+    s.add(0, 7, 20, 10)
+    s.add(1, 8, 20, 10)
+    return s, [s.step() for _ in range(11)]
+
+
+def test_swap_preemption_hand_worked_trace():
+    """Block size 4, pool [0..5] popped from the end, host slots 0..9 (slot 0
+    first).  A (prompt 7, EOS after 10) gets blocks 5, 4; B (prompt 8) gets 3, 2;
+    B grows into 1 at step 1, A into 0 at step 2.  At step 5 B (context 12)
+    needs a fourth block, none is free: B is the newest, so it preempts itself
+    and is swapped out -- its three computed blocks 3, 2, 1 to slots 0, 1, 2 --
+    keeping its 12 computed tokens; A takes block 1 at step 6 and retires after
+    step 9.  At step 10 B comes back into blocks 1, 0, 4, 5: slots 0, 1, 2 are
+    copied into 1, 0, 4 and it decodes position 12 (slot 5 * 4 + 0 = 20), where
+    recompute would re-prefill all 13 tokens."""
+    s, m = _swap_trace("swap")
+    assert m[5].seq_rids.tolist() == [0]
+    assert m[5].swap_out.tolist() == [[3, 0], [2, 1], [1, 2]] and len(m[5].swap_in) == 0
+    assert m[6].block_tables[0, :4].tolist() == [5, 4, 0, 1]
+    assert m[9].finished_rids.tolist() == [0]
+    assert m[10].swap_in.tolist() == [[0, 1], [1, 0], [2, 4]]
+    assert m[10].seq_rids.tolist() == [1] and m[10].q_lens.tolist() == [1]
+    assert m[10].context_lens.tolist() == [13] and m[10].slot_mapping.tolist() == [20]
+    assert m[10].block_tables[0, :4].tolist() == [1, 0, 4, 5]
+    st = s.stats()
+    assert st["swapped_out_blocks"] == 3 and st["swapped_in_blocks"] == 3 and st["free_swap_slots"] == 10
+    _, r = _swap_trace("recompute")
+    assert len(r[5].swap_out) == 0
+    assert r[10].q_lens.tolist() == [13] and r[10].context_lens.tolist() == [13]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_swap_preemption_invariants(seed):
+    """Under memory pressure with swapping: host slots and device blocks are
+    never lost (free + held = pool, free slots + slots held = capacity), a
+    swapped request resumes with the length it had (its only prefill chunk
+    after a swap-in starts where it stopped), every request emits the tokens it
+    would emit with recompute, and less is recomputed."""
+    rng = np.random.default_rng(seed)
+    arrivals = sorted((int(rng.integers(0, 40)), rid, int(rng.integers(1, 120)), int(rng.integers(1, 80)),
+                       int(rng.geometric(1 / 30))) for rid in range(50))
+    runs = {}
+    for mode in ("recompute", "swap"):
+        s = Scheduler(40, 16, max_batch=12, max_num_batched_tokens=160, chunk=48, max_model_len=256,
+                      preemption=mode, swap_blocks=24)
+        i, prefill = 0, 0
+        for step in range(5000):
+            while i < len(arrivals) and arrivals[i][0] <= step:
+                _, rid, p, mt, eos = arrivals[i]
+                s.add(rid, p, mt, eos)
+                i += 1
+            before = {r.rid: r.num_computed for r in s.waiting if r.slots}
+            m = s.step()
+            if m is not None:
+                prefill += int(m.q_lens[m.q_lens > 1].sum())
+                for row, slot in m.swap_in:
+                    assert 0 <= row < 24
+                for rid, q, c in zip(m.seq_rids, m.q_lens, m.context_lens):
+                    if int(rid) in before and not any(r.rid == rid and r.slots for r in s.waiting):
+                        assert int(c) - int(q) == before[int(rid)], "resumed at the wrong length"
+            held_slots = sum(len(r.slots) for r in s.waiting)
+            assert held_slots + s.stats()["free_swap_slots"] == 24
+            held = set(b for r in s.running for b in r.blocks)
+            assert len(held) + s.pool.free_count() == 40
+            if i == len(arrivals) and s.idle():
+                break
+        assert s.idle() and s.pool.free_count() == 40 and s.stats()["free_swap_slots"] == 24
+        runs[mode] = ({r.rid: r.generated for r in s.finished}, prefill, s.stats())
+    assert runs["swap"][0] == runs["recompute"][0]
+    assert runs["swap"][2]["swapped_out_blocks"] > 0
+    assert runs["swap"][1] < runs["recompute"][1]
