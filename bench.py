@@ -420,7 +420,7 @@ def run_mixed(args):
     }
 
 
-def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=False, caching=False):
+def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=False, caching=False, swap_blocks=0):
     """The continuous-batching trace: n requests, Poisson(20) arrivals per
     step, prompts lognormal (mean 512, sigma 1, clipped 8..4096), outputs
     geometric (or lognormal) with mean 256, max batch 256, 8192-token budget,
@@ -444,7 +444,9 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=Fal
         arrival, prompt, eos = make_requests(seed, n=n, outputs=outputs)
     pol = {"continuous": _binding.SCHED_CONTINUOUS, "static": _binding.SCHED_STATIC}[policy]
     eng = PagedEngine(NB, num_layers=L, num_caches=R, initial_order=np.random.default_rng(seed).permutation(NB),
-                      policy=pol, prefix_caching=caching, row_keys=row_keys)
+                      policy=pol, prefix_caching=caching, row_keys=row_keys,
+                      preemption=_binding.PREEMPT_SWAP if swap_blocks else _binding.PREEMPT_RECOMPUTE,
+                      swap_blocks=swap_blocks)
     rng = np.random.default_rng(seed + 1)
     clk = ClockSampler(0)
     with clk:
@@ -525,6 +527,8 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=Fal
         "latency_steps_p50": float(np.percentile(lat, 50)), "latency_steps_p99": float(np.percentile(lat, 99)),
         "ttft_steps_mean": round(float(ttft_steps.mean()), 2), "ttft_ms_mean": round(float(ttft_ms.mean()), 3),
         "prefill_tokens": st["prefill_tokens"], "prefix_hit_blocks": st["prefix_hit_blocks"],
+        "swapped_out_blocks": st["swapped_out_blocks"], "swapped_in_blocks": st["swapped_in_blocks"],
+        "swap_bytes": int(eng.swap_bytes),
         "upload_bytes_per_step": int(eng.upload_bytes / max(1, len(steps))),
         "oracle_check": {"rows": checked, "max_abs_err": worst, "every": "50th engine step, layer 0",
                          "oracle_s": round(t_or, 2), "oracle_keys_per_s": round(keys / max(t_or, 1e-9), 1)},
@@ -557,6 +561,82 @@ def run_prefix_bench(args):
         "throughput_ratio": round(on["output_tokens_per_s"] / off["output_tokens_per_s"], 3),
         "prefill_token_ratio": round(off["prefill_tokens"] / max(1, on["prefill_tokens"]), 3),
         "ttft_ratio_no_cache_over_cache": round(off["ttft_ms_mean"] / on["ttft_ms_mean"], 3),
+    }))
+
+
+def swap_copy_rates(NB=8192, n=4096, reps=5):
+    """Device <-> pinned host block copies of the 8B shape (32 KB per block and
+    cache array) through pkv_copy_blocks: GB/s each way, CUDA events."""
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    cache = torch.empty((NB, 8, 16, 128), dtype=torch.bfloat16, device="cuda").normal_()
+    host = torch.empty((n, 8, 16, 128), dtype=torch.bfloat16).pin_memory()
+    rng = np.random.default_rng(1)
+    pairs_out = torch.from_numpy(np.stack([rng.choice(NB, n, replace=False), rng.permutation(n)], 1)
+                                 .astype(np.int32)).cuda()
+    pairs_in = torch.from_numpy(np.stack([rng.permutation(n), rng.choice(NB, n, replace=False)], 1)
+                                .astype(np.int32)).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    nbytes = n * cache[0].numel() * 2
+    res = {}
+    for name, fn in (("device_to_host", lambda: pkv.copy_blocks(host, cache, pairs_out, dev_status=status)),
+                     ("host_to_device", lambda: pkv.copy_blocks(cache, host, pairs_in, dev_status=status))):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the swap copies" % int(status.item()))
+    res["bytes_per_call"] = nbytes
+    # the copy engines on one contiguous buffer of the same size: the bound
+    # for the gather above
+    flat_d, flat_h = cache[:n].view(-1), host.view(-1)
+    for name, (dst, src) in (("memcpy_device_to_host", (flat_h, flat_d)), ("memcpy_host_to_device", (flat_d, flat_h))):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    return res
+
+
+def run_preempt_bench(args):
+    """Preemption by recompute against preemption by swap on the trace with a
+    pool small enough to preempt: the same requests, engine and kernels; only
+    what happens to a victim's blocks differs (freed and recomputed, or copied
+    to pinned host memory and back)."""
+    import torch
+    if args.copy_rates_only:
+        torch.cuda.set_device(0)
+        print(json.dumps({"swap_copy_gbs": swap_copy_rates()}))
+        return
+    NB = args.trace_pool if args.trace_pool != 200000 else 6250
+    swap = args.swap_blocks or 2 * NB
+    n = args.trace_requests
+    rec = trace_line(args, n, NB)
+    sw = trace_line(args, n, NB, swap_blocks=swap)
+    torch.cuda.synchronize()
+    rates = swap_copy_rates() if not args.no_copy_rates else None
+    keep = ["engine_steps", "wall_s", "output_tokens", "output_tokens_per_s", "prefill_tokens", "preemptions",
+            "swapped_out_blocks", "swapped_in_blocks", "swap_bytes", "avg_running_batch", "ttft_ms_mean",
+            "latency_steps_p50", "latency_steps_p99", "oracle_check", "clocks"]
+    print(json.dumps({
+        "metric": "preemption by recompute vs by swap: output tokens/s, prefill tokens and swapped bytes",
+        "workload": "%d requests as in the trace, pool %d blocks, %d layers (8B shape) over %d caches; swap space "
+                    "%d blocks per cache array in pinned host memory" % (n, NB, args.trace_layers,
+                                                                        args.trace_caches, swap),
+        "recompute": {k: rec[k] for k in keep}, "swap": {k: sw[k] for k in keep},
+        "throughput_ratio_swap_over_recompute": round(sw["output_tokens_per_s"] / rec["output_tokens_per_s"], 3),
+        "swap_copy_gbs": rates,
     }))
 
 
@@ -704,9 +784,13 @@ def main():
     ap.add_argument("--mixed-prior", type=int, default=-1,
                     help="give every prefill chunk this prior context instead of U{0..4096} (profiling)")
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching", "prefix"],
+    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching", "prefix", "preempt"],
                     help="trace: the continuous-batching trace; batching: static vs continuous on one trace; "
-                         "prefix: with and without the prefix cache on a sharing-heavy trace")
+                         "prefix: with and without the prefix cache on a sharing-heavy trace; preempt: recompute "
+                         "vs swap on the trace with a small pool")
+    ap.add_argument("--swap-blocks", type=int, default=0, help="host swap slots for --workload preempt")
+    ap.add_argument("--copy-rates-only", action="store_true", help="--workload preempt: only the block copy rates")
+    ap.add_argument("--no-copy-rates", action="store_true")
     ap.add_argument("--trace-requests", type=int, default=1000)
     ap.add_argument("--trace-layers", type=int, default=32)
     ap.add_argument("--trace-caches", type=int, default=4)
@@ -724,6 +808,9 @@ def main():
         return
     if args.workload == "prefix":
         run_prefix_bench(args)
+        return
+    if args.workload == "preempt":
+        run_preempt_bench(args)
         return
     if args.only_mixed:
         import torch

@@ -91,6 +91,14 @@ def append(k, v, slot_mapping, k_cache, v_cache, block_size: int) -> int:
     return int(n)
 
 
+def copy_blocks(src, dst, pairs) -> None:
+    """Preemption by swap ("Continuous Batching" §5 "Preemption"): block
+    pairs[i][0] of src is copied whole into block pairs[i][1] of dst, in
+    order (a block is [Hkv][block_size][d] of one cache)."""
+    for s, d in np.asarray(pairs).reshape(-1, 2):
+        dst[int(d)] = src[int(s)]
+
+
 def decode(q, k_cache, v_cache, block_tables, context_lens, dtype: str, scale=None) -> np.ndarray:
     """Paged decode attention; q [S, Hq, d] bits, caches [NB, Hkv, bs, d] bits,
     block_tables [S, max_blocks] int32, context_lens [S] int32 -> float64 [S, Hq, d]."""

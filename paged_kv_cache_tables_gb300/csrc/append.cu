@@ -78,9 +78,13 @@ extern "C" int pkv_kv_append(const void *k, const void *v, const int64_t *slot_m
 
 namespace pkv {
 
+constexpr int kCopyUnroll = 8;
+
 // One CTA per (src, dst) pair: copies block_vec 16-byte vectors from block
 // pairs[2i] of src to block pairs[2i+1] of dst (device or pinned host memory:
-// both are addressed directly).
+// both are addressed directly).  Each thread issues kCopyUnroll loads before
+// its stores, so that enough bytes are in flight to cover the latency of the
+// host link.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ dst, const uint4 *__restrict__ src,
                                                           const int32_t *__restrict__ pairs, int num_pairs,
                                                           int64_t block_vec, int64_t src_blocks, int64_t dst_blocks,
@@ -95,7 +99,19 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ ds
         }
         const uint4 *from = src + s * block_vec;
         uint4 *to = dst + d * block_vec;
-        for (int64_t v = threadIdx.x; v < block_vec; v += blockDim.x) to[v] = from[v];
+        for (int64_t v0 = threadIdx.x; v0 < block_vec; v0 += (int64_t)blockDim.x * kCopyUnroll) {
+            uint4 r[kCopyUnroll];
+#pragma unroll
+            for (int j = 0; j < kCopyUnroll; ++j) {
+                const int64_t v = v0 + (int64_t)j * blockDim.x;
+                if (v < block_vec) r[j] = from[v];
+            }
+#pragma unroll
+            for (int j = 0; j < kCopyUnroll; ++j) {
+                const int64_t v = v0 + (int64_t)j * blockDim.x;
+                if (v < block_vec) to[v] = r[j];
+            }
+        }
     }
 }
 

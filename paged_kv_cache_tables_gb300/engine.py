@@ -13,6 +13,12 @@ layer and re-uploads all of them every layer; here the step's metadata goes
 up once).  `num_caches` physical K/V caches are rotated over the layers
 (layer l uses cache l % num_caches) so that a many-layer trace fits in HBM;
 every layer still streams its own full context.
+
+With preemption by swap ("Continuous Batching" §5 "Preemption") each
+physical K and V cache has a pinned host mirror of `swap_blocks` blocks; the
+scheduler names, per step, which device blocks go out to which host slots and
+which come back, and the step runs those copies (one pkv_copy_blocks launch
+per cache array and direction, out before in) ahead of its layers.
 """
 import ctypes
 import time
@@ -25,7 +31,8 @@ from . import _binding as B
 class PagedEngine:
     def __init__(self, num_blocks, num_layers=32, num_caches=4, Hq=32, Hkv=8, d=128, dtype="bf16",
                  max_batch=256, max_num_batched_tokens=8192, chunk=512, max_model_len=8192, initial_order=None,
-                 device="cuda", policy=B.SCHED_CONTINUOUS, prefix_caching=False, row_keys=None):
+                 device="cuda", policy=B.SCHED_CONTINUOUS, prefix_caching=False, row_keys=None,
+                 preemption=B.PREEMPT_RECOMPUTE, swap_blocks=0):
         import torch
         self.torch = torch
         self.L, self.R = num_layers, num_caches
@@ -33,7 +40,8 @@ class PagedEngine:
         self.NB = num_blocks
         self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
         self.sched = B.Scheduler(num_blocks, 16, max_batch, max_num_batched_tokens, chunk, max_model_len,
-                                 initial_order=initial_order, policy=policy, prefix_caching=prefix_caching)
+                                 initial_order=initial_order, policy=policy, prefix_caching=prefix_caching,
+                                 preemption=preemption, swap_blocks=swap_blocks)
         # row_keys(token_rids, token_pos) -> int64 keys handed to `fill` in
         # place of the request ids (a caller whose rows depend on content)
         self.row_keys = row_keys
@@ -44,6 +52,15 @@ class PagedEngine:
         shape = (num_blocks, Hkv, 16, d)
         self.k_cache = [torch.zeros(shape, dtype=self.tdt, device=dev) for _ in range(num_caches)]
         self.v_cache = [torch.zeros(shape, dtype=self.tdt, device=dev) for _ in range(num_caches)]
+        # host mirrors of the caches for swapped-out blocks (the GPU reads and
+        # writes pinned memory directly)
+        self.swap_blocks = swap_blocks if preemption == B.PREEMPT_SWAP else 0
+        hshape = (self.swap_blocks,) + shape[1:]
+        self.k_swap = [torch.empty(hshape, dtype=self.tdt).pin_memory() for _ in range(num_caches)] \
+            if self.swap_blocks else []
+        self.v_swap = [torch.empty(hshape, dtype=self.tdt).pin_memory() for _ in range(num_caches)] \
+            if self.swap_blocks else []
+        self.swap_bytes = 0
         T, S = self.max_T, self.max_S
         self.q = torch.empty((T, Hq, d), dtype=self.tdt, device=dev)
         self.k = torch.empty((T, Hkv, d), dtype=self.tdt, device=dev)
@@ -53,7 +70,7 @@ class PagedEngine:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         # one pinned staging area and one device area for the step's metadata
         self.n_i64 = 3 * T                       # slot_mapping, token_rids, (spare)
-        self.n_i32 = T + 2 * S + 1 + S * self.max_blocks
+        self.n_i32 = T + 2 * S + 1 + S * self.max_blocks + 4 * self.swap_blocks   # + swap pairs
         # two pinned staging areas used alternately: the host may only rewrite
         # one after the device has finished copying it (the GPU can be a step
         # behind the host)
@@ -71,6 +88,29 @@ class PagedEngine:
     def add(self, rid, prompt_len, max_tokens, eos_after, tokens=None):
         self.sched.add(rid, prompt_len, max_tokens, eos_after, tokens=tokens)
 
+    def _swap(self, o, n_out, n_in):
+        """The step's block copies: device -> host slots for preempted
+        sequences, then host slots -> device for re-admitted ones (a block
+        swapped out may be the destination of a swap-in of the same step)."""
+        L = B.lib()
+        blk = self.k_cache[0][0].numel() * self.k_cache[0].element_size()
+        pst, pstream = self.status.data_ptr(), self.stream.cuda_stream
+        pairs_out = self.d_i32.data_ptr() + o * 4
+        pairs_in = pairs_out + 2 * n_out * 4
+        for dev, host in zip(self.k_cache + self.v_cache, self.k_swap + self.v_swap):
+            if n_out:
+                rc = L.pkv_copy_blocks(host.data_ptr(), self.swap_blocks, dev.data_ptr(), self.NB, pairs_out, n_out,
+                                       blk, pst, pstream)
+                if rc != B.PKV_OK:
+                    raise B.PkvError("swap out", rc)
+        for dev, host in zip(self.k_cache + self.v_cache, self.k_swap + self.v_swap):
+            if n_in:
+                rc = L.pkv_copy_blocks(dev.data_ptr(), self.NB, host.data_ptr(), self.swap_blocks, pairs_in, n_in,
+                                       blk, pst, pstream)
+                if rc != B.PKV_OK:
+                    raise B.PkvError("swap in", rc)
+        self.swap_bytes += (n_out + n_in) * blk * 2 * self.R
+
     def step(self, fill, on_layer_done=None):
         """One engine step.  Returns None when nothing was scheduled, else a
         dict with the step's metadata (numpy) and device views."""
@@ -78,12 +118,14 @@ class PagedEngine:
         t0 = time.perf_counter()
         m = self.sched.step_raw()
         S, T, P = m.num_seqs, m.num_tokens, m.num_prefill
-        if S == 0:
+        n_out, n_in = m.num_swap_out, m.num_swap_in
+        arr = lambda ptr, n: np.ctypeslib.as_array(ptr, shape=(n,)) if n else np.zeros(0, np.int64)
+        if S == 0 and not (n_out or n_in):
             self.host_ms += (time.perf_counter() - t0) * 1e3
             return None
         MB = m.max_blocks
-        arr = lambda ptr, n: np.ctypeslib.as_array(ptr, shape=(n,))
-        # stage: i64 = [slot_mapping T][token_rids T]; i32 = [token_pos T][ctx S][cu S+1][tables S*MB]
+        # stage: i64 = [slot_mapping T][token_rids T];
+        #        i32 = [token_pos T][ctx S][cu S+1][tables S*MB][swap_out 2*n_out][swap_in 2*n_in]
         buf = self.nstep & 1
         self.nstep += 1
         tw = time.perf_counter()
@@ -95,15 +137,26 @@ class PagedEngine:
         h64[T:2 * T] = (arr(m.token_rids, T) if self.row_keys is None
                         else self.row_keys(arr(m.token_rids, T), arr(m.token_pos, T)))
         o = 0
-        h32[o:o + T] = arr(m.token_pos, T); o += T
-        h32[o:o + S] = arr(m.context_lens, S); o += S
-        h32[o:o + S + 1] = arr(m.cu_seqlens, S + 1); o += S + 1
-        h32[o:o + S * MB] = arr(m.block_tables, S * MB); o += S * MB
+        if S:
+            h32[o:o + T] = arr(m.token_pos, T); o += T
+            h32[o:o + S] = arr(m.context_lens, S); o += S
+            h32[o:o + S + 1] = arr(m.cu_seqlens, S + 1); o += S + 1
+            h32[o:o + S * MB] = arr(m.block_tables, S * MB); o += S * MB
+        o_swap = o
+        h32[o:o + 2 * n_out] = arr(m.swap_out, 2 * n_out); o += 2 * n_out
+        h32[o:o + 2 * n_in] = arr(m.swap_in, 2 * n_in); o += 2 * n_in
         n32 = o
         self.d_i64[:2 * T].copy_(self.h_i64[buf][:2 * T], non_blocking=True)
         self.d_i32[:n32].copy_(self.h_i32[buf][:n32], non_blocking=True)
         self.copied[buf].record(self.stream)
         self.upload_bytes += 2 * T * 8 + n32 * 4
+        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        ev[0].record(self.stream)
+        if n_out or n_in:
+            self._swap(o_swap, n_out, n_in)
+        if S == 0:
+            self.host_ms += (time.perf_counter() - t0) * 1e3 - waited
+            return None
         slots, trids = self.d_i64[:T], self.d_i64[T:2 * T]
         o = 0
         tpos = self.d_i32[o:o + T]; o += T
@@ -137,8 +190,6 @@ class PagedEngine:
         vc = [t.data_ptr() for t in self.v_cache]
         NB, Hq, Hkv, d = self.NB, self.Hq, self.Hkv, self.d
         self.host_ms += (time.perf_counter() - t0) * 1e3 - waited
-        ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        ev[0].record(self.stream)
         for layer in range(self.L):
             cid = layer % self.R
             fill(layer, cid, q, k, v, trids, tpos)

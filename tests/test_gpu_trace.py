@@ -2,7 +2,8 @@
 chunked prefill and decode over several layers for a request trace; sampled
 layer-0 attention rows are checked against the FP64 oracle on K/V rebuilt from
 the counter-based generator (so the check covers the scheduler's tables and
-slots, every append, preemption by recompute and both attention kernels)."""
+slots, every append, preemption by recompute or by swap and both attention
+kernels)."""
 import numpy as np
 import pytest
 import torch
@@ -35,12 +36,12 @@ def test_gpu_generator_matches_numpy(cuda_lib, synth_gpu):
         assert np.array_equal(got, ref)
 
 
-def run(n, rate, prompt_mean, out_mean, NB, layers, caches, max_batch, budget, chunk, mml, seed):
+def run(n, rate, prompt_mean, out_mean, NB, layers, caches, max_batch, budget, chunk, mml, seed, **kw):
     arrival, prompt, eos = make_requests(seed, n=n, rate=rate, prompt_mean=prompt_mean, out_mean=out_mean,
                                          pmax=mml // 2)
     eng = PagedEngine(NB, num_layers=layers, num_caches=caches, Hq=HQ, Hkv=HKV, d=D, max_batch=max_batch,
                       max_num_batched_tokens=budget, chunk=chunk, max_model_len=mml,
-                      initial_order=np.random.default_rng(seed).permutation(NB))
+                      initial_order=np.random.default_rng(seed).permutation(NB), **kw)
     rng = np.random.default_rng(seed + 1)
     res = run_trace(eng, arrival, prompt, eos, max_tokens=mml, fill=make_fill(), sample_every=4,
                     pick=lambda info: pick_rows(info, rng))
@@ -76,6 +77,37 @@ def test_trace_under_memory_pressure_preempts_and_recomputes_exactly(cuda_lib, s
     assert st["preemptions"] > 0
     assert st["free_blocks"] == 96
     assert int(eng.status.item()) == 0
+    assert check_samples(res) >= 10
+
+
+def test_trace_under_memory_pressure_swaps_blocks_out_and_back(cuda_lib, synth_gpu):
+    """Preemption by swap: the victims' blocks go to pinned host memory and
+    come back into other physical blocks on re-admission; every sampled row
+    read through the restored blocks equals the oracle, and the prompts are
+    prefilled fewer times than with recompute."""
+    from paged_kv_cache_tables_gb300 import PREEMPT_SWAP
+    cfg = dict(n=40, rate=8, prompt_mean=150, out_mean=40, NB=96, layers=2, caches=2, max_batch=16, budget=512,
+               chunk=128, mml=512, seed=9)
+    eng, res, _ = run(**cfg, preemption=PREEMPT_SWAP, swap_blocks=400)
+    st = eng.sched.stats()
+    assert len(res["finish_step"]) == 40 and int(eng.status.item()) == 0
+    assert st["preemptions"] > 0 and st["swapped_out_blocks"] > 0
+    assert st["swapped_in_blocks"] == st["swapped_out_blocks"]
+    assert st["free_blocks"] == 96 and st["free_swap_slots"] == 400
+    assert check_samples(res) >= 10
+    rec, _, _ = run(**cfg)
+    assert st["prefill_tokens"] < rec.sched.stats()["prefill_tokens"]
+
+
+def test_trace_with_small_swap_space_mixes_swap_and_recompute(cuda_lib, synth_gpu):
+    """With fewer host slots than the victims need, some preemptions fall back
+    to recompute; the outputs stay exact either way."""
+    from paged_kv_cache_tables_gb300 import PREEMPT_SWAP
+    eng, res, _ = run(n=40, rate=8, prompt_mean=150, out_mean=40, NB=96, layers=2, caches=2, max_batch=16,
+                      budget=512, chunk=128, mml=512, seed=11, preemption=PREEMPT_SWAP, swap_blocks=12)
+    st = eng.sched.stats()
+    assert len(res["finish_step"]) == 40 and int(eng.status.item()) == 0
+    assert st["swapped_out_blocks"] > 0 and st["free_swap_slots"] == 12 and st["free_blocks"] == 96
     assert check_samples(res) >= 10
 
 

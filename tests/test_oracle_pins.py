@@ -135,6 +135,34 @@ def test_block_permutation_invariance():
     assert np.array_equal(out, ref)
 
 
+def test_copy_blocks_hand_worked_and_swap_round_trip_keeps_attention():
+    # hand-worked: three 1-element blocks, pairs applied in order
+    src = np.array([[10], [11], [12]], np.uint16)
+    dst = np.zeros((4, 1), np.uint16)
+    oracle.copy_blocks(src, dst, [[2, 0], [0, 3], [2, 1]])
+    assert dst[:, 0].tolist() == [12, 12, 0, 10]
+    # swap every sequence's blocks out to a host pool, back into fresh ids:
+    # attention through the rewritten tables is unchanged
+    st = make_step("llama1b", S=6)
+    ctx = st.context_lens - 1
+    ref = oracle.decode(st.q, st.k_cache, st.v_cache, st.block_tables, ctx, st.dtype)
+    used = np.unique(st.block_tables[st.block_tables >= 0])
+    host_k = np.zeros((len(used),) + st.k_cache.shape[1:], np.uint16)
+    host_v = np.zeros_like(host_k)
+    out_pairs = np.stack([used, np.arange(len(used))], 1)
+    oracle.copy_blocks(st.k_cache, host_k, out_pairs)
+    oracle.copy_blocks(st.v_cache, host_v, out_pairs)
+    fresh = np.random.default_rng(2).permutation(st.NB)[:len(used)]
+    kc = np.full_like(st.k_cache, NAN_BITS[st.dtype])
+    vc = kc.copy()
+    in_pairs = np.stack([np.arange(len(used)), fresh], 1)
+    oracle.copy_blocks(host_k, kc, in_pairs)
+    oracle.copy_blocks(host_v, vc, in_pairs)
+    new_id = dict(zip(used.tolist(), fresh.tolist()))
+    tables = np.vectorize(lambda b: new_id.get(int(b), -1))(st.block_tables).astype(np.int32)
+    assert np.array_equal(oracle.decode(st.q, kc, vc, tables, ctx, st.dtype), ref)
+
+
 # ------------------------------------------------------------- closed forms
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,d", [("fp16", 4, 4, 64), ("bf16", 32, 8, 128), ("bf16", 16, 2, 64)])

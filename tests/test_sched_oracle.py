@@ -365,8 +365,8 @@ def test_swap_preemption_hand_worked_trace():
 @pytest.mark.parametrize("seed", range(4))
 def test_swap_preemption_invariants(seed):
     """Under memory pressure with swapping: host slots and device blocks are
-    never lost (free + held = pool, free slots + slots held = capacity), a
-    swapped request resumes with the length it had (its only prefill chunk
+    never lost (free + held = pool, free slots + slots held = capacity), no
+    slot is swapped in and out in one step, a swapped request resumes with the length it had (its only prefill chunk
     after a swap-in starts where it stopped), every request emits the tokens it
     would emit with recompute, and less is recomputed."""
     rng = np.random.default_rng(seed)
@@ -388,6 +388,9 @@ def test_swap_preemption_invariants(seed):
                 prefill += int(m.q_lens[m.q_lens > 1].sum())
                 for row, slot in m.swap_in:
                     assert 0 <= row < 24
+                # a slot read by a swap-in is never the target of a swap-out
+                # of the same step (the outs run first)
+                assert not set(m.swap_in[:, 0].tolist()) & set(m.swap_out[:, 1].tolist())
                 for rid, q, c in zip(m.seq_rids, m.q_lens, m.context_lens):
                     if int(rid) in before and not any(r.rid == rid and r.slots for r in s.waiting):
                         assert int(c) - int(q) == before[int(rid)], "resumed at the wrong length"
