@@ -395,6 +395,20 @@ def run_mixed(args):
     if int(status.item()) != 0:
         raise RuntimeError("device status %d in the side-by-side mixed step" % int(status.item()))
     fused_ms = statistics.mean(a.elapsed_time(b) for a, b in fe)
+    sweep = {}
+    for dn in [int(x) for x in args.mixed_decode_sms.split(",") if x]:
+        def forced(dn=dn):
+            pkv.kv_append(kn, vn, slots, kc, vc, dev_status=status, stream=stream)
+            pkv.paged_mixed_attention(out2, q, cu_p, p, max_q, kc, vc, bt, cl, workspace=work, decode_sms=dn,
+                                      dev_status=status, stream=stream)
+        for _ in range(args.warmup):
+            forced()
+        for a, b in fe:
+            a.record(stream)
+            forced()
+            b.record(stream)
+        torch.cuda.synchronize()
+        sweep[dn] = round(statistics.mean(a.elapsed_time(b) for a, b in fe), 4)
     flops = prefill_flops(st.context_lens[:p], st.q_lens[:p], st.Hq, st.d)
     dbytes = decode_bytes(st.context_lens[p:], st.Hq, st.Hkv, st.d)
     tpeak, tkind = load_tensor_peak()
@@ -409,6 +423,7 @@ def run_mixed(args):
         "side_by_side": {"ms_per_step": round(fused_ms, 4), "decode_sms": d_sms,
                          "note": "append, then pkv_paged_mixed_attention: decode on decode_sms SMs, prefill on the "
                                  "rest, concurrently; the kernel timings below are the sequential run"},
+        **({"decode_sms_sweep_ms": sweep} if sweep else {}),
         "kv_append_ms": round(app_ms, 4),
         "prefill": {"ms": round(pre_ms, 4), "gflop": round(flops / 1e9, 2), "tflops": round(tfl, 1),
                     "roofline": {"bound": "tensor", "achieved": round(tfl, 1), "peak": tpeak, "unit": "TFLOP/s",
@@ -784,6 +799,8 @@ def main():
     ap.add_argument("--mixed-prior", type=int, default=-1,
                     help="give every prefill chunk this prior context instead of U{0..4096} (profiling)")
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
+    ap.add_argument("--mixed-decode-sms", default="",
+                    help="comma-separated decode SM counts at which to time the side-by-side mixed step too")
     ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching", "prefix", "preempt"],
                     help="trace: the continuous-batching trace; batching: static vs continuous on one trace; "
                          "prefix: with and without the prefix cache on a sharing-heavy trace; preempt: recompute "
