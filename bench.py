@@ -45,8 +45,8 @@ def append_bytes(T, Hkv, d, esize=2):
 # DRAM traffic per algorithmic byte of the decode kernel, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum) of the 64-sequence case, valid
 # for the decode source with this SHA-1; reported as null once it changes.
-DECODE_TRAFFIC_RATIO = (326.75 + 3.12) / 325.041852
-DECODE_TRAFFIC_SHA1 = "8cdb21bd00476d09eb31a42860a69f98bfbbe32f"
+DECODE_TRAFFIC_RATIO = (326.76 + 3.35) / 325.041852
+DECODE_TRAFFIC_SHA1 = "3d37a90cccfffb11ea0919a2e588c10b69fff0b9"
 
 
 def decode_traffic(dbytes):
@@ -767,7 +767,7 @@ def run_pkv(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": decode_traffic(dbytes), "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel (split-KV, fused merge), bytes %d per launch" % dbytes,
-                     "traffic_source": "ncu capture of the 64-sequence case (1.015 x algorithmic), scaled by bytes"},
+                     "traffic_source": "ncu capture of the 64-sequence case (1.016 x algorithmic), scaled by bytes"},
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4)},
