@@ -174,6 +174,30 @@ int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, co
                                size_t workspace_bytes, int *dev_status, void *stream);
 
 /*
+ * pkv_paged_decode_append_attention -- the decode step's append and its
+ * attention in one launch: the same result as pkv_kv_append of k_new / v_new
+ * followed by pkv_paged_decode_attention ("tiny-vllm part 7": the new token's
+ * K/V are written into its block first, then attention runs over the whole
+ * context including it), with the slot of sequence s's new token taken from
+ * its block table: position context_lens[s] - 1, i.e. slot
+ * block_tables[s][(ctx-1)/16] * 16 + (ctx-1) % 16.
+ *   k_new, v_new  [num_seqs][num_kv_heads][head_dim], 16-B aligned
+ *   k_cache, v_cache  written at those slots (and read, as in decode)
+ * The warp that streams the last block of (s, KV head) loads the new rows
+ * with that block, uses them in place of the block's stale row and stores
+ * them to the cache, so the cache holds after the call exactly what the
+ * separate append would have written.  A sequence with context 0 appends
+ * nothing; a block id out of range skips the store and sets
+ * PKV_DEV_BAD_BLOCK_ID.  Everything else as pkv_paged_decode_attention.
+ */
+int pkv_paged_decode_append_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                      void *k_cache, void *v_cache, const int32_t *block_tables,
+                                      int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                      int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int block_size, float scale, int dtype, int out_dtype, void *workspace,
+                                      size_t workspace_bytes, int *dev_status, void *stream);
+
+/*
  * pkv_paged_prefill_attention -- chunked prefill: a chunk of new query tokens
  * per sequence attends the sequence's prior context plus the chunk, causally.
  *

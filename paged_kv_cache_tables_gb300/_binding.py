@@ -80,6 +80,7 @@ def lib():
         "pkv_kv_append": ([P, P, P, I, P, P, I, I, I, I, I, P, P], I),
         "pkv_decode_workspace_size": ([I, I, I, I], SZ),
         "pkv_paged_decode_attention": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, SZ, P, P], I),
+        "pkv_paged_decode_append_attention": ([P, P, P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, SZ, P, P], I),
         "pkv_paged_prefill_attention": ([P, P, P, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, P], I),
         "pkv_paged_decode_attention_static": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P], I),
         "pkv_paged_mixed_attention": ([P, P, P, I, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, SZ, P, P, I, P, P],
@@ -183,6 +184,28 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         float(scale), _dtype_code(q), _dtype_code(out), _dev(workspace, "workspace"), workspace.numel(),
         _status_ptr(dev_status), _stream(stream))
     _check("pkv_paged_decode_attention", st)
+
+
+def paged_decode_append_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale=None,
+                                  workspace=None, dev_status=None, stream=None):
+    """pkv_paged_decode_append_attention: kv_append of k_new/v_new [S, Hkv, d]
+    at position context_lens[s] - 1 of each sequence, then decode attention, in
+    one launch."""
+    import torch
+    L = lib()
+    S, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(max(16, decode_workspace_size(S, Hq, Hkv, d)), dtype=torch.uint8, device=q.device)
+    st = L.pkv_paged_decode_append_attention(
+        _dev(out, "out", ndim=3), _dev(q, "q", ndim=3), _dev(k_new, "k_new", q.dtype, 3),
+        _dev(v_new, "v_new", q.dtype, 3), _dev(k_cache, "k_cache", q.dtype, 4), _dev(v_cache, "v_cache", q.dtype, 4),
+        _dev(block_tables, "block_tables", torch.int32, 2), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32, 1), S, NB, Hq, Hkv, d, bs, float(scale), _dtype_code(q),
+        _dtype_code(out), _dev(workspace, "workspace"), workspace.numel(), _status_ptr(dev_status), _stream(stream))
+    _check("pkv_paged_decode_append_attention", st)
 
 
 def paged_prefill_attention(out, q, cu_seqlens, max_q_len, k_cache, v_cache, block_tables, context_lens, scale=None,

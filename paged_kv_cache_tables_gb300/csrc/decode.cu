@@ -69,6 +69,10 @@ struct DecodeParams {
     int rec_floats;     // m[G], l[G], acc[G][D], next, first block, padding to 16 B
     int pool_cap, steal_cap;
     uint32_t epoch;     // nonzero, different for every call
+    // fused append (null: none): row s of k_new / v_new [S][Hkv][D] is the
+    // token at position context_lens[s] - 1 of sequence s
+    const void *k_new, *v_new;
+    void *k_cache, *v_cache;
 };
 
 template <int D, int NT>
@@ -80,7 +84,11 @@ struct DecodeShape {
     static constexpr int STAGES = D == 128 ? 3 : 6;
     static constexpr int HP = 8 * NT;                   // heads an MMA tile holds
     static constexpr int RING_BYTES = kDecodeWarps * STAGES * STAGE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + kDecodeWarps * STAGES * 8 + 256;
+    // per slot: the new token's K and V rows (fused append) and its block id
+    static constexpr int ROW_BYTES = D * 2;
+    static constexpr int SIDE_BYTES = 2 * ROW_BYTES + 16;
+    static constexpr int SIDE_TOTAL = kDecodeWarps * STAGES * SIDE_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + SIDE_TOTAL + kDecodeWarps * STAGES * 8 + 256;
 };
 
 __device__ __forceinline__ int blocks_of(const int32_t *context_lens, int s, int max_blocks, int *dev_status,
@@ -298,7 +306,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + Sh::RING_BYTES);
+    uint8_t *side = smem + Sh::RING_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(side + Sh::SIDE_TOTAL);
     int64_t *sh_scan = reinterpret_cast<int64_t *>(bars + kDecodeWarps * STAGES);
     int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);   // segment holding each warp's first block
     int *plan_off = plan_s + kDecodeWarps;
@@ -369,7 +378,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
     // ---- this warp's ring ----
     uint8_t *wring = ring + warp * STAGES * Sh::STAGE_BYTES;
+    uint8_t *wside = side + warp * STAGES * Sh::SIDE_BYTES;
     uint64_t *wbar = bars + warp * STAGES;
+    const bool fuse_append = p.k_new != nullptr;
     if (lane == 0) {
         for (int st = 0; st < STAGES; ++st) mbar_init(&wbar[st], 1);
         fence_mbar_init();
@@ -431,13 +442,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     }
                     const int stage = (int)(slot % STAGES);
                     uint64_t *bar = &wbar[stage];
-                    mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES);
+                    // the last block of a range also brings the range's new
+                    // token (fused append), with the block id it goes to
+                    const bool with_row = fuse_append && pj == p_nb - 1;
+                    mbar_arrive_expect_tx(bar, Sh::STAGE_BYTES + (with_row ? 2 * Sh::ROW_BYTES : 0));
                     uint8_t *kdst = wring + stage * Sh::STAGE_BYTES;
                     uint8_t *vdst = kdst + Sh::TILE_BYTES;
 #pragma unroll
                     for (int hf = 0; hf < Sh::HALVES; ++hf) {
                         tma_load_2d(kdst + hf * Sh::HALF_BYTES, &tk, hf * 64, row, bar, policy);
                         tma_load_2d(vdst + hf * Sh::HALF_BYTES, &tv, hf * 64, row, bar, policy);
+                    }
+                    if (with_row) {
+                        uint8_t *sd = wside + stage * Sh::SIDE_BYTES;
+                        const size_t src = ((size_t)ps * Hkv + ph) * Sh::ROW_BYTES;
+                        bulk_load(sd, static_cast<const uint8_t *>(p.k_new) + src, Sh::ROW_BYTES, bar);
+                        bulk_load(sd + Sh::ROW_BYTES, static_cast<const uint8_t *>(p.v_new) + src, Sh::ROW_BYTES,
+                                  bar);
+                        *reinterpret_cast<int *>(sd + 2 * Sh::ROW_BYTES) = blk;
                     }
                 }
             };
@@ -614,6 +636,28 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 }
                 const uint32_t kbase = ring_addr + (slot % STAGES) * Sh::STAGE_BYTES;
                 const uint32_t vbase = kbase + Sh::TILE_BYTES;
+                if (fuse_append && cj == c_nb - 1) {
+                    // fused append: the new token's rows replace row (ctx-1)%16
+                    // of the tiles (which held the cache's old bytes) and go to
+                    // the cache; one lane per 16-byte chunk of the K and V rows
+                    constexpr int CH = D / 8;   // chunks per row
+                    const uint8_t *sd = wside + (slot % STAGES) * Sh::SIDE_BYTES;
+                    const int r = (c_ctx - 1) & 15;
+                    if (lane < 2 * CH) {
+                        const int which = lane / CH, c = lane % CH;
+                        const uint4 val = *reinterpret_cast<const uint4 *>(sd + which * Sh::ROW_BYTES + c * 16);
+                        const uint32_t dst = (which ? vbase : kbase) + (c >> 3) * Sh::HALF_BYTES + r * 128 +
+                                             (((c & 7) ^ (r & 7)) << 4);
+                        st_shared_v4(dst, val);
+                        const int blk = *reinterpret_cast<const int *>(sd + 2 * Sh::ROW_BYTES);
+                        if (blk >= 0 && blk < p.num_blocks) {
+                            uint8_t *cache = static_cast<uint8_t *>(which ? p.v_cache : p.k_cache);
+                            *reinterpret_cast<uint4 *>(cache + (((size_t)blk * Hkv + ch) * 16 + r) * Sh::ROW_BYTES +
+                                                       c * 16) = val;
+                        }
+                    }
+                    __syncwarp();
+                }
 
                 // ---- pull the block's K and V fragments into registers, then
                 // hand the slot straight back to the TMA engine ----
@@ -956,7 +1000,7 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
                      const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                      int num_blocks, int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
                      int dtype, int out_dtype, void *workspace, size_t workspace_bytes, int *dev_status,
-                     cudaStream_t stream, int max_sms) {
+                     cudaStream_t stream, int max_sms, const void *k_new, const void *v_new) {
     if (num_seqs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0)
         return PKV_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
@@ -974,6 +1018,8 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
         !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PKV_ERR_INVALID_ARG;
     if (!aligned(workspace, 16)) return PKV_ERR_WORKSPACE;
+    if ((k_new == nullptr) != (v_new == nullptr)) return PKV_ERR_INVALID_ARG;
+    if (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))) return PKV_ERR_INVALID_ARG;
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != PKV_OK) return rc;
@@ -1027,6 +1073,10 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     const char *det = std::getenv("PKV_DETERMINISTIC");
     if (det && det[0] == '1') prm.steal_cap = 0;
     prm.epoch = next_epoch();
+    prm.k_new = k_new;
+    prm.v_new = v_new;
+    prm.k_cache = const_cast<void *>(k_cache);
+    prm.v_cache = const_cast<void *>(v_cache);
     cudaStream_t st = stream;
     const bool wide = G > 8;
     if (dtype == PKV_DTYPE_BF16) {
@@ -1054,4 +1104,18 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
     return pkv::decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                  num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype,
                                  workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), 0);
+}
+
+extern "C" int pkv_paged_decode_append_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                                 void *k_cache, void *v_cache, const int32_t *block_tables,
+                                                 int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                                                 int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                                                 int block_size, float scale, int dtype, int out_dtype,
+                                                 void *workspace, size_t workspace_bytes, int *dev_status,
+                                                 void *stream) {
+    if (num_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
+    return pkv::decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                 num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype,
+                                 workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), 0, k_new,
+                                 v_new);
 }

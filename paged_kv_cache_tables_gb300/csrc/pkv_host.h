@@ -30,12 +30,14 @@ bool first_on_device(unsigned long long *flag_bits);
 // partial records per warp; no room left for stolen pieces).
 size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 
-// pkv_paged_decode_attention with its grid capped at max_sms CTAs (0: no cap).
+// pkv_paged_decode_attention with its grid capped at max_sms CTAs (0: no cap);
+// with k_new / v_new given, the append of each sequence's new token is fused
+// in (pkv_paged_decode_append_attention).
 int decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                      const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
                      int num_blocks, int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
                      int dtype, int out_dtype, void *workspace, size_t workspace_bytes, int *dev_status,
-                     cudaStream_t stream, int max_sms);
+                     cudaStream_t stream, int max_sms, const void *k_new = nullptr, const void *v_new = nullptr);
 
 // Encodes a 2-D TMA descriptor over a paged cache viewed as
 // [num_blocks * num_kv_heads * block_size rows][head_dim elements] of 16-bit
