@@ -98,6 +98,7 @@ extern "C" int pkv_paged_mixed_attention(void *out, const void *q, const int32_t
     using namespace pkv;
     if (num_prefill < 0 || num_decode < 0 || prefill_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0)
         return PKV_ERR_INVALID_ARG;
+    if (num_prefill == 0 && num_decode == 0) return PKV_OK;
     if (!out || !q || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
     const size_t in_row = (size_t)num_q_heads * head_dim * 2;
     const size_t out_row = (size_t)num_q_heads * head_dim * (out_dtype == PKV_DTYPE_F32 ? 4 : 2);

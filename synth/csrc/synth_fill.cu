@@ -45,7 +45,42 @@ __global__ void fill_rows_kernel(uint16_t *out, const int64_t *rids, const int32
     }
 }
 
+// One launch for a layer's Q, K and V rows: block (t, which) writes the row of
+// token t in out_which; the row's base hash is computed once.
+__device__ __forceinline__ uint16_t synth_value(uint32_t b, uint32_t e, int bf16) {
+    const uint32_t h = lowbias32(b ^ e);
+    const float x = (float)(h >> 8) * (1.0f / 16777216.0f) * 4.0f - 2.0f;
+    if (bf16) {
+        __nv_bfloat16 v = __float2bfloat16_rn(x);
+        return *reinterpret_cast<uint16_t *>(&v);
+    }
+    __half v = __float2half_rn(x);
+    return *reinterpret_cast<uint16_t *>(&v);
+}
+
+__global__ void fill_qkv_kernel(uint16_t *q, uint16_t *k, uint16_t *v, const int64_t *rids, const int32_t *pos,
+                                int wq, int wkv, uint32_t seed, uint32_t tq, uint32_t tk, uint32_t tv, int bf16) {
+    const int t = blockIdx.x, which = blockIdx.y;
+    uint16_t *out = which == 0 ? q : (which == 1 ? k : v);
+    const int width = which == 0 ? wq : wkv;
+    const uint32_t tag = which == 0 ? tq : (which == 1 ? tk : tv);
+    uint32_t b = lowbias32(seed ^ (uint32_t)rids[t]);
+    b = lowbias32(b ^ (uint32_t)pos[t]);
+    b = lowbias32(b ^ tag);
+    uint16_t *row = out + (int64_t)t * width;
+    for (int e = threadIdx.x; e < width; e += blockDim.x) row[e] = synth_value(b, (uint32_t)e, bf16);
+}
+
 }  // namespace
+
+extern "C" int synth_fill_qkv(void *q, void *k, void *v, const int64_t *rids, const int32_t *pos, int n, int wq,
+                              int wkv, uint32_t seed, uint32_t tq, uint32_t tk, uint32_t tv, int bf16, void *stream) {
+    if (n <= 0) return 0;
+    fill_qkv_kernel<<<dim3(n, 3), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint16_t *>(q), static_cast<uint16_t *>(k), static_cast<uint16_t *>(v), rids, pos, wq, wkv, seed,
+        tq, tk, tv, bf16);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
 
 extern "C" int synth_fill_rows(void *out, const int64_t *rids, const int32_t *pos, int n, int width, uint32_t seed,
                                uint32_t tag, int bf16, void *stream) {

@@ -148,6 +148,9 @@ def _gpu_lib():
         L.synth_fill_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, ctypes.c_void_p]
         L.synth_fill_rows.restype = ctypes.c_int
+        L.synth_fill_qkv.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int] * 3 + [ctypes.c_uint32] * 4 + \
+            [ctypes.c_int, ctypes.c_void_p]
+        L.synth_fill_qkv.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -165,13 +168,25 @@ def fill_rows_gpu(out, rids, pos, tag: int, stream=None) -> None:
         raise RuntimeError("synth_fill_rows failed")
 
 
+def fill_qkv_gpu(q, k, v, rids, pos, tq: int, tk: int, tv: int, stream=None) -> None:
+    """fill_rows_gpu of q, k and v (tags tq, tk, tv) in one launch."""
+    import torch
+    n = q.shape[0]
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = _gpu_lib().synth_fill_qkv(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                   ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(rids.data_ptr()),
+                                   ctypes.c_void_p(pos.data_ptr()), n, q.numel() // max(n, 1),
+                                   k.numel() // max(n, 1), HASH_SEED, tq, tk, tv,
+                                   1 if q.dtype == torch.bfloat16 else 0, ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise RuntimeError("synth_fill_qkv failed")
+
+
 def make_fill():
     """Per-layer filler for PagedEngine.step: Q rows tagged by layer, K/V rows
-    by the physical cache the layer writes."""
+    by the physical cache the layer writes (one launch per layer)."""
     def fill(layer, cid, q, k, v, trids, tpos):
-        fill_rows_gpu(q, trids, tpos, q_tag(layer))
-        fill_rows_gpu(k, trids, tpos, kv_tag(cid, "k"))
-        fill_rows_gpu(v, trids, tpos, kv_tag(cid, "v"))
+        fill_qkv_gpu(q, k, v, trids, tpos, q_tag(layer), kv_tag(cid, "k"), kv_tag(cid, "v"))
     return fill
 
 

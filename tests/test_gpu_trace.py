@@ -36,6 +36,21 @@ def test_gpu_generator_matches_numpy(cuda_lib, synth_gpu):
         assert np.array_equal(got, ref)
 
 
+def test_gpu_qkv_generator_matches_numpy(cuda_lib, synth_gpu):
+    from synth.trace import fill_qkv_gpu
+    rids = torch.tensor([5, 0, 99999999999, 7, 3], dtype=torch.int64, device="cuda")
+    pos = torch.tensor([3, 0, 4095, 16, 17], dtype=torch.int32, device="cuda")
+    q = torch.empty((5, HQ, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((5, HKV, D), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    tags = (q_tag(3), kv_tag(1, "k"), kv_tag(1, "v"))
+    fill_qkv_gpu(q, k, v, rids, pos, *tags)
+    torch.cuda.synchronize()
+    for t, tag in zip((q, k, v), tags):
+        got = t.cpu().view(torch.int16).numpy().view(np.uint16).reshape(5, -1)
+        assert np.array_equal(got, token_rows(rids.cpu().numpy(), pos.cpu().numpy(), tag, got.shape[1], "bf16"))
+
+
 def run(n, rate, prompt_mean, out_mean, NB, layers, caches, max_batch, budget, chunk, mml, seed, **kw):
     arrival, prompt, eos = make_requests(seed, n=n, rate=rate, prompt_mean=prompt_mean, out_mean=out_mean,
                                          pmax=mml // 2)
