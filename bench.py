@@ -466,6 +466,16 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=Fal
         raise RuntimeError("device status %d in the trace" % int(eng.status.item()))
     st = eng.sched.stats()
     steps = res["steps"]
+    if args.steps_jsonl:
+        # one record per engine step: batch shape, KV bytes per layer, device time
+        with open(args.steps_jsonl, "a") as f:
+            for s_ in steps:
+                ctx_ = s_["context_lens"]
+                f.write(json.dumps({"policy": policy, "caching": caching, "swap_blocks": swap_blocks,
+                                    "step": s_["step"], "seqs": int(s_["S"]), "tokens": int(s_["T"]),
+                                    "prefill_chunks": int(s_["P"]), "context_tokens": int(ctx_.sum()),
+                                    "kv_bytes_per_layer": int(ctx_.sum()) * 2 * 8 * 128 * 2,
+                                    "device_ms": round(s_["device_ms"], 4)}) + "\n")
     Hq, Hkv, d = 32, 8, 128
     dec_tokens = pre_keys = kv_bytes = 0
     big_bytes, big_ms, big_steps, dev_ms = 0, 0.0, 0, 0.0
@@ -827,6 +837,7 @@ def main():
                          "prefix: with and without the prefix cache on a sharing-heavy trace; preempt: recompute "
                          "vs swap on the trace with a small pool")
     ap.add_argument("--swap-blocks", type=int, default=0, help="host swap slots for --workload preempt")
+    ap.add_argument("--steps-jsonl", default="", help="trace workloads: append one JSON record per engine step here")
     ap.add_argument("--copy-rates-only", action="store_true", help="--workload preempt: only the block copy rates")
     ap.add_argument("--no-copy-rates", action="store_true")
     ap.add_argument("--trace-requests", type=int, default=1000)

@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const uint4 *__restrict_
 extern "C" int pkv_kv_append(const void *k, const void *v, const int64_t *slot_mapping, int num_tokens,
                              void *k_cache, void *v_cache, int num_blocks, int block_size, int num_kv_heads,
                              int head_dim, int dtype, int *dev_status, void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_kv_append");
     using namespace pkv;
     if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0) return PKV_ERR_INVALID_ARG;
     if (dtype != PKV_DTYPE_F16 && dtype != PKV_DTYPE_BF16) return PKV_ERR_UNSUPPORTED;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ ds
 extern "C" int pkv_copy_blocks(void *dst, int64_t dst_blocks, const void *src, int64_t src_blocks,
                                const int32_t *pairs, int num_pairs, int64_t block_bytes, int *dev_status,
                                void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_copy_blocks");
     using namespace pkv;
     if (num_pairs < 0 || block_bytes <= 0 || dst_blocks <= 0 || src_blocks <= 0) return PKV_ERR_INVALID_ARG;
     if (num_pairs == 0) return PKV_OK;

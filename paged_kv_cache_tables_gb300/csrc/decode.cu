@@ -1101,6 +1101,7 @@ extern "C" int pkv_paged_decode_attention(void *out, const void *q, const void *
                                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                           float scale, int dtype, int out_dtype, void *workspace,
                                           size_t workspace_bytes, int *dev_status, void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_paged_decode_attention");
     return pkv::decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                  num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype,
                                  workspace, workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), 0);
@@ -1113,6 +1114,7 @@ extern "C" int pkv_paged_decode_append_attention(void *out, const void *q, const
                                                  int block_size, float scale, int dtype, int out_dtype,
                                                  void *workspace, size_t workspace_bytes, int *dev_status,
                                                  void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_paged_decode_append_attention");
     if (num_seqs > 0 && (!k_new || !v_new)) return PKV_ERR_INVALID_ARG;
     return pkv::decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
                                  num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype,

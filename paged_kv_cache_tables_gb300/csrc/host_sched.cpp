@@ -18,6 +18,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "pkv.h"
 
 struct pkv_pool {
@@ -484,9 +486,11 @@ extern "C" int pkv_sched_add_tokens(pkv_sched *sched, int64_t rid, const int32_t
 
 extern "C" int pkv_sched_step(pkv_sched *sched, pkv_step_meta *out) {
     if (!sched || !out) return PKV_ERR_INVALID_ARG;
+    nvtxRangePushA("pkv_sched_step");
     auto t0 = std::chrono::steady_clock::now();
     int n = sched->step(out);
     auto t1 = std::chrono::steady_clock::now();
+    nvtxRangePop();
     sched->stats.host_ms += std::chrono::duration<double, std::milli>(t1 - t0).count();
     return n;
 }

@@ -95,6 +95,7 @@ extern "C" int pkv_paged_mixed_attention(void *out, const void *q, const int32_t
                                          int out_dtype, void *workspace, size_t workspace_bytes,
                                          const int32_t *cu_seqlens_host, const int32_t *context_lens_host,
                                          int decode_sms, int *dev_status, void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_paged_mixed_attention");
     using namespace pkv;
     if (num_prefill < 0 || num_decode < 0 || prefill_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0)
         return PKV_ERR_INVALID_ARG;

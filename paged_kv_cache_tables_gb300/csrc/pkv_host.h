@@ -6,11 +6,22 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <utility>
 
 #include "pkv.h"
 
 namespace pkv {
+
+// NVTX range around a host call (named after the entry point), so profilers
+// can filter and attribute the launches; costs a null check without a tool.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 // Records the CUDA error name for pkv_last_cuda_error() and returns PKV_ERR_CUDA.
 int cuda_fail(cudaError_t err);

@@ -20,6 +20,7 @@ extern "C" int pkv_paged_prefill_attention(void *out, const void *q, const int32
                                            const int32_t *context_lens, int num_blocks, int num_q_heads,
                                            int num_kv_heads, int head_dim, int block_size, float scale, int dtype,
                                            int out_dtype, int *dev_status, void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_paged_prefill_attention");
     using namespace pkv;
     if (num_seqs < 0 || max_q_len < 0 || total_q < 0 || num_blocks <= 0 || num_kv_heads <= 0 || num_q_heads <= 0 ||
         max_blocks_per_seq <= 0)
