@@ -103,7 +103,11 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
-            time.sleep(0.3)
+            # the timed region starts once nvidia-smi is up and sampling (its
+            # start-up on a fresh machine can take seconds)
+            t_end = time.time() + 15.0
+            while not self.lines and time.time() < t_end and self.proc.poll() is None:
+                time.sleep(0.05)
         except Exception:
             self.proc = None
         return self
@@ -430,6 +434,37 @@ def run_mixed(args):
     }
 
 
+def warm_up_kernels():
+    """One small call of every entry point the engine uses (module loading,
+    kernel attributes, the side stream, the tensor-map encoder) and of the
+    torch ops of the row sampling, so that a trace's first step is not
+    charged for them."""
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    from synth.trace import fill_qkv_gpu
+    NB, Hq, Hkv, d = 64, 32, 8, 128
+    kc = torch.zeros((NB, Hkv, 16, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    cl = torch.tensor([200, 17, 40], dtype=torch.int32, device="cuda")
+    bt = torch.arange(3 * 16, dtype=torch.int32, device="cuda").view(3, 16)
+    cu = torch.tensor([0, 128], dtype=torch.int32, device="cuda")
+    q = torch.zeros((130, Hq, d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    new = torch.zeros((130, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    rid = torch.zeros(130, dtype=torch.int64, device="cuda")
+    pos = torch.arange(130, dtype=torch.int32, device="cuda")
+    fill_qkv_gpu(q, new, new.clone(), rid, pos, 2, 0, 1)
+    pkv.kv_append(new, new, torch.arange(130, dtype=torch.int64, device="cuda"), kc, vc)
+    pkv.paged_prefill_attention(out[:128], q[:128], cu, 128, kc, vc, bt[:1], cl[:1])
+    pkv.paged_decode_append_attention(out[128:], q[128:], new[128:], new[128:], kc, vc, bt[1:], cl[1:])
+    pkv.paged_mixed_attention(out, q, cu, 1, 128, kc, vc, bt, cl, cu_seqlens_host=np.array([0, 128], np.int32),
+                              context_lens_host=np.array([200, 17, 40], np.int32))
+    # and the torch ops that copy sampled rows back (their kernels load lazily:
+    # seconds on a machine whose first process this is)
+    out.index_select(0, torch.tensor([0, 129], device="cuda")).float().to("cpu")
+    torch.cuda.synchronize()
+
+
 def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=False, caching=False, swap_blocks=0):
     """The continuous-batching trace: n requests, Poisson(20) arrivals per
     step, prompts lognormal (mean 512, sigma 1, clipped 8..4096), outputs
@@ -458,6 +493,8 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=Fal
                       preemption=_binding.PREEMPT_SWAP if swap_blocks else _binding.PREEMPT_RECOMPUTE,
                       swap_blocks=swap_blocks)
     rng = np.random.default_rng(seed + 1)
+    warm_up_kernels()
+    torch.cuda.synchronize()
     clk = ClockSampler(0)
     with clk:
         res = run_trace(eng, arrival, prompt, eos, max_tokens=4096, fill=make_fill(), sample_every=50,
