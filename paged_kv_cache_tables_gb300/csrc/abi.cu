@@ -26,14 +26,16 @@ int cuda_fail_driver(int cu_result, const char *what) {
 
 void set_error_message(const char *msg) { std::snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
 
-bool first_on_device(unsigned long long *flag_bits) {
+bool done_on_device(const unsigned long long *flag_bits) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return true;
-    const unsigned long long bit = 1ull << dev;
-    // races only repeat an idempotent attribute call
-    if (__atomic_load_n(flag_bits, __ATOMIC_ACQUIRE) & bit) return false;
-    __atomic_fetch_or(flag_bits, bit, __ATOMIC_ACQ_REL);
-    return true;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    return (__atomic_load_n(flag_bits, __ATOMIC_ACQUIRE) >> dev) & 1ull;
+}
+
+void mark_done_on_device(unsigned long long *flag_bits) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    __atomic_fetch_or(flag_bits, 1ull << dev, __ATOMIC_ACQ_REL);
 }
 
 int current_sm_count(int *num_sms) {
@@ -44,9 +46,12 @@ int current_sm_count(int *num_sms) {
         cuda_fail(e);
         return PKV_ERR_NO_DEVICE;
     }
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) {
-        *num_sms = cached[dev];
-        return PKV_OK;
+    if (dev >= 0 && dev < 64) {
+        const int c = __atomic_load_n(&cached[dev], __ATOMIC_RELAXED);
+        if (c > 0) {
+            *num_sms = c;
+            return PKV_OK;
+        }
     }
     int n = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
@@ -54,7 +59,7 @@ int current_sm_count(int *num_sms) {
         cuda_fail(e);
         return PKV_ERR_NO_DEVICE;
     }
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    if (dev >= 0 && dev < 64) __atomic_store_n(&cached[dev], n, __ATOMIC_RELAXED);
     *num_sms = n;
     return PKV_OK;
 }

@@ -915,10 +915,11 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
                          cudaStream_t stream) {
     using Sh = DecodeShape<D, NT>;
     static unsigned long long attr_set = 0;   // per instantiation and device
-    if (first_on_device(&attr_set)) {
+    if (!done_on_device(&attr_set)) {
         cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
+        mark_done_on_device(&attr_set);
     }
     cudaError_t e = launch_pdl(paged_decode_kernel<T, D, NT>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES,
                                stream, prm, tk, tv);

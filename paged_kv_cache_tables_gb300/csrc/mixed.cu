@@ -36,6 +36,8 @@ struct SideStream {
 SideStream g_side[64];
 std::mutex g_side_mu;   // also serialises the fork / launch / join sequence
 
+// The current device's side stream and events, created on first use.  Call
+// with g_side_mu held.
 int side_stream(SideStream **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -43,10 +45,16 @@ int side_stream(SideStream **out) {
     if (dev < 0 || dev >= 64) return PKV_ERR_UNSUPPORTED;
     SideStream &s = g_side[dev];
     if (!s.stream) {
-        e = cudaStreamCreateWithFlags(&s.stream, cudaStreamNonBlocking);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
-        if (e != cudaSuccess) return cuda_fail(e);
+        SideStream n;
+        e = cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            if (n.fork) cudaEventDestroy(n.fork);
+            if (n.stream) cudaStreamDestroy(n.stream);
+            return cuda_fail(e);
+        }
+        s = n;
     }
     *out = &s;
     return PKV_OK;
@@ -129,10 +137,10 @@ extern "C" int pkv_paged_mixed_attention(void *out, const void *q, const int32_t
                     : sms * 3 / 5;
     }
     d_sms = std::max(1, std::min(d_sms, sms - 1));
+    std::lock_guard<std::mutex> lock(g_side_mu);
     SideStream *side = nullptr;
     rc = side_stream(&side);
     if (rc != PKV_OK) return rc;
-    std::lock_guard<std::mutex> lock(g_side_mu);
     cudaError_t e = cudaEventRecord(side->fork, st);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
     if (e != cudaSuccess) return cuda_fail(e);

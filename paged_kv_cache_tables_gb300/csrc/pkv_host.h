@@ -32,10 +32,13 @@ void set_error_message(const char *msg);
 // SM count of the current device (cached per device).  PKV_OK or an error.
 int current_sm_count(int *num_sms);
 
-// Per-device "done once" flags (kernel attributes are set per device): true
-// the first time this is called for (flag, current device), false after.
-// Devices 0..63; beyond that it always returns true (setting again is harmless).
-bool first_on_device(unsigned long long *flag_bits);
+// Per-device "done once" flags (kernel attributes are set per device):
+// done_on_device tells whether mark_done_on_device has been called for the
+// current device.  A caller marks only after its one-time work succeeded, so a
+// concurrent caller either sees it done or repeats it (the attribute calls are
+// idempotent).  Devices 0..63; beyond that the work is always repeated.
+bool done_on_device(const unsigned long long *flag_bits);
+void mark_done_on_device(unsigned long long *flag_bits);
 
 // Smallest workspace pkv_paged_decode_attention accepts for this shape (two
 // partial records per warp; no room left for stolen pieces).

@@ -482,10 +482,11 @@ int launch_prefill_tc(const PrefillTcParams &prm, const CUtensorMap &tk, const C
     }
     if (regs_ok < 0) return PKV_ERR_UNSUPPORTED;
     static unsigned long long attr_set = 0;   // per instantiation and device
-    if (first_on_device(&attr_set)) {
+    if (!done_on_device(&attr_set)) {
         cudaError_t e = cudaFuncSetAttribute(paged_prefill_tc_kernel<T, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
+        mark_done_on_device(&attr_set);
     }
     cudaError_t e = launch_pdl(paged_prefill_tc_kernel<T, D>, dim3(grid), dim3(kTcThreads), Sh::SMEM_BYTES, stream,
                                prm, tk, tv, tq);
