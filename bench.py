@@ -41,8 +41,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # 64-sequence case, valid for the decode source with this SHA-1; reported as
 # null once it changes.
-DECODE_TRAFFIC_RATIO = (327.02 + 3.32) / 325.566140
-DECODE_TRAFFIC_SHA1 = "bfd712c96628147c190c3c6347553c99615bcd94"
+DECODE_TRAFFIC_RATIO = (327.02 + 3.50) / 325.566140
+DECODE_TRAFFIC_SHA1 = "b614c3bdc5c3b1e83c42a2b322bcecf900ec6f13"
 
 
 def decode_traffic(dbytes):
