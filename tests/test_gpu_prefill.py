@@ -62,6 +62,31 @@ def test_prefill_small_chunks_full_compare(cuda_lib, Hq, Hkv, d, dtype):
     assert int(ds.status.item()) == 0
 
 
+@pytest.mark.parametrize("Hq,Hkv,d", [(32, 8, 128), (16, 16, 64)])
+def test_prefill_long_chunks_sampled_rows(cuda_lib, Hq, Hkv, d):
+    """Chunks far longer than one tile pair (many pairs, ragged last pair),
+    one behind an 8,000-token context: sampled rows against the oracle, each
+    row being the decode of its own position (keys 0..pos) over the cache
+    after the append."""
+    priors, q_lens = [6500, 0, 77], [1500, 1100, 301]
+    st = chunk_step(priors, q_lens, Hq, Hkv, d, "bf16", seed=d + 1)
+    ds = DeviceStep(st)
+    kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
+    out = run_prefill(ds, "fp32")
+    kc, vc = oracle_after_append(st)
+    rng = np.random.default_rng(3)
+    got, ref = [], []
+    for c, (pr, ql) in enumerate(zip(priors, q_lens)):
+        rows = sorted(set([0, ql - 1, ql // 2] + list(rng.integers(0, ql, size=8))))
+        for i in rows:
+            row = int(st.cu_seqlens[c]) + i
+            ref.append(oracle.decode(st.q[row:row + 1], kc, vc, st.block_tables[c:c + 1],
+                                     np.array([pr + i + 1], np.int32), "bf16")[0])
+            got.append(out_to_f64(out[row:row + 1])[0])
+    assert_close(np.array(got), np.array(ref), "fp32", what="long chunks %d/%d d%d" % (Hq, Hkv, d))
+    assert int(ds.status.item()) == 0
+
+
 def test_prefill_with_one_query_row_equals_decode(cuda_lib):
     st = make_step("llama1b", S=24)
     ds = DeviceStep(st)
