@@ -41,8 +41,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # 64-sequence case, valid for the decode source with this SHA-1; reported as
 # null once it changes.
-DECODE_TRAFFIC_RATIO = (327.02 + 3.50) / 325.566140
-DECODE_TRAFFIC_SHA1 = "b614c3bdc5c3b1e83c42a2b322bcecf900ec6f13"
+DECODE_TRAFFIC_RATIO = (327.01 + 3.50) / 325.566140
+DECODE_TRAFFIC_SHA1 = "b651ff122b61c1dd6717761cebfe5d3a0545d63e"
 
 
 def decode_traffic(dbytes):

@@ -48,7 +48,13 @@ constexpr int kDecodeWarps = 8;
 constexpr int kClaimBatch = 4;      // blocks an owner claims per atomic add
 constexpr int kStealMin = 10;       // unclaimed blocks a warp must hold to be robbed
 constexpr int kMaxWarpBlocks = 1 << 22;   // range offsets live in 24-bit fields
-constexpr int kMinWarpBlocks = 20;  // a small step uses fewer warps, each with at least this many blocks
+// A step too small to give every warp a share uses fewer warps, each with at
+// least clamp(ceil(longest range / kMaxPieces), 1, kMinWarpBlocks) blocks:
+// short ranges spread over many warps (a small step is bound by latency, not
+// bandwidth), while a long range is not cut into more pieces than its merge
+// (a chain of dependent loads) is worth.
+constexpr int kMaxPieces = 4;
+constexpr int kMinWarpBlocks = 20;
 
 struct DecodeParams {
     void *out;
@@ -148,30 +154,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     unsigned long long v;
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
-}
-
-__device__ __forceinline__ unsigned long long cas_acq_rel(unsigned long long *p, unsigned long long cmp,
-                                                          unsigned long long val) {
-    unsigned long long prev;
-    asm volatile("atom.acq_rel.gpu.global.cas.b64 %0, [%1], %2, %3;" : "=l"(prev) : "l"(p), "l"(cmp), "l"(val)
-                 : "memory");
-    return prev;
-}
-
-// Adds n to an epoch-tagged counter ((epoch << 32) | count) and returns the
-// new count of this call; a value left by an earlier call counts as zero.
-// Acquire and release: it publishes this thread's earlier writes and sees
-// those of every earlier adder.  Returns 0 if the update kept losing races.
-__device__ __forceinline__ uint32_t epoch_add(unsigned long long *ctr, uint32_t epoch, uint32_t n) {
-    unsigned long long cur = ld_relaxed_u64(ctr);
-    for (int it = 0; it < (1 << 16); ++it) {
-        const unsigned long long want =
-            (uint32_t)(cur >> 32) == epoch ? cur + n : (((unsigned long long)epoch << 32) | n);
-        const unsigned long long prev = cas_acq_rel(ctr, cur, want);
-        if (prev == cur) return (uint32_t)(want & 0xffffffffull);
-        cur = prev;
-    }
-    return 0;
 }
 
 // Shared counters hit by every warp of the grid ((epoch << 32) | count): each
@@ -311,6 +293,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int64_t *sh_scan = reinterpret_cast<int64_t *>(bars + kDecodeWarps * STAGES);
     int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);   // segment holding each warp's first block
     int *plan_off = plan_s + kDecodeWarps;
+    int *sh_max = plan_off + kDecodeWarps;                           // per-warp longest sequence, in blocks
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
@@ -326,13 +309,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     // ---- plan: total blocks, this CTA's warp starts; CTA 0 publishes the
     // per-sequence block offsets that thieves search ----
     int64_t local = 0;
-    for (int s = tid; s < p.S; s += blockDim.x) local += blocks_of(p.context_lens, s, p.max_blocks, p.dev_status, nullptr);
+    int local_max = 0;
+    for (int s = tid; s < p.S; s += blockDim.x) {
+        const int nb = blocks_of(p.context_lens, s, p.max_blocks, p.dev_status, nullptr);
+        local += nb;
+        local_max = max(local_max, nb);
+    }
+    local_max = __reduce_max_sync(0xffffffffu, local_max);
+    if (lane == 0) sh_max[warp] = local_max;
     int64_t total_nblk;
     block_scan(local, sh_scan, &total_nblk);
     const int64_t total = total_nblk * Hkv;
     // warps that get a share: all of them, unless the step is too small to
-    // give each at least kMinWarpBlocks blocks
-    int64_t nw = (total + kMinWarpBlocks - 1) / kMinWarpBlocks;
+    // give each at least min_blocks blocks (the scan's barriers published sh_max)
+    int max_nb = 0;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) max_nb = max(max_nb, sh_max[w]);
+    const int64_t min_blocks = min(kMinWarpBlocks, max(1, (max_nb + kMaxPieces - 1) / kMaxPieces));
+    int64_t nw = (total + min_blocks - 1) / min_blocks;
     if (nw > p.total_warps) nw = p.total_warps;
     if (nw < 1) nw = 1;
     if (tid < kDecodeWarps) plan_s[tid] = -1;
@@ -571,7 +565,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     const uint32_t nxt = (uint32_t)(prev >> 32) == p.epoch ? (uint32_t)prev : 0u;
                     rec[2 * G + G * D] = __uint_as_float(nxt);
                     rec[2 * G + G * D + 1] = __int_as_float(piece_j0);
-                    done = epoch_add(p.seg_done + seg, p.epoch, (uint32_t)piece_n);
+                    // the pieces of a range often finish together: open the
+                    // counter for this call (one compare-and-swap that only
+                    // the first opener wins) and count with a plain add, which
+                    // does not retry under contention as a swap loop would;
+                    // the fences around the add make it a release for this
+                    // piece's record and an acquire for the others'
+                    __threadfence();
+                    epoch_open(p.seg_done + seg, p.epoch);
+                    done = epoch_fetch_add(p.seg_done + seg, p.epoch, (uint32_t)piece_n);
+                    __threadfence();
                 }
                 done = __shfl_sync(0xffffffffu, done, 0);
                 if (done == (uint32_t)c_nb) {
