@@ -473,6 +473,12 @@ int pkv_sched_inject_alloc_failure(pkv_sched *sched, int64_t nth);
 /* Request state: 0 waiting, 1 running, 2 finished, -1 unknown rid.
  * generated (may be NULL) receives its output-token count. */
 int pkv_sched_request_state(const pkv_sched *sched, int64_t rid, int *generated);
+/* Drops a finished request's record (its blocks, prompt tokens and swap
+ * slots were already released when it finished; what remains are a few
+ * counters), so that a long-running scheduler's memory stays bounded; its rid
+ * may then be added again.  PKV_ERR_INVALID_ARG for an unknown rid or a
+ * request that has not finished. */
+int pkv_sched_forget(pkv_sched *sched, int64_t rid);
 
 #ifdef __cplusplus
 }

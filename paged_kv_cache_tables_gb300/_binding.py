@@ -102,6 +102,7 @@ def lib():
         "pkv_sched_get_stats": ([P, ctypes.POINTER(SchedStats)], I),
         "pkv_sched_inject_alloc_failure": ([P, I64], I),
         "pkv_sched_request_state": ([P, I64, ctypes.POINTER(ctypes.c_int)], I),
+        "pkv_sched_forget": ([P, I64], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -417,3 +418,7 @@ class Scheduler:
         g = ctypes.c_int(0)
         st = lib().pkv_sched_request_state(self._h, rid, ctypes.byref(g))
         return st, g.value
+
+    def forget(self, rid):
+        """pkv_sched_forget: drop a finished request's record."""
+        _check("pkv_sched_forget", lib().pkv_sched_forget(self._h, rid))

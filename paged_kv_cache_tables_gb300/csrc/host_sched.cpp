@@ -147,6 +147,7 @@ struct pkv_sched {
     int max_blocks = 0;
     std::vector<Request> reqs;
     std::unordered_map<int64_t, int> index;
+    std::vector<int> free_reqs;        // slots of forgotten requests, reused by add
     std::vector<int> running;          // request indices, admission order
     std::deque<int> waiting;
     pkv_sched_stats stats{};
@@ -415,6 +416,10 @@ int pkv_sched::step(pkv_step_meta *out) {
             if (r.generated >= r.eos_after || r.generated >= r.max_tokens ||
                 r.length() >= cfg.max_model_len) {
                 release_blocks(r.blocks);
+                // a finished request keeps only its counters
+                std::vector<int32_t>().swap(r.blocks);
+                std::vector<int32_t>().swap(r.tokens);
+                std::vector<int32_t>().swap(r.slots);
                 r.state = FINISHED;
                 running.erase(std::find(running.begin(), running.end(), x.first));
                 ++stats.finished;
@@ -469,9 +474,26 @@ extern "C" int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int 
     r.prompt_len = prompt_len;
     r.max_tokens = max_tokens;
     r.eos_after = eos_after;
-    sched->index[rid] = (int)sched->reqs.size();
-    sched->reqs.push_back(std::move(r));
-    sched->waiting.push_back((int)sched->reqs.size() - 1);
+    int idx;
+    if (!sched->free_reqs.empty()) {
+        idx = sched->free_reqs.back();
+        sched->free_reqs.pop_back();
+        sched->reqs[idx] = std::move(r);
+    } else {
+        idx = (int)sched->reqs.size();
+        sched->reqs.push_back(std::move(r));
+    }
+    sched->index[rid] = idx;
+    sched->waiting.push_back(idx);
+    return PKV_OK;
+}
+
+extern "C" int pkv_sched_forget(pkv_sched *sched, int64_t rid) {
+    if (!sched) return PKV_ERR_INVALID_ARG;
+    auto it = sched->index.find(rid);
+    if (it == sched->index.end() || sched->reqs[it->second].state != FINISHED) return PKV_ERR_INVALID_ARG;
+    sched->free_reqs.push_back(it->second);
+    sched->index.erase(it);
     return PKV_OK;
 }
 
@@ -480,7 +502,7 @@ extern "C" int pkv_sched_add_tokens(pkv_sched *sched, int64_t rid, const int32_t
     if (!tokens) return PKV_ERR_INVALID_ARG;
     const int rc = pkv_sched_add(sched, rid, prompt_len, max_tokens, eos_after);
     if (rc != PKV_OK) return rc;
-    sched->reqs.back().tokens.assign(tokens, tokens + prompt_len);
+    sched->reqs[sched->index[rid]].tokens.assign(tokens, tokens + prompt_len);
     return PKV_OK;
 }
 

@@ -32,7 +32,7 @@ class PagedEngine:
     def __init__(self, num_blocks, num_layers=32, num_caches=4, Hq=32, Hkv=8, d=128, dtype="bf16",
                  max_batch=256, max_num_batched_tokens=8192, chunk=512, max_model_len=8192, initial_order=None,
                  device="cuda", policy=B.SCHED_CONTINUOUS, prefix_caching=False, row_keys=None,
-                 preemption=B.PREEMPT_RECOMPUTE, swap_blocks=0):
+                 preemption=B.PREEMPT_RECOMPUTE, swap_blocks=0, forget_finished=True):
         import torch
         self.torch = torch
         self.L, self.R = num_layers, num_caches
@@ -42,6 +42,7 @@ class PagedEngine:
         self.sched = B.Scheduler(num_blocks, 16, max_batch, max_num_batched_tokens, chunk, max_model_len,
                                  initial_order=initial_order, policy=policy, prefix_caching=prefix_caching,
                                  preemption=preemption, swap_blocks=swap_blocks)
+        self.forget_finished = forget_finished
         # row_keys(token_rids, token_pos) -> int64 keys handed to `fill` in
         # place of the request ids (a caller whose rows depend on content)
         self.row_keys = row_keys
@@ -171,6 +172,11 @@ class PagedEngine:
                 "context_lens": arr(m.context_lens, S).copy(), "cu_seqlens": cu_h.copy(),
                 "q_lens": arr(m.q_lens, S).copy(),
                 "finished": arr(m.finished_rids, m.num_finished).copy() if m.num_finished else np.zeros(0, np.int64)}
+        if self.forget_finished:
+            # the scheduler keeps a finished request's counters until told to
+            # drop them; a serving loop learns of the finish here
+            for rid in info["finished"]:
+                self.sched.forget(int(rid))
         # the step's device pointers are resolved once; every layer then calls
         # the C ABI directly (the same entry points the binding wraps)
         L = B.lib()

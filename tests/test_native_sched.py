@@ -226,3 +226,49 @@ def test_request_state_and_host_time():
     assert s.request_state(5) == (2, 3)
     assert s.request_state(99)[0] == -1
     assert s.stats()["host_ms"] >= 0.0
+
+
+def test_forget_releases_finished_requests_and_reuses_their_slots():
+    """A finished request can be forgotten (then unknown, its rid free again);
+    a waiting or running one cannot; a long run that forgets every finished
+    request emits the same steps as one that keeps them all."""
+    s = Scheduler(64, max_model_len=256)
+    s.add(5, 20, 3, 100)
+    s.add(6, 40, 2, 100)
+    with pytest.raises(PkvError):
+        s.forget(5)                      # waiting
+    s.step()
+    with pytest.raises(PkvError):
+        s.forget(5)                      # running
+    while s.step() is not None:
+        pass
+    s.forget(5)
+    assert s.request_state(5)[0] == -1 and s.request_state(6) == (2, 2)
+    with pytest.raises(PkvError):
+        s.forget(5)                      # already forgotten
+    s.add(5, 16, 1, 100)                 # the rid is free again
+    assert s.step()["seq_rids"].tolist() == [5]
+
+    rng = np.random.default_rng(4)
+    arrivals = [(int(rng.integers(0, 60)), rid, int(rng.integers(1, 90)), int(rng.integers(1, 40)))
+                for rid in range(120)]
+    arrivals.sort()
+    traces = []
+    for forget in (False, True):
+        sc = Scheduler(48, max_batch=8, max_num_batched_tokens=128, chunk=48, max_model_len=256)
+        i, steps = 0, []
+        for step in range(4000):
+            while i < len(arrivals) and arrivals[i][0] <= step:
+                _, rid, p, eos = arrivals[i]
+                sc.add(rid, p, 64, eos)
+                i += 1
+            m = sc.step()
+            if m is not None:
+                steps.append((m["seq_rids"].tolist(), m["slot_mapping"].tolist()))
+                if forget:
+                    for rid in m["finished_rids"]:
+                        sc.forget(int(rid))
+            if i == len(arrivals) and sc.stats()["running"] == 0 and sc.stats()["waiting"] == 0:
+                break
+        traces.append(steps)
+    assert traces[0] == traces[1]
