@@ -57,6 +57,7 @@ extern "C" {
 #define PKV_ERR_CUDA (-4)          /* a CUDA runtime/driver call failed */
 #define PKV_ERR_OUT_OF_BLOCKS (-5) /* block pool exhausted (host allocator) */
 #define PKV_ERR_NO_DEVICE (-6)     /* no CUDA device is current / visible */
+#define PKV_ERR_NO_MEMORY (-7)     /* a host allocation inside the library failed */
 
 /* ---- dtypes ---------------------------------------------------------------- */
 #define PKV_DTYPE_F16 0

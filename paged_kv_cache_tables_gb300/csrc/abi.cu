@@ -124,6 +124,7 @@ extern "C" const char *pkv_status_string(int status) {
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
         case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
         case PKV_ERR_NO_DEVICE: return "PKV_ERR_NO_DEVICE";
+        case PKV_ERR_NO_MEMORY: return "PKV_ERR_NO_MEMORY";
         default: return "PKV_ERR_UNKNOWN";
     }
 }

@@ -68,7 +68,7 @@ struct pkv_pool {
     }
 };
 
-extern "C" pkv_pool *pkv_pool_create(int num_blocks, const int32_t *initial_order) {
+static pkv_pool *pool_create_impl(int num_blocks, const int32_t *initial_order) {
     pkv_pool *p = new (std::nothrow) pkv_pool();
     if (!p) return nullptr;
     if (!p->init(num_blocks, initial_order)) {
@@ -80,7 +80,7 @@ extern "C" pkv_pool *pkv_pool_create(int num_blocks, const int32_t *initial_orde
 
 extern "C" void pkv_pool_destroy(pkv_pool *pool) { delete pool; }
 
-extern "C" int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *out_ids) {
+static int pool_alloc_impl(pkv_pool *pool, int n, int32_t *out_ids) {
     if (!pool || n < 0 || (n > 0 && !out_ids)) return PKV_ERR_INVALID_ARG;
     std::vector<int32_t> got;
     got.reserve(n);
@@ -89,7 +89,7 @@ extern "C" int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *out_ids) {
     return PKV_OK;
 }
 
-extern "C" int pkv_pool_free(pkv_pool *pool, const int32_t *ids, int n) {
+static int pool_free_impl(pkv_pool *pool, const int32_t *ids, int n) {
     if (!pool || n < 0 || (n > 0 && !ids)) return PKV_ERR_INVALID_ARG;
     std::vector<uint8_t> seen(pool->num_blocks, 0);
     for (int i = 0; i < n; ++i) {
@@ -437,7 +437,7 @@ int pkv_sched::step(pkv_step_meta *out) {
     return (int)scheduled.size();
 }
 
-extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
+static pkv_sched *sched_create_impl(const pkv_sched_config *config) {
     if (!config) return nullptr;
     const pkv_sched_config &c = *config;
     if (c.num_blocks <= 0 || c.block_size <= 0 || c.max_batch <= 0 || c.max_num_batched_tokens <= 0 ||
@@ -463,7 +463,7 @@ extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
 
 extern "C" void pkv_sched_destroy(pkv_sched *sched) { delete sched; }
 
-extern "C" int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int max_tokens,
+static int sched_add_impl(pkv_sched *sched, int64_t rid, int prompt_len, int max_tokens,
                              int eos_after) {
     if (!sched || prompt_len < 1 || prompt_len >= sched->cfg.max_model_len || max_tokens < 1 ||
         eos_after < 1)
@@ -488,7 +488,7 @@ extern "C" int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int 
     return PKV_OK;
 }
 
-extern "C" int pkv_sched_forget(pkv_sched *sched, int64_t rid) {
+static int sched_forget_impl(pkv_sched *sched, int64_t rid) {
     if (!sched) return PKV_ERR_INVALID_ARG;
     auto it = sched->index.find(rid);
     if (it == sched->index.end() || sched->reqs[it->second].state != FINISHED) return PKV_ERR_INVALID_ARG;
@@ -497,16 +497,16 @@ extern "C" int pkv_sched_forget(pkv_sched *sched, int64_t rid) {
     return PKV_OK;
 }
 
-extern "C" int pkv_sched_add_tokens(pkv_sched *sched, int64_t rid, const int32_t *tokens, int prompt_len,
+static int sched_add_tokens_impl(pkv_sched *sched, int64_t rid, const int32_t *tokens, int prompt_len,
                                     int max_tokens, int eos_after) {
     if (!tokens) return PKV_ERR_INVALID_ARG;
-    const int rc = pkv_sched_add(sched, rid, prompt_len, max_tokens, eos_after);
+    const int rc = sched_add_impl(sched, rid, prompt_len, max_tokens, eos_after);
     if (rc != PKV_OK) return rc;
     sched->reqs[sched->index[rid]].tokens.assign(tokens, tokens + prompt_len);
     return PKV_OK;
 }
 
-extern "C" int pkv_sched_step(pkv_sched *sched, pkv_step_meta *out) {
+static int sched_step_impl(pkv_sched *sched, pkv_step_meta *out) {
     if (!sched || !out) return PKV_ERR_INVALID_ARG;
     nvtxRangePushA("pkv_sched_step");
     auto t0 = std::chrono::steady_clock::now();
@@ -540,4 +540,74 @@ extern "C" int pkv_sched_request_state(const pkv_sched *sched, int64_t rid, int 
     const Request &r = sched->reqs[it->second];
     if (generated) *generated = r.generated;
     return (int)r.state;
+}
+
+// ---------------------------------------------------------- C entry points
+// The C ABI never lets a C++ exception out: an allocation failure inside
+// returns PKV_ERR_NO_MEMORY (a null handle from the create calls); a
+// scheduler that hit one mid-step should be destroyed.
+
+extern "C" pkv_pool *pkv_pool_create(int num_blocks, const int32_t *initial_order) {
+    try {
+        return pool_create_impl(num_blocks, initial_order);
+    } catch (const std::bad_alloc &) {
+        return nullptr;
+    }
+}
+
+extern "C" int pkv_pool_alloc(pkv_pool *pool, int n, int32_t *out_ids) {
+    try {
+        return pool_alloc_impl(pool, n, out_ids);
+    } catch (const std::bad_alloc &) {
+        return PKV_ERR_NO_MEMORY;
+    }
+}
+
+extern "C" int pkv_pool_free(pkv_pool *pool, const int32_t *ids, int n) {
+    try {
+        return pool_free_impl(pool, ids, n);
+    } catch (const std::bad_alloc &) {
+        return PKV_ERR_NO_MEMORY;
+    }
+}
+
+extern "C" pkv_sched *pkv_sched_create(const pkv_sched_config *config) {
+    try {
+        return sched_create_impl(config);
+    } catch (const std::bad_alloc &) {
+        return nullptr;
+    }
+}
+
+extern "C" int pkv_sched_add(pkv_sched *sched, int64_t rid, int prompt_len, int max_tokens, int eos_after) {
+    try {
+        return sched_add_impl(sched, rid, prompt_len, max_tokens, eos_after);
+    } catch (const std::bad_alloc &) {
+        return PKV_ERR_NO_MEMORY;
+    }
+}
+
+extern "C" int pkv_sched_forget(pkv_sched *sched, int64_t rid) {
+    try {
+        return sched_forget_impl(sched, rid);
+    } catch (const std::bad_alloc &) {
+        return PKV_ERR_NO_MEMORY;
+    }
+}
+
+extern "C" int pkv_sched_add_tokens(pkv_sched *sched, int64_t rid, const int32_t *tokens, int prompt_len,
+                                    int max_tokens, int eos_after) {
+    try {
+        return sched_add_tokens_impl(sched, rid, tokens, prompt_len, max_tokens, eos_after);
+    } catch (const std::bad_alloc &) {
+        return PKV_ERR_NO_MEMORY;
+    }
+}
+
+extern "C" int pkv_sched_step(pkv_sched *sched, pkv_step_meta *out) {
+    try {
+        return sched_step_impl(sched, out);
+    } catch (const std::bad_alloc &) {
+        return PKV_ERR_NO_MEMORY;
+    }
 }

@@ -35,6 +35,7 @@ def test_status_strings():
     L = _binding.lib()
     assert L.pkv_status_string(0) == b"PKV_OK"
     assert L.pkv_status_string(-3) == b"PKV_ERR_WORKSPACE"
+    assert L.pkv_status_string(-7) == b"PKV_ERR_NO_MEMORY"
     assert L.pkv_status_string(12345) == b"PKV_ERR_UNKNOWN"
     assert b"sm_103a" in L.pkv_version()
 
