@@ -2,8 +2,9 @@
 workload (256 sequences, 32 query / 8 KV heads, head_dim 128, 16-token blocks,
 lognormal contexts with median 1024 clipped to 32..8192, bf16, 64k-block pool).
 
-A step = append of the 256 new tokens' K/V by slot mapping, then paged decode
-attention over every sequence's whole context (split-KV kernel + merge).
+A step = append of the 256 new tokens' K/V, then paged decode attention over
+every sequence's whole context, in one launch (the append fused into the
+split-KV decode kernel; the same step as two launches is timed beside it).
 Prints ONE JSON line (rank 0).  `--impl reference` times the FP64 CPU oracle
 on a bounded sample of the same workload instead.
 
@@ -217,6 +218,17 @@ def cpu_oracle_run(st, k, min_seconds=0.0):
             "seconds": dt / reps}
 
 
+def step_config(st, ws):
+    """The `config` of the decode-step line (both arms)."""
+    dbytes = decode_bytes(st.context_lens, st.Hq, st.Hkv, st.d)
+    return {"workload": WORKLOAD, "seqs_per_gpu": st.S, "q_heads": st.Hq, "kv_heads": st.Hkv, "head_dim": st.d,
+            "block_size": st.bs, "pool_blocks": st.NB, "mean_context": round(float(st.context_lens.mean()), 1),
+            "step": "kv_append(256 tokens) + paged_decode_attention, fused in one launch "
+                    "(pkv_paged_decode_append_attention)",
+            "l2": "inputs larger than L2 (%.2f GB of KV per step vs 129 MB L2), no flush" % (dbytes / 1e9),
+            "parallelism": "dp%d" % ws}
+
+
 def run_reference(args):
     ws, rank, _ = dist_setup(args)
     if rank != 0:
@@ -235,8 +247,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "seqs": st.S, "q_heads": st.Hq, "kv_heads": st.Hkv, "head_dim": st.d,
-                       "block_size": st.bs, "sample": vals[-1]["sample"]},
+            "config": step_config(st, args.gpus),
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": vals[-1]["sample"]},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -822,11 +833,7 @@ def run_pkv(args):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "seqs_per_gpu": S, "q_heads": Hq, "kv_heads": Hkv, "head_dim": d,
-                   "block_size": st.bs, "pool_blocks": st.NB, "mean_context": round(float(st.context_lens.mean()), 1),
-                   "step": "kv_append(256 tokens) + paged_decode_attention, fused in one launch "
-                           "(pkv_paged_decode_append_attention)", "l2": "inputs larger than L2 "
-                   "(%.2f GB of KV per step vs 129 MB L2), no flush" % (dbytes / 1e9), "parallelism": "dp%d" % ws},
+        "config": step_config(st, ws),
         "attended_tokens_per_s": round(attended * ws / (ms_step * 1e-3), 1),
         "pct_of_8tbs": round(100 * value / 8000.0, 2),
         "kernels_ms": {"paged_decode_append_attention": round(fused_ms, 4)},
