@@ -440,6 +440,9 @@ def run_mixed(args):
         **({"decode_sms_sweep_ms": sweep} if sweep else {}),
         "kv_append_ms": round(app_ms, 4),
         "prefill": {"ms": round(pre_ms, 4), "gflop": round(flops / 1e9, 2), "tflops": round(tfl, 1),
+                    "executed_tflops": round(tfl * 1.5, 1),
+                    "executed_note": "tensor-core work actually issued: Q.K^T once and P.V twice (the rounded "
+                                     "16-bit P and its rounding residual), 1.5 x the algorithmic FLOPs",
                     "roofline": {"bound": "tensor", "achieved": round(tfl, 1), "peak": tpeak, "unit": "TFLOP/s",
                                  "frac": round(tfl / tpeak, 4), "traffic": None, "peak_source": tkind}},
         "decode": {"ms": round(dec_ms, 4), "bytes": dbytes,
