@@ -258,6 +258,34 @@ int pkv_paged_mixed_attention(void *out, const void *q, const int32_t *cu_seqlen
                               const int32_t *context_lens_host, int decode_sms, int *dev_status, void *stream);
 
 /*
+ * pkv_paged_mixed_append_attention -- one whole mixed step in one call: the
+ * append of the step's new tokens ("tiny-vllm part 7": each new token's K/V
+ * is written into its block before attention) and then the attention of
+ * pkv_paged_mixed_attention.
+ *   k_new, v_new   [prefill_tokens + num_decode][num_kv_heads][head_dim],
+ *                  rows in the order of q; 16-B aligned
+ *   slot_mapping   int64 [prefill_tokens]: slots of the prefill chunks' rows
+ *                  (as pkv_kv_append; < 0 skips).  A decode row s goes to
+ *                  position context_lens[s] - 1 through its block table, as
+ *                  in pkv_paged_decode_append_attention.
+ * The prefill rows are appended just before the prefill kernel (on the side
+ * stream, where both kinds of work are present) and the decode rows inside the
+ * decode kernel, so the append no longer delays the decode kernel's start.
+ * Results (outputs and caches) equal pkv_kv_append of all rows followed by
+ * pkv_paged_mixed_attention.  Prefill chunks and decodes must not write the
+ * same block (true of scheduler output: a shared prefix page is never
+ * written).
+ */
+int pkv_paged_mixed_append_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                     const int64_t *slot_mapping, const int32_t *cu_seqlens, int num_prefill,
+                                     int prefill_tokens, int max_q_len, int num_decode, void *k_cache, void *v_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                                     int num_blocks, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                     float scale, int dtype, int out_dtype, void *workspace, size_t workspace_bytes,
+                                     const int32_t *cu_seqlens_host, const int32_t *context_lens_host, int decode_sms,
+                                     int *dev_status, void *stream);
+
+/*
  * The SMs pkv_paged_mixed_attention gives the decode kernel for a step (host
  * arrays as above): the split that balances the two kernels' times under a
  * model of their per-SM rates on GB300 -- prefill ~7 TFLOP/s of algorithmic

@@ -85,6 +85,8 @@ def lib():
         "pkv_paged_decode_attention_static": ([P, P, P, P, P, I, P, I, I, I, I, I, I, F, I, I, P, P], I),
         "pkv_paged_mixed_attention": ([P, P, P, I, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P, SZ, P, P, I, P, P],
                                       I),
+        "pkv_paged_mixed_append_attention": ([P, P, P, P, P, P, I, I, I, I, P, P, P, I, P, I, I, I, I, I, F, I, I, P,
+                                              SZ, P, P, I, P, P], I),
         "pkv_mixed_split": ([I, P, I, P, I, I, I, I, I], I),
         "pkv_copy_blocks": ([P, I64, P, I64, P, I, I64, P, P], I),
         "pkv_pool_create": ([I, P], P),
@@ -262,6 +264,43 @@ def paged_mixed_attention(out, q, cu_seqlens, num_prefill, max_q_len, k_cache, v
         _dtype_code(q), _dtype_code(out), _dev(workspace, "workspace"), workspace.numel(), hp(cu_seqlens_host),
         hp(context_lens_host), int(decode_sms), _status_ptr(dev_status), _stream(stream))
     _check("pkv_paged_mixed_attention", st)
+
+
+def paged_mixed_append_attention(out, q, k_new, v_new, slot_mapping, cu_seqlens, num_prefill, max_q_len, k_cache,
+                                 v_cache, block_tables, context_lens, scale=None, workspace=None, cu_seqlens_host=None,
+                                 context_lens_host=None, decode_sms=0, dev_status=None, stream=None):
+    """pkv_paged_mixed_append_attention: the append of k_new/v_new (rows as q;
+    prefill rows by slot_mapping, int64 [prefill tokens]; decode rows at
+    position context_lens - 1) and the mixed step's attention in one call."""
+    import torch
+    L = lib()
+    T, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    S = context_lens.shape[0]
+    num_decode = S - num_prefill
+    if cu_seqlens_host is not None:
+        cu_seqlens_host = np.ascontiguousarray(cu_seqlens_host, dtype=np.int32)
+        prefill_tokens = int(cu_seqlens_host[num_prefill])
+    else:
+        prefill_tokens = T - num_decode
+    if context_lens_host is not None:
+        context_lens_host = np.ascontiguousarray(context_lens_host, dtype=np.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        workspace = torch.empty(max(16, decode_workspace_size(num_decode, Hq, Hkv, d)), dtype=torch.uint8,
+                                device=q.device)
+    hp = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    st = L.pkv_paged_mixed_append_attention(
+        _dev(out, "out", ndim=3), _dev(q, "q", ndim=3), _dev(k_new, "k_new", q.dtype, 3),
+        _dev(v_new, "v_new", q.dtype, 3), _dev(slot_mapping, "slot_mapping", torch.int64, 1),
+        _dev(cu_seqlens, "cu_seqlens", torch.int32, 1), num_prefill, prefill_tokens, int(max_q_len), num_decode,
+        _dev(k_cache, "k_cache", q.dtype, 4), _dev(v_cache, "v_cache", q.dtype, 4),
+        _dev(block_tables, "block_tables", torch.int32, 2), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32, 1), NB, Hq, Hkv, d, bs, float(scale), _dtype_code(q),
+        _dtype_code(out), _dev(workspace, "workspace"), workspace.numel(), hp(cu_seqlens_host),
+        hp(context_lens_host), int(decode_sms), _status_ptr(dev_status), _stream(stream))
+    _check("pkv_paged_mixed_append_attention", st)
 
 
 def copy_blocks(dst, src, pairs, dev_status=None, stream=None):

@@ -95,37 +95,54 @@ extern "C" int pkv_mixed_split(int num_sms, const int32_t *cu_seqlens, int num_p
     return best;
 }
 
-extern "C" int pkv_paged_mixed_attention(void *out, const void *q, const int32_t *cu_seqlens, int num_prefill,
-                                         int prefill_tokens, int max_q_len, int num_decode, const void *k_cache,
-                                         const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
-                                         const int32_t *context_lens, int num_blocks, int num_q_heads,
-                                         int num_kv_heads, int head_dim, int block_size, float scale, int dtype,
-                                         int out_dtype, void *workspace, size_t workspace_bytes,
-                                         const int32_t *cu_seqlens_host, const int32_t *context_lens_host,
-                                         int decode_sms, int *dev_status, void *stream) {
-    pkv::NvtxRange nvtx_range("pkv_paged_mixed_attention");
-    using namespace pkv;
+namespace pkv {
+namespace {
+
+// The mixed step's attention, and with k_new / v_new / slot_mapping given its
+// append too: the prefill chunks' rows by slot mapping ahead of the prefill
+// kernel (on the side stream when decodes run beside it), the decode rows
+// inside the decode kernel.
+int mixed_attention(void *out, const void *q, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                    const int32_t *cu_seqlens, int num_prefill, int prefill_tokens, int max_q_len, int num_decode,
+                    const void *k_cache, const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int num_blocks, int num_q_heads, int num_kv_heads, int head_dim,
+                    int block_size, float scale, int dtype, int out_dtype, void *workspace, size_t workspace_bytes,
+                    const int32_t *cu_seqlens_host, const int32_t *context_lens_host, int decode_sms,
+                    int *dev_status, cudaStream_t st) {
     if (num_prefill < 0 || num_decode < 0 || prefill_tokens < 0 || num_kv_heads <= 0 || num_q_heads <= 0)
         return PKV_ERR_INVALID_ARG;
     if (num_prefill == 0 && num_decode == 0) return PKV_OK;
     if (!out || !q || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+    const bool append = k_new != nullptr;
+    if (append && (!v_new || (num_prefill > 0 && !slot_mapping))) return PKV_ERR_INVALID_ARG;
     const size_t in_row = (size_t)num_q_heads * head_dim * 2;
+    const size_t kv_row = (size_t)num_kv_heads * head_dim * 2;
     const size_t out_row = (size_t)num_q_heads * head_dim * (out_dtype == PKV_DTYPE_F32 ? 4 : 2);
     void *out_d = static_cast<char *>(out) + prefill_tokens * out_row;
     const void *q_d = static_cast<const char *>(q) + prefill_tokens * in_row;
     const int32_t *bt_d = block_tables + (size_t)num_prefill * max_blocks_per_seq;
     const int32_t *cl_d = context_lens + num_prefill;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // one kind of work only: the plain entry points
-    if (num_decode == 0)
+    const void *k_d = append ? static_cast<const char *>(k_new) + prefill_tokens * kv_row : nullptr;
+    const void *v_d = append ? static_cast<const char *>(v_new) + prefill_tokens * kv_row : nullptr;
+    // the prefill part, on stream s: its rows appended first
+    auto prefill = [&](cudaStream_t s) {
+        if (append) {
+            const int rc = pkv_kv_append(k_new, v_new, slot_mapping, prefill_tokens, const_cast<void *>(k_cache),
+                                         const_cast<void *>(v_cache), num_blocks, block_size, num_kv_heads,
+                                         head_dim, dtype, dev_status, s);
+            if (rc != PKV_OK) return rc;
+        }
         return pkv_paged_prefill_attention(out, q, cu_seqlens, num_prefill, max_q_len, prefill_tokens, k_cache,
                                            v_cache, block_tables, max_blocks_per_seq, context_lens, num_blocks,
                                            num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype,
-                                           dev_status, stream);
+                                           dev_status, s);
+    };
+    // one kind of work only: no side stream
+    if (num_decode == 0) return prefill(st);
     if (num_prefill == 0)
         return decode_attention(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                                 num_decode, num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype,
-                                out_dtype, workspace, workspace_bytes, dev_status, st, 0);
+                                out_dtype, workspace, workspace_bytes, dev_status, st, 0, k_new, v_new);
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != PKV_OK) return rc;
@@ -145,18 +162,54 @@ extern "C" int pkv_paged_mixed_attention(void *out, const void *q, const int32_t
     if (e == cudaSuccess) e = cudaStreamWaitEvent(side->stream, side->fork, 0);
     if (e != cudaSuccess) return cuda_fail(e);
     // decode first, so that its persistent CTAs hold their SMs; the prefill
-    // CTAs take the rest and keep cycling through them
+    // CTAs take the rest and keep cycling through them.  The two touch
+    // different sequences' blocks (a shared prefix page is never written).
     rc = decode_attention(out_d, q_d, k_cache, v_cache, bt_d, max_blocks_per_seq, cl_d, num_decode, num_blocks,
                           num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype, out_dtype, workspace,
-                          workspace_bytes, dev_status, st, d_sms);
-    const int rc2 = pkv_paged_prefill_attention(out, q, cu_seqlens, num_prefill, max_q_len, prefill_tokens, k_cache,
-                                                v_cache, block_tables, max_blocks_per_seq, context_lens, num_blocks,
-                                                num_q_heads, num_kv_heads, head_dim, block_size, scale, dtype,
-                                                out_dtype, dev_status, side->stream);
+                          workspace_bytes, dev_status, st, d_sms, k_d, v_d);
+    const int rc2 = prefill(side->stream);
     // join, whatever happened, so the caller's stream never runs ahead of
     // work still queued on the side stream
     e = cudaEventRecord(side->join, side->stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
     if (e != cudaSuccess) return cuda_fail(e);
     return rc != PKV_OK ? rc : rc2;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_paged_mixed_attention(void *out, const void *q, const int32_t *cu_seqlens, int num_prefill,
+                                         int prefill_tokens, int max_q_len, int num_decode, const void *k_cache,
+                                         const void *v_cache, const int32_t *block_tables, int max_blocks_per_seq,
+                                         const int32_t *context_lens, int num_blocks, int num_q_heads,
+                                         int num_kv_heads, int head_dim, int block_size, float scale, int dtype,
+                                         int out_dtype, void *workspace, size_t workspace_bytes,
+                                         const int32_t *cu_seqlens_host, const int32_t *context_lens_host,
+                                         int decode_sms, int *dev_status, void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_paged_mixed_attention");
+    return pkv::mixed_attention(out, q, nullptr, nullptr, nullptr, cu_seqlens, num_prefill, prefill_tokens,
+                                max_q_len, num_decode, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                                dtype, out_dtype, workspace, workspace_bytes, cu_seqlens_host, context_lens_host,
+                                decode_sms, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_mixed_append_attention(void *out, const void *q, const void *k_new, const void *v_new,
+                                                const int64_t *slot_mapping, const int32_t *cu_seqlens,
+                                                int num_prefill, int prefill_tokens, int max_q_len, int num_decode,
+                                                void *k_cache, void *v_cache, const int32_t *block_tables,
+                                                int max_blocks_per_seq, const int32_t *context_lens, int num_blocks,
+                                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                                float scale, int dtype, int out_dtype, void *workspace,
+                                                size_t workspace_bytes, const int32_t *cu_seqlens_host,
+                                                const int32_t *context_lens_host, int decode_sms, int *dev_status,
+                                                void *stream) {
+    pkv::NvtxRange nvtx_range("pkv_paged_mixed_append_attention");
+    if (!k_new || !v_new) return PKV_ERR_INVALID_ARG;
+    return pkv::mixed_attention(out, q, k_new, v_new, slot_mapping, cu_seqlens, num_prefill, prefill_tokens,
+                                max_q_len, num_decode, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_blocks, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                                dtype, out_dtype, workspace, workspace_bytes, cu_seqlens_host, context_lens_host,
+                                decode_sms, dev_status, static_cast<cudaStream_t>(stream));
 }

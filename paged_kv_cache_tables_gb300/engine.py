@@ -199,25 +199,12 @@ class PagedEngine:
         for layer in range(self.L):
             cid = layer % self.R
             fill(layer, cid, q, k, v, trids, tpos)
-            if not P:
-                # decode only: row s of k/v is sequence s's new token, at
-                # position ctx - 1 of its table; append fused into the launch
-                rc = L.pkv_paged_decode_append_attention(pout, pq, pk, pv, kc[cid], vc[cid], ptab, MB, pctx, S, NB,
-                                                         Hq, Hkv, d, 16, scale, dt, dt, pwork, nwork, pst, pstream)
-                if rc != B.PKV_OK:
-                    raise B.PkvError("engine step, layer %d" % layer, rc)
-                if on_layer_done is not None:
-                    on_layer_done(layer, info, out)
-                continue
-            rc = L.pkv_kv_append(pk, pv, pslots, T, kc[cid], vc[cid], NB, 16, Hkv, d, dt, pst, pstream)
-            if rc == B.PKV_OK and P and S > P:
-                # prefill chunks and decodes side by side on split SMs
-                rc = L.pkv_paged_mixed_attention(pout, pq, pcu, P, t1, max_q, S - P, kc[cid], vc[cid], ptab, MB, pctx,
-                                                 NB, Hq, Hkv, d, 16, scale, dt, dt, pwork, nwork, hcu, hctx, 0, pst,
-                                                 pstream)
-            elif rc == B.PKV_OK and P:
-                rc = L.pkv_paged_prefill_attention(pout, pq, pcu, P, max_q, t1, kc[cid], vc[cid], ptab, MB, pctx, NB,
-                                                   Hq, Hkv, d, 16, scale, dt, dt, pst, pstream)
+            # the layer's append and attention in one call: prefill chunks
+            # (their rows appended by slot) beside the decodes on split SMs,
+            # each decode's row appended inside the decode kernel
+            rc = L.pkv_paged_mixed_append_attention(pout, pq, pk, pv, pslots, pcu, P, t1, max_q, S - P, kc[cid],
+                                                    vc[cid], ptab, MB, pctx, NB, Hq, Hkv, d, 16, scale, dt, dt, pwork,
+                                                    nwork, hcu, hctx, 0, pst, pstream)
             if rc != B.PKV_OK:
                 raise B.PkvError("engine step, layer %d" % layer, rc)
             if on_layer_done is not None:

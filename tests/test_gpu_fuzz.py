@@ -1,9 +1,10 @@
 """Seeded random steps against the oracle: many small shapes, each a mixed
 step (prefill chunks first, then one-token decodes) with random head counts,
 head sizes, 16-bit types and context lengths (including empty and
-block-boundary ones), run through the plain entry points and the fused and
-side-by-side ones.  Append must be bit-exact and attention within the
-tolerance; every call must leave the status word clear."""
+block-boundary ones), run through the plain entry points, the side-by-side
+one, the fused decode + append one and the one-call mixed step with its
+append.  Append must be bit-exact and attention within the tolerance; every
+call must leave the status word clear."""
 import numpy as np
 import pytest
 import torch
@@ -11,7 +12,8 @@ import torch
 import oracle
 from gpu_helpers import DeviceStep, assert_close, out_to_f64, host_bits
 from paged_kv_cache_tables_gb300 import (kv_append, paged_decode_append_attention, paged_decode_attention,
-                                         paged_mixed_attention, paged_prefill_attention)
+                                         paged_mixed_append_attention, paged_mixed_attention,
+                                         paged_prefill_attention)
 from synth import build_step
 
 pytestmark = pytest.mark.gpu
@@ -95,3 +97,15 @@ def test_random_mixed_steps_match_oracle(cuda_lib, seed):
         assert np.array_equal(host_bits(ds3.k_cache), kc) and np.array_equal(host_bits(ds3.v_cache), vc)
         assert_close(out_to_f64(out3), ref[t1:], st.dtype, what="fuzz %d fused" % seed)
         assert int(ds3.status.item()) == 0
+
+    # 4) the whole step (append included) in one call, on fresh caches
+    ds4 = DeviceStep(st)
+    out4 = torch.full((st.T, st.Hq, st.d), float("nan"), dtype=torch.float32, device="cuda")
+    paged_mixed_append_attention(out4, ds4.q, ds4.k_new, ds4.v_new, ds4.slot_mapping[:t1],
+                                 ds4.cu_seqlens[:p + 1], p, max_q, ds4.k_cache, ds4.v_cache, ds4.block_tables, ds4.context_lens,
+                                 dev_status=ds4.status, cu_seqlens_host=st.cu_seqlens[:p + 1].astype(np.int32),
+                                 context_lens_host=st.context_lens.astype(np.int32))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(ds4.k_cache), kc) and np.array_equal(host_bits(ds4.v_cache), vc)
+    assert_close(out_to_f64(out4), ref, "fp32", what="fuzz %d one call" % seed)
+    assert int(ds4.status.item()) == 0
