@@ -859,6 +859,11 @@ def run_pkv(args):
         "dtype": "bf16", "data": "synthetic",
         "config": step_config(st, ws),
         "attended_tokens_per_s": round(attended * ws / (ms_step * 1e-3), 1),
+        "attended_q_head_tokens_per_s": round(attended * Hq * ws / (ms_step * 1e-3), 1),
+        # bytes the kernel touches: whole 16-token blocks, so the masked tail
+        # of each sequence's last block counts too
+        "touched_bytes_per_step": int(step_bytes + (((st.context_lens + 15) // 16 * 16 - st.context_lens).sum())
+                                      * 2 * Hkv * d * 2),
         "pct_of_8tbs": round(100 * value / 8000.0, 2),
         "kernels_ms": {"paged_decode_append_attention": round(fused_ms, 4)},
         "two_launch_step": {"ms_per_step": round(two_ms, 4), "kv_append_ms": round(app_ms, 4),
