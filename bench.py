@@ -238,50 +238,75 @@ def _oracle_worker(args):
             m.close()
 
 
-def cpu_oracle_all_cores(st, budget_s, one_pass_s):
-    """The oracle on every host core at once: the step's sequences split into
-    equal-work slices, one spawned process each (the caches shared, not
-    copied), the whole step repeated to fill about budget_s.  Wall time of
-    the slowest worker."""
-    import multiprocessing as mp
-    from multiprocessing import shared_memory
-    cores = len(os.sched_getaffinity(0))
-    arrays = [st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens]
-    # shared memory lives in /dev/shm; writing past a small tmpfs there would
-    # kill the process (SIGBUS), so check its room first
-    need = sum(a.nbytes for a in arrays)
-    vfs = os.statvfs("/dev/shm")
-    if vfs.f_bavail * vfs.f_frsize < need * 1.25:
-        raise RuntimeError("/dev/shm has %.1f GB free, %.1f GB needed" % (vfs.f_bavail * vfs.f_frsize / 1e9,
-                                                                          need * 1.25 / 1e9))
-    shms, names, shapes = [], [], []
-    try:
-        for a in arrays:
-            m = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
-            np.ndarray(a.shape, dtype=a.dtype, buffer=m.buf)[...] = a
-            shms.append(m)
-            names.append(m.name)
-            shapes.append((a.shape, a.dtype.str))
-        # slices of about equal attended tokens
-        cum = np.concatenate([[0], np.cumsum(st.context_lens.astype(np.int64))])
-        cuts = [int(np.searchsorted(cum, cum[-1] * k / cores)) for k in range(cores + 1)]
-        cuts[0], cuts[-1] = 0, st.S
-        passes = max(1, int(budget_s / max(one_pass_s / cores, 1e-3)))
-        jobs = [(names, shapes, st.dtype, cuts[k], cuts[k + 1], passes) for k in range(cores) if cuts[k + 1] > cuts[k]]
-        ctx = mp.get_context("spawn")
-        with ctx.Pool(len(jobs)) as pool:
-            t0 = time.perf_counter()
-            times = pool.map(_oracle_worker, jobs)
-            wall = time.perf_counter() - t0
-    finally:
-        for m in shms:
+class OraclePool:
+    """The oracle on every host core: the step's sequences split into slices
+    of about equal attended tokens, one spawned process per slice (spawned,
+    not forked: the parent may hold a CUDA context), the caches in shared
+    memory rather than copied.  run(passes) times `passes` decodes of the
+    whole step, as wall time until the slowest slice is done."""
+
+    def __init__(self, st):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        self.st = st
+        cores = len(os.sched_getaffinity(0))
+        arrays = [st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens]
+        # shared memory lives in /dev/shm; writing past a small tmpfs there
+        # would kill the process (SIGBUS), so check its room first
+        need = sum(a.nbytes for a in arrays)
+        vfs = os.statvfs("/dev/shm")
+        if vfs.f_bavail * vfs.f_frsize < need * 1.25:
+            raise RuntimeError("/dev/shm has %.1f GB free, %.1f GB needed" % (vfs.f_bavail * vfs.f_frsize / 1e9,
+                                                                              need * 1.25 / 1e9))
+        self.shms, names, shapes = [], [], []
+        try:
+            for a in arrays:
+                m = shared_memory.SharedMemory(create=True, size=max(1, a.nbytes))
+                self.shms.append(m)
+                np.ndarray(a.shape, dtype=a.dtype, buffer=m.buf)[...] = a
+                names.append(m.name)
+                shapes.append((a.shape, a.dtype.str))
+            cum = np.concatenate([[0], np.cumsum(st.context_lens.astype(np.int64))])
+            cuts = [int(np.searchsorted(cum, cum[-1] * k / cores)) for k in range(cores + 1)]
+            cuts[0], cuts[-1] = 0, st.S
+            self.slices = [(names, shapes, st.dtype, cuts[k], cuts[k + 1]) for k in range(cores)
+                           if cuts[k + 1] > cuts[k]]
+            self.pool = mp.get_context("spawn").Pool(len(self.slices))
+        except Exception:
+            self.close()
+            raise
+        self.cores = len(self.slices)
+
+    def run(self, passes):
+        t0 = time.perf_counter()
+        times = self.pool.map(_oracle_worker, [sl + (passes,) for sl in self.slices])
+        return time.perf_counter() - t0, max(times)
+
+    def close(self):
+        if getattr(self, "pool", None) is not None:
+            self.pool.close()
+            self.pool.join()
+            self.pool = None
+        for m in self.shms:
             m.close()
             m.unlink()
+        self.shms = []
+
+
+def cpu_oracle_all_cores(st, budget_s, one_pass_s):
+    """cpu_baseline on every host core: OraclePool, the whole step repeated to
+    fill about budget_s."""
+    op = OraclePool(st)
+    try:
+        op.run(1)   # process start and first touch of the shared caches
+        passes = max(1, int(budget_s / max(one_pass_s / op.cores, 1e-3)))
+        wall, slowest = op.run(passes)
+    finally:
+        op.close()
     nbytes = decode_bytes(st.context_lens, st.Hq, st.Hkv, st.d) * passes
-    return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": len(jobs), "kind": "oracle",
-            "sample": "the whole decode step, %d pass%s, split over %d spawned processes (slowest %.2f s of work, "
-                      "%.2f s wall including process start)" % (passes, "" if passes == 1 else "es", len(jobs),
-                                                               max(times), wall)}
+    return {"value": nbytes / wall / 1e9, "unit": "GB/s", "cores": op.cores, "kind": "oracle",
+            "sample": "the whole decode step, %d pass%s, split over %d spawned processes (%.2f s wall, slowest "
+                      "slice %.2f s)" % (passes, "" if passes == 1 else "es", op.cores, wall, slowest)}
 
 
 def step_config(st, ws):
@@ -301,20 +326,36 @@ def run_reference(args):
         return
     from synth import make_step
     st = make_step("llama8b")
-    budget = min(args.ref_budget, 150.0 / (args.steps + args.warmup))
-    k = oracle_sample_size(st, budget)
+    # each step: one decode of the whole step by the oracle on every host
+    # core (a few tenths of a second on a 16-core host); one core if the
+    # host cannot start the worker processes
+    try:
+        op = OraclePool(st)
+    except Exception as e:
+        op, why = None, "%s: %s" % (type(e).__name__, e)
     vals = []
-    for i in range(args.warmup + args.steps):
-        r = cpu_oracle_run(st, k)
-        if i >= args.warmup:
-            vals.append(r)
-    v = statistics.median([r["value"] for r in vals])
-    ms = statistics.median([r["seconds"] for r in vals]) * 1e3
+    try:
+        for i in range(args.warmup + args.steps):
+            if op is not None:
+                wall, _ = op.run(1)
+            else:
+                wall = cpu_oracle_run(st, st.S)["seconds"]
+            if i >= args.warmup:
+                vals.append(wall)
+    finally:
+        if op is not None:
+            op.close()
+    sec = statistics.median(vals)
+    v = decode_bytes(st.context_lens, st.Hq, st.Hkv, st.d) / sec / 1e9
+    cores = op.cores if op is not None else 1
+    sample = ("the whole decode step (%d sequences, %d attended tokens) per step, split over %d spawned processes"
+              % (st.S, int(st.context_lens.sum()), cores) if op is not None else
+              "the whole decode step per step on one core (%s)" % why)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": step_config(st, args.gpus),
-            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": vals[-1]["sample"]},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -970,7 +1011,6 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--ref-budget", type=float, default=8.0, help="seconds of oracle work per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed prefill + decode step")
