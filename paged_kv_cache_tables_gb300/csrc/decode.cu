@@ -471,15 +471,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             // prologue: fill the ring (loads run ahead of the claims; a load
             // of a block that turns out not to be ours is only waited out)
             int issued = 0;
-            int pending = table_entry();
             const int pro = len < STAGES ? len : STAGES;
-            for (; issued < pro; ++issued) {
-                issue(slot_base + issued, pending);
-                if (issued + 1 < len) {
-                    advance_producer();
-                    pending = table_entry();
+            // the ring's first table entries are read by lanes 0..pro-1 at
+            // once (lane l walks a copy of the cursor l blocks ahead), not one
+            // dependent load after another
+            int first_entries = 0;
+            if (lane < pro) {
+                int ls = ps, lnb = p_nb, lh = ph, lj = pj;
+                for (int k = 0; k < lane; ++k) {
+                    if (++lj == lnb) {
+                        lj = 0;
+                        if (++lh == Hkv) {
+                            lh = 0;
+                            ls = next_seq(ls, lnb, nullptr);
+                        }
+                    }
                 }
+                first_entries = __ldg(p.block_tables + (int64_t)ls * p.max_blocks + lj);
             }
+            int pending = 0;
+            for (; issued < pro; ++issued) {
+                issue(slot_base + issued, __shfl_sync(0xffffffffu, first_entries, issued));
+                if (issued + 1 < len) advance_producer();
+            }
+            if (issued < len) pending = table_entry();
 
             uint32_t qa[D / 16][4];
             float acc[D / 16][NT][4];
