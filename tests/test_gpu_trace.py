@@ -167,3 +167,30 @@ def test_prefix_cached_trace_under_memory_pressure(cuda_lib, synth_gpu):
     assert len(res["finish_step"]) == 40 and int(eng.status.item()) == 0
     assert st["preemptions"] > 0 and st["prefix_hit_blocks"] > 0 and st["free_blocks"] == 60
     assert checked >= 10
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,dtype", [(8, 8, 64, "fp16"), (16, 2, 128, "fp16"), (12, 4, 64, "bf16")])
+def test_trace_other_shapes_and_types(cuda_lib, synth_gpu, Hq, Hkv, d, dtype):
+    """The engine loop on other head layouts, head sizes and 16-bit types, under
+    memory pressure with swapping: every sampled row against the oracle."""
+    from paged_kv_cache_tables_gb300 import PREEMPT_SWAP
+    seed = Hq * 100 + d
+    arrival, prompt, eos = make_requests(seed, n=30, rate=6, prompt_mean=150, out_mean=30, pmax=256)
+    eng = PagedEngine(80, num_layers=2, num_caches=2, Hq=Hq, Hkv=Hkv, d=d, dtype=dtype, max_batch=12,
+                      max_num_batched_tokens=384, chunk=96, max_model_len=512,
+                      initial_order=np.random.default_rng(seed).permutation(80), preemption=PREEMPT_SWAP,
+                      swap_blocks=200)
+    rng = np.random.default_rng(seed + 1)
+    res = run_trace(eng, arrival, prompt, eos, max_tokens=512, fill=make_fill(), sample_every=3,
+                    pick=lambda info: pick_rows(info, rng))
+    st = eng.sched.stats()
+    assert len(res["finish_step"]) == 30 and int(eng.status.item()) == 0
+    assert st["free_blocks"] == 80 and st["free_swap_slots"] == 200
+    assert st["preemptions"] > 0 and st["swapped_out_blocks"] > 0
+    checked = 0
+    for rows, vals in res["samples"]:
+        for (row, rid, pos), got in zip(rows, vals.numpy()):
+            ref = layer0_row(rid, pos, Hq, Hkv, d, dtype=dtype)
+            assert_close(got, ref, dtype, what="%d/%d d%d %s rid %d pos %d" % (Hq, Hkv, d, dtype, rid, pos))
+            checked += 1
+    assert checked >= 10
