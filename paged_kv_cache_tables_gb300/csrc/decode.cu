@@ -303,8 +303,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     pdl_wait_primary();
     pdl_launch_dependents();
 
-    if (tid == 0)
-        for (int k = 0; k < 3; ++k) epoch_open(p.ctl + k, p.epoch);
+    // the three counters are opened side by side (one thread each: a load and
+    // a compare-and-swap apiece, not three such round trips in a row)
+    if (tid < 3) epoch_open(p.ctl + tid, p.epoch);
 
     // ---- plan: total blocks, this CTA's warp starts; CTA 0 publishes the
     // per-sequence block offsets that thieves search ----
@@ -846,14 +847,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
         // ---------------- steal the far half of a busy warp's blocks ----------------
         if (n_own == 0) return;   // a warp without a share of its own does not rob others
+        // no share reaches kStealMin blocks (shares differ by at most one
+        // block): no warp can ever be robbed in this call
+        if ((total + nw - 1) / nw < kStealMin) return;
         // nothing left to take: unclaimed work only shrinks, so once one full
-        // scan found no warp worth robbing, none will be again in this call
+        // scan found no warp worth robbing, none will be again in this call.
+        // The drained word and the ready count are read side by side.
         const unsigned long long kDrained = ((unsigned long long)p.epoch << 32) | 1ull;
-        if (ld_relaxed_u64(p.ctl + 3) == kDrained) return;
+        const unsigned long long drained_w = ld_relaxed_u64(p.ctl + 3);
+        unsigned long long rdy = 0ull;
+        if (lane == 0 && !steal_reserved) rdy = ld_acquire_u64(p.ctl + 0);
+        if (drained_w == kDrained) return;
         if (lane == 0 && !steal_reserved) {
             // every CTA has published its words, and the steal budget allows
             // one more piece (each steal can leave two partial records)
-            const unsigned long long rdy = ld_acquire_u64(p.ctl + 0);
             const bool all_ready = (uint32_t)(rdy >> 32) == p.epoch && (uint32_t)rdy >= gridDim.x;
             if (all_ready) {
                 const uint32_t r = epoch_fetch_add(&p.ctl[1], p.epoch, 1);
