@@ -42,8 +42,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # 64-sequence case, valid for the decode source with this SHA-1; reported as
 # null once it changes.
-DECODE_TRAFFIC_RATIO = (327.01 + 3.21) / 325.566140
-DECODE_TRAFFIC_SHA1 = "1a186fa6c22335e2c90712aacd6cbe9e7a4cb793"
+DECODE_TRAFFIC_RATIO = (327.03 + 3.38) / 325.566140
+DECODE_TRAFFIC_SHA1 = "bf76613e03302d02806573c246ad78196dbff36e"
 
 
 def decode_traffic(dbytes):
@@ -981,8 +981,8 @@ def run_pkv(args):
                      "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel with the append fused (split-KV, in-kernel merge), "
                                "bytes %d per launch" % step_bytes,
-                     "traffic_source": "ncu capture of the 64-sequence case (1.014 x algorithmic), scaled by "
-                                       "bytes"},
+                     "traffic_source": "ncu capture of the 64-sequence case (%.4f x algorithmic), scaled by "
+                                       "bytes" % DECODE_TRAFFIC_RATIO},
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4)},
