@@ -42,8 +42,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
 # 64-sequence case, valid for the decode source with this SHA-1; reported as
 # null once it changes.
-DECODE_TRAFFIC_RATIO = (327.03 + 3.38) / 325.566140
-DECODE_TRAFFIC_SHA1 = "bf76613e03302d02806573c246ad78196dbff36e"
+DECODE_TRAFFIC_RATIO = (326.97 + 3.24) / 325.566140
+DECODE_TRAFFIC_SHA1 = "925cb1a75289b5ed3eb47de04b7a8adf1c9bca23"
 
 
 def decode_traffic(dbytes):

@@ -20,7 +20,10 @@
 //    partial record (m, l, acc) per piece on a per-range list; a per-range
 //    counter of finished blocks (tagged with the call's epoch, so the
 //    workspace never needs clearing) tells the warp that finishes the range's
-//    last block to combine the records by log-sum-exp.
+//    last block to combine the records by log-sum-exp.  Each record also
+//    carries (epoch, range) in one 64-bit word, so when the call has taken
+//    few records the merging warp finds its range's records with one
+//    parallel scan of them instead of walking the list a load at a time.
 //  * Each warp runs its own ring of STAGES shared-memory slots.  Lane 0 issues
 //    2-D TMA loads (128-byte swizzle) of the K and V tiles of a block -- the
 //    block id comes from the block table -- and the warp waits on the slot's
@@ -55,6 +58,10 @@ constexpr int kMaxWarpBlocks = 1 << 22;   // range offsets live in 24-bit fields
 // (a chain of dependent loads) is worth.
 constexpr int kMaxPieces = 4;
 constexpr int kMinWarpBlocks = 20;
+// A merge scans the records taken by the call (a few loads per lane, all in
+// flight together) when there are at most this many; otherwise it walks the
+// range's list.
+constexpr int kScanRecords = 512;
 
 struct DecodeParams {
     void *out;
@@ -72,7 +79,8 @@ struct DecodeParams {
     float scale_log2;   // scale * log2(e): scores are kept in base-2 units
     int out_dtype;
     int total_warps;
-    int rec_floats;     // m[G], l[G], acc[G][D], next, first block, padding to 16 B
+    int rec_floats;     // m[G], l[G], acc[G][D], padding, then a 16-byte trailer:
+                        // next, first block, (epoch << 32 | range) as one u64
     int pool_cap, steal_cap;
     uint32_t epoch;     // nonzero, different for every call
     // fused append (null: none): row s of k_new / v_new [S][Hkv][D] is the
@@ -156,6 +164,10 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Shared counters hit by every warp of the grid ((epoch << 32) | count): each
 // CTA first moves a counter left by an earlier call to (epoch, 0) -- only the
 // first such swap succeeds, later ones see this epoch -- and then counts with
@@ -195,26 +207,72 @@ __device__ __forceinline__ int locate_seq(const DecodeParams &p, int64_t x, int 
 // of head hh; then every lane accumulates its D/32 output columns of every
 // head.
 template <typename T, int D, int NT>
-__device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, int lane) {
+__device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, int lane, bool try_scan) {
     constexpr int HP = 8 * NT, PER = D / 32;
     const int G = p.G;
-    const int next_at = 2 * G + G * D;
+    const int next_at = p.rec_floats - 4;
     auto rec_of = [&](uint32_t idx1) { return p.part + (size_t)(idx1 - 1) * p.rec_floats; };
-    // lane k takes the k-th record of the list: (first block, record)
-    uint32_t r = (uint32_t)ld_acquire_u64(p.seg_list + (size_t)s * p.Hkv + h);
     int n = 0;
     int key = INT32_MAX;
     uint32_t mine = 0u;
-    while (r != 0u && n < 32) {
-        const float *rec = rec_of(r);
-        if (lane == n) {
-            key = __float_as_int(__ldcg(rec + next_at + 1));
-            mine = r;
-        }
-        r = __float_as_uint(__ldcg(rec + next_at));
-        ++n;
+    uint32_t rest = 0u;   // pieces past the 32nd (not produced by the usual splits) follow in list order
+    // records taken by the call so far (every piece of this range took its
+    // record before the count that made this warp the merger), read side by
+    // side with the head of the range's list -- in a small step only: a step
+    // that gave every warp a share takes many records, and the count is a
+    // line every SM's atomics hit
+    uint32_t taken = 0xFFFFFFFFu;
+    if (try_scan) {
+        const unsigned long long taken_w = ld_relaxed_u64(p.ctl + 2);
+        if ((uint32_t)(taken_w >> 32) == p.epoch) taken = min((uint32_t)taken_w, (uint32_t)p.pool_cap);
     }
-    const uint32_t rest = r;   // pieces past the 32nd (not produced by the usual splits) follow in list order
+    const uint32_t head = (uint32_t)ld_acquire_u64(p.seg_list + (size_t)s * p.Hkv + h);
+    bool scanned = false;
+    if (taken <= (uint32_t)kScanRecords) {
+        // lane k takes the k-th record tagged (epoch, this range)
+        const unsigned long long want = ((unsigned long long)p.epoch << 32) | (uint32_t)(s * p.Hkv + h);
+        for (uint32_t b0 = 0; b0 < taken; b0 += 8 * 32) {
+            unsigned long long tg[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t i = b0 + u * 32 + lane;
+                tg[u] = i < taken ? ld_relaxed_u64(reinterpret_cast<const unsigned long long *>(
+                                        rec_of(i + 1) + next_at + 2))
+                                  : 0ull;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                unsigned m = __ballot_sync(0xffffffffu, tg[u] == want);
+                while (m != 0u) {
+                    const int src = __ffs(m) - 1;
+                    m &= m - 1;
+                    if (lane == n) mine = b0 + u * 32 + src + 1;
+                    ++n;
+                }
+            }
+        }
+        scanned = n <= 32;
+        if (scanned) {
+            if (lane < n) key = __float_as_int(__ldcg(rec_of(mine) + next_at + 1));
+        } else {
+            n = 0;
+            mine = 0u;
+        }
+    }
+    if (!scanned) {
+        // lane k takes the k-th record of the list: (first block, record)
+        uint32_t r = head;
+        while (r != 0u && n < 32) {
+            const float *rec = rec_of(r);
+            if (lane == n) {
+                key = __float_as_int(__ldcg(rec + next_at + 1));
+                mine = r;
+            }
+            r = __float_as_uint(__ldcg(rec + next_at));
+            ++n;
+        }
+        rest = r;
+    }
     // bitonic sort of the 32 (key, record) pairs by key, ascending
 #pragma unroll
     for (int k = 2; k <= 32; k <<= 1) {
@@ -330,6 +388,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int64_t nw = (total + min_blocks - 1) / min_blocks;
     if (nw > p.total_warps) nw = p.total_warps;
     if (nw < 1) nw = 1;
+    const bool scan_merge = nw < p.total_warps;   // a small step: merges scan the few records
     if (tid < kDecodeWarps) plan_s[tid] = -1;
     __syncthreads();
     int64_t carry = 0;
@@ -579,8 +638,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     const unsigned long long prev =
                         atomicExch(p.seg_list + seg, ((unsigned long long)p.epoch << 32) | ri);
                     const uint32_t nxt = (uint32_t)(prev >> 32) == p.epoch ? (uint32_t)prev : 0u;
-                    rec[2 * G + G * D] = __uint_as_float(nxt);
-                    rec[2 * G + G * D + 1] = __int_as_float(piece_j0);
+                    float *trailer = rec + p.rec_floats - 4;
+                    trailer[0] = __uint_as_float(nxt);
+                    trailer[1] = __int_as_float(piece_j0);
+                    // (epoch, range) in one single-copy-atomic store: a scan
+                    // never sees half of an earlier call's tag
+                    st_relaxed_u64(reinterpret_cast<unsigned long long *>(trailer + 2),
+                                   ((unsigned long long)p.epoch << 32) | (uint32_t)seg);
                     // the pieces of a range often finish together: open the
                     // counter for this call (one compare-and-swap that only
                     // the first opener wins) and count with a plain add, which
@@ -595,7 +659,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 done = __shfl_sync(0xffffffffu, done, 0);
                 if (done == (uint32_t)c_nb) {
                     __syncwarp();
-                    merge_list<T, D, NT>(p, cs, ch, lane);
+                    merge_list<T, D, NT>(p, cs, ch, lane, scan_merge);
                 } else if (done == 0u) {
                     set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
                 }
@@ -960,7 +1024,7 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static int record_floats(int G, int head_dim) { return (2 * G + G * head_dim + 2 + 3) & ~3; }
+static int record_floats(int G, int head_dim) { return ((2 * G + G * head_dim + 3) & ~3) + 4; }
 
 struct DecodeLayout {
     size_t seg_done, seg_list, ranges, ctl, prefix, part, fixed;
