@@ -864,6 +864,83 @@ def run_batching_bench(args):
 
 
 
+def run_llama1b(args):
+    """The Llama-3.2-1B-shaped decode step: 64 sequences, contexts U{128..2048},
+    32 query / 8 KV heads, head_dim 64, 16,384-block pool, append fused, one
+    launch per step.  A step streams about 143 MB of K/V, close to the 129 MB
+    L2, so R = 8 independent instances (own caches, tables, queries and new
+    rows; seeds apart) are stepped in turn: a step's data was last touched
+    eight steps (over 1.1 GB of traffic) earlier."""
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    from synth import SEEDS, make_step
+    torch.cuda.set_device(0)
+    R = 8
+    inst = []
+    for r in range(R):
+        st = make_step("llama1b", seed=SEEDS["llama1b"] + 1000 * (r + 1))
+        inst.append({
+            "st": st, "q": to_dev_bits(st.q, st.dtype), "kn": to_dev_bits(st.k_new, st.dtype),
+            "vn": to_dev_bits(st.v_new, st.dtype), "kc": to_dev_bits(st.k_cache, st.dtype),
+            "vc": to_dev_bits(st.v_cache, st.dtype), "bt": torch.from_numpy(st.block_tables).cuda(),
+            "cl": torch.from_numpy(st.context_lens).cuda(),
+            "out": torch.empty((st.S, st.Hq, st.d), dtype=torch.bfloat16, device="cuda"),
+            "work": torch.empty(pkv.decode_workspace_size(st.S, st.Hq, st.Hkv, st.d), dtype=torch.uint8,
+                                device="cuda"),
+            # the decode bytes of the method plus the new rows read and written
+            "bytes": decode_bytes(st.context_lens, st.Hq, st.Hkv, st.d) + st.T * 2 * st.Hkv * st.d * 2 * 2,
+        })
+    st0 = inst[0]["st"]
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(st0.d)
+
+    def step(k):
+        x = inst[k % R]
+        pkv.paged_decode_append_attention(x["out"], x["q"], x["kn"], x["vn"], x["kc"], x["vc"], x["bt"], x["cl"],
+                                          scale=scale, workspace=x["work"], dev_status=status, stream=stream)
+
+    for k in range(max(args.warmup, R)):
+        step(k)
+    torch.cuda.synchronize()
+    K = args.steps
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for k in range(K):
+            step(k)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d during the benchmark" % int(status.item()))
+    ms = t0.elapsed_time(t1) / K
+    total_bytes = sum(inst[k % R]["bytes"] for k in range(K))
+    attended = sum(float(inst[k % R]["st"].context_lens.sum()) for k in range(K))
+    value = total_bytes / (ms * K * 1e-3) / 1e9
+    peak, peak_kind = load_peaks()
+    ctx_all = np.concatenate([x["st"].context_lens for x in inst])
+    print(json.dumps({
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": K,
+        "warmup": max(args.warmup, R), "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "llama1b-decode", "seqs_per_gpu": st0.S, "q_heads": st0.Hq, "kv_heads": st0.Hkv,
+                   "head_dim": st0.d, "block_size": 16, "pool_blocks": int(st0.k_cache.shape[0]),
+                   "mean_context": round(float(ctx_all.mean()), 1), "instances": R,
+                   "l2": "%d instances stepped in turn, %.2f GB of K/V between two visits of one"
+                         % (R, sum(x["bytes"] for x in inst) / 1e9),
+                   "append": "fused (pkv_paged_decode_append_attention)", "parallelism": "dp1"},
+        "attended_tokens_per_s": round(attended / (ms * K * 1e-3), 1),
+        "pct_of_8tbs": round(100 * value / 8000.0, 2),
+        "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4), "traffic": None, "peak_source": peak_kind,
+                     "kernel": "paged_decode_kernel<bf16, 64, 1> with the append fused, one launch per step"},
+        "gpu_launches": K,
+        "clocks": clk.summary(),
+    }))
+
+
 def run_pkv(args):
     import torch
     import paged_kv_cache_tables_gb300 as pkv
@@ -1021,8 +1098,10 @@ def main():
     ap.add_argument("--only-mixed", action="store_true", help="run only the mixed step (profiling)")
     ap.add_argument("--mixed-decode-sms", default="",
                     help="comma-separated decode SM counts at which to time the side-by-side mixed step too")
-    ap.add_argument("--workload", default="llama8b", choices=["llama8b", "trace", "batching", "prefix", "preempt"],
-                    help="trace: the continuous-batching trace; batching: static vs continuous on one trace; "
+    ap.add_argument("--workload", default="llama8b",
+                    choices=["llama8b", "llama1b", "trace", "batching", "prefix", "preempt"],
+                    help="llama1b: the Llama-3.2-1B-shaped decode step (8 instances in turn); "
+                         "trace: the continuous-batching trace; batching: static vs continuous on one trace; "
                          "prefix: with and without the prefix cache on a sharing-heavy trace; preempt: recompute "
                          "vs swap on the trace with a small pool")
     ap.add_argument("--swap-blocks", type=int, default=0, help="host swap slots for --workload preempt")
@@ -1038,6 +1117,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload == "llama1b":
+        run_llama1b(args)
+        return
     if args.workload == "trace":
         run_trace_bench(args)
         return
