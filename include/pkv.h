@@ -70,6 +70,10 @@ extern "C" {
 #define PKV_DEV_WAIT_TIMEOUT 4  /* a bounded wait for a tile gave up; outputs are invalid */
 #define PKV_DEV_BAD_SLOT 8      /* a slot_mapping entry pointed outside the pool */
 #define PKV_DEV_BAD_CHUNK 16    /* a prefill chunk had q_len > context_len or q_len < 0 */
+#define PKV_DEV_SPLIT 32        /* decode's own bookkeeping failed a self-check: the pieces of a
+                                   split range did not tile it exactly, or the blocks streamed
+                                   differ from the planned total; the affected outputs are wrong.
+                                   Never expected; a library bug if seen. */
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *pkv_status_string(int status);
@@ -154,7 +158,11 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  *   scale          score scale (pass 1/sqrt(head_dim) for the standard one)
  *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 16-B aligned;
  *                  scratch for split-context partial results, contents on entry
- *                  ignored.  Owned by the caller; must not be used by another
+ *                  ignored: the call first enqueues a small kernel that zeroes
+ *                  the workspace's control region (its first few KB: counters
+ *                  and list heads, about 16 bytes per (sequence, KV head)),
+ *                  and everything else it reads there it wrote earlier in the
+ *                  same call.  Owned by the caller; must not be used by another
  *                  call that may run concurrently.
  *   dev_status     device int or NULL (see conventions)
  * One persistent kernel: every warp starts on an equal share of the
@@ -311,20 +319,28 @@ int pkv_mixed_split(int num_sms, const int32_t *cu_seqlens, int num_prefill, con
  * until the process exits).  It calls no cudaMalloc/cudaFree and no
  * allocating library routine.
  *
- * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS and a shape whose smallest
- *   accepted workspace (see pkv_decode_workspace_size) fits in
- *   PKV_STATIC_SCRATCH_BYTES (every supported head_dim/group size does on a
- *   152-SM GB300; the rest of the array is room for rebalancing); otherwise
- *   PKV_ERR_WORKSPACE is returned before anything is enqueued, and
- *   pkv_last_cuda_error() names the limit.
+ * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS, and the smallest workspace the
+ *   shape accepts must fit in PKV_STATIC_SCRATCH_BYTES.  On a GB300 (152
+ *   SMs, 1216 warps) that smallest workspace is about
+ *       8 * num_seqs * num_kv_heads + 8 * num_seqs + 12 KB
+ *       + 2432 * 4 * (2G + G * head_dim + 8)  bytes,  G = num_q_heads / num_kv_heads,
+ *   so the largest group (G = 16, head_dim 128: 20.3 MB of records) leaves
+ *   room for num_seqs * num_kv_heads up to about 590,000 (every shape with
+ *   num_seqs <= 16384 and num_kv_heads <= 32), and G = 4, head_dim 128
+ *   (5.1 MB of records) up to about 2.4 million.  Anything larger returns
+ *   PKV_ERR_WORKSPACE before anything is enqueued, and pkv_last_cuda_error()
+ *   names the limit.  The rest of the array is room for rebalancing work
+ *   between SMs.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
  * - All calls on a device share the one array, and it keeps the last call's
- *   contents.  The kernels read nothing from it that the same call did not
- *   write first, so nothing needs clearing; but calls that overlap on the GPU
- *   (different streams, or different host threads, without ordering between
- *   them) race on the array and give wrong results.  Serialise them.
+ *   contents.  Each call first zeroes the array's small control region (as
+ *   pkv_paged_decode_attention does with its workspace), and everything else
+ *   it reads there it wrote earlier in the same call, so what an earlier call
+ *   left behind does not matter; but calls that overlap on the GPU (different
+ *   streams, or different host threads, without ordering between them) race
+ *   on the array and give wrong results.  Serialise them.
  * Results equal pkv_paged_decode_attention's for the same inputs.
  */
 #define PKV_STATIC_SCRATCH_BYTES (24u << 20)

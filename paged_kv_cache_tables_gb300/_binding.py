@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_HERE, "libpkv.so")
 
 PKV_OK = 0
 DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
-DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_WAIT_TIMEOUT, DEV_BAD_SLOT, DEV_BAD_CHUNK = 1, 2, 4, 8, 16
+DEV_BAD_BLOCK_ID, DEV_BAD_CONTEXT, DEV_WAIT_TIMEOUT, DEV_BAD_SLOT, DEV_BAD_CHUNK, DEV_SPLIT = 1, 2, 4, 8, 16, 32
 
 _lib = None
 

@@ -17,13 +17,19 @@
 //    swap on the same word, and streams that piece too.  Owner and thief can
 //    never both get a block.
 //  * A (sequence, KV head) range processed in more than one piece leaves one
-//    partial record (m, l, acc) per piece on a per-range list; a per-range
-//    counter of finished blocks (tagged with the call's epoch, so the
-//    workspace never needs clearing) tells the warp that finishes the range's
-//    last block to combine the records by log-sum-exp.  Each record also
-//    carries (epoch, range) in one 64-bit word, so when the call has taken
-//    few records the merging warp finds its range's records with one
-//    parallel scan of them instead of walking the list a load at a time.
+//    partial record (m, l, acc, first block, block count) per piece on a
+//    per-range list; a per-range counter of finished blocks tells the warp
+//    that finishes the range's last block to combine the records by
+//    log-sum-exp.  The counters, list heads and a small registry of the first
+//    records taken (which lets a merge in a small step find its records with
+//    one parallel scan instead of walking the list a load at a time) sit in a
+//    control region at the front of the workspace that a small kernel zeroes
+//    just before every call, so nothing read from the workspace depends on
+//    what the memory held before the call.
+//  * The kernel checks its own bookkeeping: a merge verifies that its pieces
+//    tile the range exactly (no gap, no overlap), and the last CTA to leave
+//    compares the blocks consumed by all warps with the planned total; either
+//    failure sets PKV_DEV_SPLIT in the status word.
 //  * Each warp runs its own ring of STAGES shared-memory slots.  Lane 0 issues
 //    2-D TMA loads (128-byte swizzle) of the K and V tiles of a block -- the
 //    block id comes from the block table -- and the warp waits on the slot's
@@ -36,7 +42,7 @@
 //    rounding residual), so the weights keep ~16 significant bits.
 #include <cuda_runtime.h>
 
-#include <atomic>
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 
@@ -50,7 +56,6 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a tile that has not landed 
 constexpr int kDecodeWarps = 8;
 constexpr int kClaimBatch = 4;      // blocks an owner claims per atomic add
 constexpr int kStealMin = 10;       // unclaimed blocks a warp must hold to be robbed
-constexpr int kMaxWarpBlocks = 1 << 22;   // range offsets live in 24-bit fields
 // A step too small to give every warp a share uses fewer warps, each with at
 // least clamp(ceil(longest range / kMaxPieces), 1, kMinWarpBlocks) blocks:
 // short ranges spread over many warps (a small step is bound by latency, not
@@ -58,20 +63,34 @@ constexpr int kMaxWarpBlocks = 1 << 22;   // range offsets live in 24-bit fields
 // (a chain of dependent loads) is worth.
 constexpr int kMaxPieces = 4;
 constexpr int kMinWarpBlocks = 20;
-// A merge scans the records taken by the call (a few loads per lane, all in
-// flight together) when there are at most this many; otherwise it walks the
-// range's list.
+// A merge scans the registry of the records taken by the call (a few loads
+// per lane, all in flight together) when there are at most this many;
+// otherwise it walks the range's list.
 constexpr int kScanRecords = 512;
+
+// Control words, zeroed before every call (u32 each).
+enum Ctl : int {
+    kCtlReady = 0,      // CTAs that have published their warps' range words
+    kCtlSteals = 1,     // steals reserved
+    kCtlTaken = 2,      // partial records taken
+    kCtlDrained = 3,    // 1 once a full scan found no warp worth robbing
+    kCtlExited = 4,     // CTAs that have finished
+    kCtlConsumed64 = 8, // u64 at words 8-9: blocks streamed by all warps (checked at exit)
+    kCtlBytes = 256,
+};
 
 struct DecodeParams {
     void *out;
     const void *q;
     const int32_t *block_tables;
     const int32_t *context_lens;
-    unsigned long long *seg_done;   // [S * Hkv]: (epoch << 32) | blocks of the range finished
-    unsigned long long *seg_list;   // [S * Hkv]: (epoch << 32) | 1 + first partial record (0: none)
-    unsigned long long *ranges;     // [total_warps]: (tag << 48) | (end << 24) | begin
-    unsigned long long *ctl;        // [0] CTAs ready, [1] steals reserved, [2] records taken, [3] drained
+    // control region (zeroed before the call)
+    uint32_t *ctl;                  // [kCtlBytes / 4]
+    uint32_t *reg;                  // [kScanRecords]: range + 1 of record i + 1 (0: not yet registered)
+    uint32_t *seg_done;             // [S * Hkv]: blocks of the range finished in recorded pieces
+    uint32_t *seg_list;             // [S * Hkv]: 1 + the range's last linked record (0: none)
+    // written by the call before they are read
+    unsigned long long *ranges;     // [total_warps]: (end << 32) | begin, offsets from the warp's range start
     long long *prefix;              // [S + 1]: blocks before sequence s (written by CTA 0)
     float *part;                    // [pool_cap][rec_floats] partial records
     int *dev_status;
@@ -80,9 +99,8 @@ struct DecodeParams {
     int out_dtype;
     int total_warps;
     int rec_floats;     // m[G], l[G], acc[G][D], padding, then a 16-byte trailer:
-                        // next, first block, (epoch << 32 | range) as one u64
+                        // next record, first block, block count, unused
     int pool_cap, steal_cap;
-    uint32_t epoch;     // nonzero, different for every call
     // fused append (null: none): row s of k_new / v_new [S][Hkv][D] is the
     // token at position context_lens[s] - 1 of sequence s
     const void *k_new, *v_new;
@@ -144,18 +162,13 @@ __device__ __forceinline__ int64_t block_scan(int64_t v, int64_t *sh, int64_t *t
 
 __device__ __forceinline__ int64_t range_lo(int64_t w, int64_t total, int64_t nw) { return w * total / nw; }
 
-// ---- range words: (tag << 48) | (end << 24) | begin, offsets from the warp's range start
-__device__ __forceinline__ int rw_begin(unsigned long long w) { return (int)(w & 0xFFFFFFull); }
-__device__ __forceinline__ int rw_end(unsigned long long w) { return (int)((w >> 24) & 0xFFFFFFull); }
-__device__ __forceinline__ uint32_t rw_tag(unsigned long long w) { return (uint32_t)(w >> 48); }
-__device__ __forceinline__ unsigned long long rw_make(uint32_t tag, int b, int e) {
-    return ((unsigned long long)(tag & 0xFFFFu) << 48) | ((unsigned long long)e << 24) | (unsigned long long)b;
-}
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
+// ---- range words: (end << 32) | begin, offsets from the warp's range start.
+// The owner claims from the front with atomic adds on begin; a thief takes
+// from the back with a compare-and-swap of the whole word.
+__device__ __forceinline__ int rw_begin(unsigned long long w) { return (int)(uint32_t)w; }
+__device__ __forceinline__ int rw_end(unsigned long long w) { return (int)(uint32_t)(w >> 32); }
+__device__ __forceinline__ unsigned long long rw_make(int b, int e) {
+    return ((unsigned long long)(uint32_t)e << 32) | (uint32_t)b;
 }
 
 __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
@@ -164,24 +177,16 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
     return v;
 }
 
-__device__ __forceinline__ void st_relaxed_u64(unsigned long long *p, unsigned long long v) {
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
-// Shared counters hit by every warp of the grid ((epoch << 32) | count): each
-// CTA first moves a counter left by an earlier call to (epoch, 0) -- only the
-// first such swap succeeds, later ones see this epoch -- and then counts with
-// plain atomic adds, which do not serialise the way a compare-and-swap loop
-// does under contention.
-__device__ __forceinline__ void epoch_open(unsigned long long *ctr, uint32_t epoch) {
-    const unsigned long long v = ld_relaxed_u64(ctr);
-    if ((uint32_t)(v >> 32) != epoch) atomicCAS(ctr, v, (unsigned long long)epoch << 32);
-}
-
-// Count after adding n to an opened counter (0 if it was not opened).
-__device__ __forceinline__ uint32_t epoch_fetch_add(unsigned long long *ctr, uint32_t epoch, uint32_t n) {
-    const unsigned long long old = atomicAdd(ctr, (unsigned long long)n);
-    return (uint32_t)(old >> 32) == epoch ? (uint32_t)old + n : 0u;
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // The sequence holding flat triple x (the last s with prefix[s] * Hkv <= x,
@@ -200,99 +205,108 @@ __device__ __forceinline__ int locate_seq(const DecodeParams &p, int64_t x, int 
     return lo;
 }
 
-// Log-sum-exp combination of the partial records on the list of (s, h), run
-// by the warp that finished the range's last block.  The records are taken in
-// the order of their first block (not the order they were linked), so a given
-// split always combines to the same bits.  Lane hh folds the (max, sum) pairs
-// of head hh; then every lane accumulates its D/32 output columns of every
-// head.
+// Log-sum-exp combination of the partial records of range (s, h), run by the
+// warp that finished the range's last block.  The records are taken in the
+// order of their first block (not the order they were linked), so a given
+// split always combines to the same bits, and the sorted pieces must tile
+// blocks [0, c_nb) exactly, else PKV_DEV_SPLIT is set.  Lane hh folds the
+// (max, sum) pairs of head hh; then every lane accumulates its D/32 output
+// columns of every head.
 template <typename T, int D, int NT>
-__device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, int lane, bool try_scan) {
+__device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, int c_nb, int lane, bool try_scan) {
     constexpr int HP = 8 * NT, PER = D / 32;
     const int G = p.G;
-    const int next_at = p.rec_floats - 4;
+    const int tr = p.rec_floats - 4;   // trailer: next, first block, block count
+    const uint32_t seg = (uint32_t)s * (uint32_t)p.Hkv + (uint32_t)h;
     auto rec_of = [&](uint32_t idx1) { return p.part + (size_t)(idx1 - 1) * p.rec_floats; };
     int n = 0;
-    int key = INT32_MAX;
     uint32_t mine = 0u;
     uint32_t rest = 0u;   // pieces past the 32nd (not produced by the usual splits) follow in list order
-    // records taken by the call so far (every piece of this range took its
-    // record before the count that made this warp the merger), read side by
-    // side with the head of the range's list -- in a small step only: a step
-    // that gave every warp a share takes many records, and the count is a
-    // line every SM's atomics hit
-    uint32_t taken = 0xFFFFFFFFu;
-    if (try_scan) {
-        const unsigned long long taken_w = ld_relaxed_u64(p.ctl + 2);
-        if ((uint32_t)(taken_w >> 32) == p.epoch) taken = min((uint32_t)taken_w, (uint32_t)p.pool_cap);
-    }
-    const uint32_t head = (uint32_t)ld_acquire_u64(p.seg_list + (size_t)s * p.Hkv + h);
     bool scanned = false;
-    if (taken <= (uint32_t)kScanRecords) {
-        // lane k takes the k-th record tagged (epoch, this range)
-        const unsigned long long want = ((unsigned long long)p.epoch << 32) | (uint32_t)(s * p.Hkv + h);
-        for (uint32_t b0 = 0; b0 < taken; b0 += 8 * 32) {
-            unsigned long long tg[8];
+    if (try_scan) {
+        // every piece of this range registered its record before the count
+        // that made this warp the merger, so the records taken so far hold
+        // them all -- in a small step only: a step that gave every warp a
+        // share takes many records, and the count is a line every SM's
+        // atomics hit
+        const uint32_t taken = min(ld_relaxed_u32(p.ctl + kCtlTaken), (uint32_t)p.pool_cap);
+        if (taken <= (uint32_t)kScanRecords) {
+            for (uint32_t b0 = 0; b0 < taken; b0 += 8 * 32) {
+                uint32_t tg[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t i = b0 + u * 32 + lane;
-                tg[u] = i < taken ? ld_relaxed_u64(reinterpret_cast<const unsigned long long *>(
-                                        rec_of(i + 1) + next_at + 2))
-                                  : 0ull;
-            }
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t i = b0 + u * 32 + lane;
+                    tg[u] = i < taken ? ld_relaxed_u32(p.reg + i) : 0u;
+                }
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                unsigned m = __ballot_sync(0xffffffffu, tg[u] == want);
-                while (m != 0u) {
-                    const int src = __ffs(m) - 1;
-                    m &= m - 1;
-                    if (lane == n) mine = b0 + u * 32 + src + 1;
-                    ++n;
+                for (int u = 0; u < 8; ++u) {
+                    unsigned m = __ballot_sync(0xffffffffu, tg[u] == seg + 1u);
+                    while (m != 0u) {
+                        const int src = __ffs(m) - 1;
+                        m &= m - 1;
+                        if (lane == n) mine = b0 + u * 32 + src + 1;
+                        ++n;
+                    }
                 }
             }
-        }
-        scanned = n <= 32;
-        if (scanned) {
-            if (lane < n) key = __float_as_int(__ldcg(rec_of(mine) + next_at + 1));
-        } else {
-            n = 0;
-            mine = 0u;
+            scanned = n <= 32;
+            if (!scanned) {
+                n = 0;
+                mine = 0u;
+            }
         }
     }
     if (!scanned) {
-        // lane k takes the k-th record of the list: (first block, record)
-        uint32_t r = head;
+        // lane k takes the k-th record of the list
+        uint32_t r = ld_acquire_u32(p.seg_list + seg);
         while (r != 0u && n < 32) {
-            const float *rec = rec_of(r);
-            if (lane == n) {
-                key = __float_as_int(__ldcg(rec + next_at + 1));
-                mine = r;
-            }
-            r = __float_as_uint(__ldcg(rec + next_at));
+            if (lane == n) mine = r;
+            r = __float_as_uint(__ldcg(rec_of(r) + tr));
             ++n;
         }
         rest = r;
     }
-    // bitonic sort of the 32 (key, record) pairs by key, ascending
+    // (first block, block count) of each lane's record, all loads at once
+    int key = INT32_MAX, cnt = 0;
+    if (lane < n) {
+        const float *rec = rec_of(mine);
+        key = __float_as_int(__ldcg(rec + tr + 1));
+        cnt = __float_as_int(__ldcg(rec + tr + 2));
+    }
+    // bitonic sort of the 32 (first block, record, count) triples, ascending
 #pragma unroll
     for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
             const int ok = __shfl_xor_sync(0xffffffffu, key, j);
             const uint32_t om = __shfl_xor_sync(0xffffffffu, mine, j);
+            const int oc = __shfl_xor_sync(0xffffffffu, cnt, j);
             const bool up = (lane & k) == 0;
             const bool lower = (lane & j) == 0;
             const bool take = lower == up ? ok < key : ok > key;
             if (take) {
                 key = ok;
                 mine = om;
+                cnt = oc;
             }
         }
     }
+    // the pieces must tile [0, c_nb): sorted, each starts where the previous
+    // one ended, the first at 0 and the last at the range's end
+    const int pkey = __shfl_up_sync(0xffffffffu, key, 1), pcnt = __shfl_up_sync(0xffffffffu, cnt, 1);
+    bool bad = false;
+    if (lane < n) {
+        bad = cnt <= 0 || (lane == 0 ? key != 0 : (rest == 0u && key != pkey + pcnt));
+        if (lane == n - 1 && rest == 0u) bad |= key + cnt != c_nb;
+    }
+    int counted = cnt;   // with more than 32 pieces only the total is checked
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) counted += __shfl_xor_sync(0xffffffffu, counted, o);
     auto record_k = [&](int k, uint32_t &walk) -> const float * {
         if (k < n) return rec_of(__shfl_sync(0xffffffffu, mine, k));
         const float *rec = rec_of(walk);
-        walk = __float_as_uint(__ldcg(rec + next_at));
+        walk = __float_as_uint(__ldcg(rec + tr));
+        counted += __float_as_int(__ldcg(rec + tr + 2));
         return rec;
     };
     float M = -INFINITY, L = 0.f;
@@ -306,6 +320,8 @@ __device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, 
             M = Mn;
         }
     }
+    if (rest != 0u) bad |= counted != c_nb;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(p.dev_status, PKV_DEV_SPLIT);
     float Mh[HP], invL[HP], o[HP][PER];
 #pragma unroll
     for (int hh = 0; hh < HP; ++hh) {
@@ -355,15 +371,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
-    const uint32_t tag = p.epoch & 0xFFFFu;
 
-    // inputs may come from the previous kernel on the stream (the append)
+    // inputs may come from the previous kernel on the stream (the append, or
+    // the clear of the control region)
     pdl_wait_primary();
     pdl_launch_dependents();
-
-    // the three counters are opened side by side (one thread each: a load and
-    // a compare-and-swap apiece, not three such round trips in a row)
-    if (tid < 3) epoch_open(p.ctl + tid, p.epoch);
 
     // ---- plan: total blocks, this CTA's warp starts; CTA 0 publishes the
     // per-sequence block offsets that thieves search ----
@@ -425,10 +437,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int64_t wg = (int64_t)blockIdx.x * kDecodeWarps + warp;
     const int64_t lo_w = wg < nw ? range_lo(wg, total, nw) : total;
     const int n_own = wg < nw ? (int)(range_lo(wg + 1, total, nw) - lo_w) : 0;
-    if (lane == 0) p.ranges[wg] = rw_make(tag, 0, n_own);
+    if (lane == 0) p.ranges[wg] = rw_make(0, n_own);
     __threadfence();
     __syncthreads();
-    if (tid == 0) epoch_fetch_add(&p.ctl[0], p.epoch, 1);
+    if (tid == 0) atomicAdd(p.ctl + kCtlReady, 1u);
 
     // ---- this warp's ring ----
     uint8_t *wring = ring + warp * STAGES * Sh::STAGE_BYTES;
@@ -454,6 +466,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
     uint32_t slot_base = 0;     // ring slots used by earlier pieces of work (phases continue)
     bool steal_reserved = false;
+    uint32_t warp_blocks = 0;   // blocks this warp has streamed (checked against the plan at exit)
 
     // Work: first the warp's own range (claimed in batches), then stolen pieces.
     int64_t x0 = lo_w;          // flat start of the current work
@@ -564,6 +577,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
             // closes the piece of (cs, ch) that ends with block cj of this warp
             auto finish_piece = [&]() {
+                warp_blocks += (uint32_t)piece_n;
                 float lsum[NT];
 #pragma unroll
                 for (int pn = 0; pn < NT; ++pn) {
@@ -598,10 +612,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 }
                 // one piece of a range: leave (m, l, acc) on the range's list
                 uint32_t ri = 0;
-                if (lane == 0) ri = epoch_fetch_add(&p.ctl[2], p.epoch, 1);
+                if (lane == 0) ri = atomicAdd(p.ctl + kCtlTaken, 1u) + 1u;
                 ri = __shfl_sync(0xffffffffu, ri, 0);
-                if (ri == 0u || (int)ri > p.pool_cap) {
-                    set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+                if ((int64_t)ri > (int64_t)p.pool_cap) {
+                    // cannot happen: steals are budgeted so that the records fit
+                    if (lane == 0) set_status(p.dev_status, PKV_DEV_SPLIT);
                     return;
                 }
                 float *rec = p.part + (size_t)(ri - 1) * p.rec_floats;
@@ -628,40 +643,31 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     }
                 }
                 // publish: every lane's record stores, then lane 0 links the
-                // record and adds the piece's blocks to the range's counter
-                // (a release; the warp that completes the count acquires)
+                // record, registers it and adds the piece's blocks to the
+                // range's counter (a release; the warp that completes the
+                // count acquires)
                 __threadfence();
                 __syncwarp();
-                const size_t seg = (size_t)cs * Hkv + ch;
+                const uint32_t seg = (uint32_t)cs * (uint32_t)Hkv + (uint32_t)ch;
                 uint32_t done = 0;
                 if (lane == 0) {
-                    const unsigned long long prev =
-                        atomicExch(p.seg_list + seg, ((unsigned long long)p.epoch << 32) | ri);
-                    const uint32_t nxt = (uint32_t)(prev >> 32) == p.epoch ? (uint32_t)prev : 0u;
+                    const uint32_t nxt = atomicExch(p.seg_list + seg, ri);
                     float *trailer = rec + p.rec_floats - 4;
                     trailer[0] = __uint_as_float(nxt);
                     trailer[1] = __int_as_float(piece_j0);
-                    // (epoch, range) in one single-copy-atomic store: a scan
-                    // never sees half of an earlier call's tag
-                    st_relaxed_u64(reinterpret_cast<unsigned long long *>(trailer + 2),
-                                   ((unsigned long long)p.epoch << 32) | (uint32_t)seg);
-                    // the pieces of a range often finish together: open the
-                    // counter for this call (one compare-and-swap that only
-                    // the first opener wins) and count with a plain add, which
-                    // does not retry under contention as a swap loop would;
-                    // the fences around the add make it a release for this
-                    // piece's record and an acquire for the others'
+                    trailer[2] = __int_as_float(piece_n);
+                    if (ri <= (uint32_t)kScanRecords) p.reg[ri - 1] = seg + 1u;
                     __threadfence();
-                    epoch_open(p.seg_done + seg, p.epoch);
-                    done = epoch_fetch_add(p.seg_done + seg, p.epoch, (uint32_t)piece_n);
+                    done = atomicAdd(p.seg_done + seg, (uint32_t)piece_n) + (uint32_t)piece_n;
                     __threadfence();
+                    // a count past the range's blocks means a block was
+                    // streamed twice (a merge may already have run short)
+                    if (done > (uint32_t)c_nb) set_status(p.dev_status, PKV_DEV_SPLIT);
                 }
                 done = __shfl_sync(0xffffffffu, done, 0);
                 if (done == (uint32_t)c_nb) {
                     __syncwarp();
-                    merge_list<T, D, NT>(p, cs, ch, lane, scan_merge);
-                } else if (done == 0u) {
-                    set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
+                    merge_list<T, D, NT>(p, cs, ch, c_nb, lane, scan_merge);
                 }
             };
 
@@ -673,7 +679,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     // the batch claimed a batch ago: [b, min(b + batch, e)) is ours
                     const unsigned long long c = __shfl_sync(0xffffffffu, claim, 0);
                     const int b = rw_begin(c), e = rw_end(c);
-                    const int got = rw_tag(c) != tag ? 0 : max(0, min(kClaimBatch, e - b));
+                    const int got = max(0, min(kClaimBatch, e - b));
                     limit += got;
                     more = got == kClaimBatch && b + kClaimBatch < e;
                     if (more && lane == 0) claim = atomicAdd(p.ranges + wg, (unsigned long long)kClaimBatch);
@@ -905,33 +911,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             slot_base += issued;
             if (timed_out) {
                 set_status(p.dev_status, PKV_DEV_WAIT_TIMEOUT);
-                return;
+                break;
             }
         }
 
         // ---------------- steal the far half of a busy warp's blocks ----------------
-        if (n_own == 0) return;   // a warp without a share of its own does not rob others
+        if (n_own == 0) break;   // a warp without a share of its own does not rob others
         // no share reaches kStealMin blocks (shares differ by at most one
         // block): no warp can ever be robbed in this call
-        if ((total + nw - 1) / nw < kStealMin) return;
+        if ((total + nw - 1) / nw < kStealMin) break;
         // nothing left to take: unclaimed work only shrinks, so once one full
         // scan found no warp worth robbing, none will be again in this call.
         // The drained word and the ready count are read side by side.
-        const unsigned long long kDrained = ((unsigned long long)p.epoch << 32) | 1ull;
-        const unsigned long long drained_w = ld_relaxed_u64(p.ctl + 3);
-        unsigned long long rdy = 0ull;
-        if (lane == 0 && !steal_reserved) rdy = ld_acquire_u64(p.ctl + 0);
-        if (drained_w == kDrained) return;
+        const uint32_t drained = ld_relaxed_u32(p.ctl + kCtlDrained);
+        uint32_t rdy = 0u;
+        if (lane == 0 && !steal_reserved) rdy = ld_acquire_u32(p.ctl + kCtlReady);
+        if (drained != 0u) break;
         if (lane == 0 && !steal_reserved) {
             // every CTA has published its words, and the steal budget allows
             // one more piece (each steal can leave two partial records)
-            const bool all_ready = (uint32_t)(rdy >> 32) == p.epoch && (uint32_t)rdy >= gridDim.x;
-            if (all_ready) {
-                const uint32_t r = epoch_fetch_add(&p.ctl[1], p.epoch, 1);
-                steal_reserved = r != 0u && (int)r <= p.steal_cap;
+            if (rdy >= gridDim.x) {
+                const uint32_t r = atomicAdd(p.ctl + kCtlSteals, 1u) + 1u;
+                steal_reserved = (int64_t)r <= (int64_t)p.steal_cap;
             }
         }
-        if (!__shfl_sync(0xffffffffu, steal_reserved ? 1 : 0, 0)) return;
+        // (the other lanes' reads of range words and prefixes below come
+        // after lane 0's acquire of the ready count)
+        __syncwarp();
+        if (!__shfl_sync(0xffffffffu, steal_reserved ? 1 : 0, 0)) break;
         bool got = false;
         for (int attempt = 0; attempt < 8 && !got; ++attempt) {
             // every lane reads its share of the range words, eight at a time
@@ -948,7 +955,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                     const int64_t v = (k0 + u) * 32 + lane;
-                    const int rem = (v < nw && v != wg && rw_tag(w[u]) == tag) ? rw_end(w[u]) - rw_begin(w[u]) : 0;
+                    const int rem = (v < nw && v != wg) ? rw_end(w[u]) - rw_begin(w[u]) : 0;
                     if (rem > best) {
                         best = rem;
                         best_v = v;
@@ -973,14 +980,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             const int picked = __shfl_sync(0xffffffffu, best, pick);
             if (top >= kStealMin && picked >= kStealMin) top_lane = pick;
             if (top < kStealMin) {
-                if (lane == 0) atomicExch(p.ctl + 3, kDrained);
+                if (lane == 0) atomicExch(p.ctl + kCtlDrained, 1u);
                 break;
             }
             int start = 0, take = 0;
             if (lane == top_lane) {
+                // the unclaimed blocks are [begin, end): take the far half
                 take = (best + 1) / 2;
                 start = rw_end(best_w) - take;
-                if (atomicCAS(p.ranges + best_v, best_w, rw_make(tag, rw_begin(best_w), start)) != best_w) take = 0;
+                if (atomicCAS(p.ranges + best_v, best_w, rw_make(rw_begin(best_w), start)) != best_w) take = 0;
             }
             take = __shfl_sync(0xffffffffu, take, top_lane);
             start = __shfl_sync(0xffffffffu, start, top_lane);
@@ -991,17 +999,39 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 len = take;
             }
         }
-        if (!got) return;
+        if (!got) break;
         steal_reserved = false;
         own = false;
         s0 = locate_seq(p, x0, lane);
         off0 = (int)(x0 - __ldcg(p.prefix + s0) * Hkv);
     }
+
+    // ---- exit: every block of the plan must have been streamed exactly once
+    // (the last CTA out compares the warps' counts with the planned total) ----
+    unsigned long long *consumed_ctr = reinterpret_cast<unsigned long long *>(p.ctl + kCtlConsumed64);
+    if (lane == 0 && warp_blocks != 0u) atomicAdd(consumed_ctr, (unsigned long long)warp_blocks);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0 && atomicAdd(p.ctl + kCtlExited, 1u) == gridDim.x - 1) {
+        __threadfence();
+        const unsigned long long consumed = atomicAdd(consumed_ctr, 0ull);
+        if ((int64_t)consumed != total) set_status(p.dev_status, PKV_DEV_SPLIT);
+    }
+}
+
+// Zeroes the decode kernel's control region (n16 16-byte words) before a call.
+// It waits for the previous kernel on the stream (which may be the previous
+// call, still using the region) and lets the decode kernel launch at once.
+__global__ void __launch_bounds__(256) decode_clear_kernel(uint4 *ctl, int n16) {
+    pdl_wait_primary();
+    pdl_launch_dependents();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x)
+        ctl[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 template <typename T, int D, int NT>
 static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
-                         cudaStream_t stream) {
+                         size_t clear_bytes, cudaStream_t stream) {
     using Sh = DecodeShape<D, NT>;
     static unsigned long long attr_set = 0;   // per instantiation and device
     if (!done_on_device(&attr_set)) {
@@ -1010,37 +1040,49 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
         if (e != cudaSuccess) return cuda_fail(e);
         mark_done_on_device(&attr_set);
     }
-    cudaError_t e = launch_pdl(paged_decode_kernel<T, D, NT>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES,
-                               stream, prm, tk, tv);
+    // the control region sits at the front of the workspace
+    const int n16 = (int)(clear_bytes / 16);
+    const int cgrid = std::min(64, (n16 + 255) / 256);
+    cudaError_t e = launch_pdl(decode_clear_kernel, dim3(cgrid), dim3(256), 0, stream,
+                               reinterpret_cast<uint4 *>(prm.ctl), n16);
+    if (e == cudaSuccess)
+        e = launch_pdl(paged_decode_kernel<T, D, NT>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES, stream,
+                       prm, tk, tv);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
 }
 
 // ---- workspace ----------------------------------------------------------------
-// [range counters S*Hkv x 8][range lists S*Hkv x 8][range words, one per warp]
-// [control words][prefix (S+1) x 8][partial records], each part 256-B aligned.
-// A partial record holds G maxima, G sums, G x head_dim accumulators, a link
-// and the piece's first block.
+// Control region, zeroed before every call:
+//   [control words 256 B][record registry kScanRecords x 4]
+//   [range counters S*Hkv x 4][range list heads S*Hkv x 4]
+// then, written by the call before it reads them:
+//   [range words, one per warp x 8][prefix (S+1) x 8][partial records]
+// each part 256-B aligned.  A partial record holds G maxima, G sums,
+// G x head_dim accumulators and a trailer (link, first block, block count).
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 static int record_floats(int G, int head_dim) { return ((2 * G + G * head_dim + 3) & ~3) + 4; }
 
 struct DecodeLayout {
-    size_t seg_done, seg_list, ranges, ctl, prefix, part, fixed;
+    size_t ctl, reg, seg_done, seg_list, clear_bytes, ranges, prefix, part, fixed;
 };
 
 static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
     DecodeLayout L;
     size_t o = 0;
+    L.ctl = o;
+    o += kCtlBytes;
+    L.reg = o;
+    o += align256((size_t)kScanRecords * 4);
     L.seg_done = o;
-    o += align256((size_t)S * Hkv * 8);
+    o += align256((size_t)S * Hkv * 4);
     L.seg_list = o;
-    o += align256((size_t)S * Hkv * 8);
+    o += align256((size_t)S * Hkv * 4);
+    L.clear_bytes = o;
     L.ranges = o;
     o += align256((size_t)total_warps * 8);
-    L.ctl = o;
-    o += 256;
     L.prefix = o;
     o += align256((size_t)(S + 1) * 8);
     L.part = o;
@@ -1052,13 +1094,6 @@ static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
 // per steal; the recommended size allows four steals per warp
 static size_t records_min(int total_warps) { return (size_t)2 * total_warps; }
 static size_t records_recommended(int total_warps) { return (size_t)10 * total_warps; }
-
-static uint32_t next_epoch() {
-    static std::atomic<uint32_t> epoch{0};
-    uint32_t e = ++epoch;
-    if (e == 0) e = ++epoch;
-    return e;
-}
 
 size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
@@ -1120,8 +1155,8 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     if (max_sms > 0 && grid > max_sms) grid = max_sms;
     if (grid < 1) grid = 1;
     const int total_warps = grid * kDecodeWarps;
-    // range offsets are 24-bit fields
-    if (upper / total_warps + 1 >= kMaxWarpBlocks) return PKV_ERR_UNSUPPORTED;
+    // range offsets are 32-bit fields
+    if (upper / total_warps + 1 >= ((int64_t)1 << 30)) return PKV_ERR_UNSUPPORTED;
     const DecodeLayout lay = decode_layout(num_seqs, num_kv_heads, total_warps);
     const size_t rec_bytes = (size_t)record_floats(G, head_dim) * sizeof(float);
     if (workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) return PKV_ERR_WORKSPACE;
@@ -1139,10 +1174,11 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     prm.q = q;
     prm.block_tables = block_tables;
     prm.context_lens = context_lens;
-    prm.seg_done = reinterpret_cast<unsigned long long *>(ws + lay.seg_done);
-    prm.seg_list = reinterpret_cast<unsigned long long *>(ws + lay.seg_list);
+    prm.ctl = reinterpret_cast<uint32_t *>(ws + lay.ctl);
+    prm.reg = reinterpret_cast<uint32_t *>(ws + lay.reg);
+    prm.seg_done = reinterpret_cast<uint32_t *>(ws + lay.seg_done);
+    prm.seg_list = reinterpret_cast<uint32_t *>(ws + lay.seg_list);
     prm.ranges = reinterpret_cast<unsigned long long *>(ws + lay.ranges);
-    prm.ctl = reinterpret_cast<unsigned long long *>(ws + lay.ctl);
     prm.prefix = reinterpret_cast<long long *>(ws + lay.prefix);
     prm.part = reinterpret_cast<float *>(ws + lay.part);
     prm.dev_status = dev_status;
@@ -1162,7 +1198,6 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     // by the contexts alone and the output bits repeat from call to call
     const char *det = std::getenv("PKV_DETERMINISTIC");
     if (det && det[0] == '1') prm.steal_cap = 0;
-    prm.epoch = next_epoch();
     prm.k_new = k_new;
     prm.v_new = v_new;
     prm.k_cache = const_cast<void *>(k_cache);
@@ -1171,16 +1206,16 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     const bool wide = G > 8;
     if (dtype == PKV_DTYPE_BF16) {
         if (head_dim == 128)
-            return wide ? launch_decode<__nv_bfloat16, 128, 2>(prm, tk, tv, grid, st)
-                        : launch_decode<__nv_bfloat16, 128, 1>(prm, tk, tv, grid, st);
-        return wide ? launch_decode<__nv_bfloat16, 64, 2>(prm, tk, tv, grid, st)
-                    : launch_decode<__nv_bfloat16, 64, 1>(prm, tk, tv, grid, st);
+            return wide ? launch_decode<__nv_bfloat16, 128, 2>(prm, tk, tv, grid, lay.clear_bytes, st)
+                        : launch_decode<__nv_bfloat16, 128, 1>(prm, tk, tv, grid, lay.clear_bytes, st);
+        return wide ? launch_decode<__nv_bfloat16, 64, 2>(prm, tk, tv, grid, lay.clear_bytes, st)
+                    : launch_decode<__nv_bfloat16, 64, 1>(prm, tk, tv, grid, lay.clear_bytes, st);
     }
     if (head_dim == 128)
-        return wide ? launch_decode<__half, 128, 2>(prm, tk, tv, grid, st)
-                    : launch_decode<__half, 128, 1>(prm, tk, tv, grid, st);
-    return wide ? launch_decode<__half, 64, 2>(prm, tk, tv, grid, st)
-                : launch_decode<__half, 64, 1>(prm, tk, tv, grid, st);
+        return wide ? launch_decode<__half, 128, 2>(prm, tk, tv, grid, lay.clear_bytes, st)
+                    : launch_decode<__half, 128, 1>(prm, tk, tv, grid, lay.clear_bytes, st);
+    return wide ? launch_decode<__half, 64, 2>(prm, tk, tv, grid, lay.clear_bytes, st)
+                : launch_decode<__half, 64, 1>(prm, tk, tv, grid, lay.clear_bytes, st);
 }
 
 }  // namespace pkv

@@ -6,6 +6,9 @@ Tolerance (from the 2e-3 max-abs target on fp32-accumulated outputs):
   * 16-bit output: |gpu - oracle| <= max(2e-3, ulp(oracle)/2 + 1e-4), because a
     correctly rounded bf16 value near 1 is already 2^-8 = 3.9e-3 away at worst.
 """
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -76,3 +79,24 @@ class DeviceStep:
         self.context_lens = dev(st.context_lens)
         self.cu_seqlens = dev(st.cu_seqlens)
         self.status = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def oracle_decode_all(q, k_cache, v_cache, block_tables, context_lens, dtype, scale=None):
+    """oracle.decode over every sequence of a step, the sequences split into
+    slices of about equal attended tokens run side by side on host threads
+    (the oracle's C loops run outside the GIL).  The oracle itself is
+    unchanged: each slice is one plain call."""
+    S = q.shape[0]
+    threads = max(1, min(len(os.sched_getaffinity(0)), 16, S))
+    cum = np.concatenate([[0], np.cumsum(np.asarray(context_lens, np.int64))])
+    cuts = sorted(set([0, S] + [int(np.searchsorted(cum, cum[-1] * k / threads)) for k in range(1, threads)]))
+    out = np.empty((S,) + q.shape[1:], np.float64)
+
+    def run(lo_hi):
+        lo, hi = lo_hi
+        out[lo:hi] = oracle.decode(q[lo:hi], k_cache, v_cache, block_tables[lo:hi], context_lens[lo:hi], dtype,
+                                   scale=scale)
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, [(cuts[i], cuts[i + 1]) for i in range(len(cuts) - 1) if cuts[i + 1] > cuts[i]]))
+    return out

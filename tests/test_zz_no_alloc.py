@@ -5,9 +5,12 @@ their path).  It runs on a scratch array the library keeps in device global
 memory instead of a caller workspace.
 
 Called through the C ABI and compared with pkv_paged_decode_attention (which
-takes a caller workspace) on two calls in a row: a Llama-3.2-1B-shaped step,
-then a Llama-3-8B-shaped one, so the second call runs on scratch the first one
-left behind.  Collected last on purpose.
+takes a caller workspace): a Llama-3.2-1B-shaped step, then a Llama-3-8B-shaped
+one, so the later calls run on scratch an earlier call of another shape left
+behind.  With the split fixed the two entry points agree bit for bit; with
+work stealing, within rounding, on two calls in a row that change neither
+torch's allocation count nor the device's free memory.  Collected last on
+purpose.
 """
 import ctypes
 import math
@@ -34,22 +37,41 @@ def call_static(L, out, q, ds, dev_status):
 
 
 @pytest.mark.parametrize("calls", [[("llama1b", {"S": 64}), ("llama8b", {"S": 128, "NB": 16384})]])
-def test_static_scratch_decode_matches_workspace_decode(cuda_lib, calls):
+def test_static_scratch_decode_matches_workspace_decode(cuda_lib, calls, monkeypatch):
     L = cuda_lib
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for name, kw in calls:
         st = make_step(name, **kw)
         ds = DeviceStep(st)
-        ref = torch.empty((st.S, st.Hq, st.d), dtype=torch.float32, device="cuda")
-        paged_decode_attention(ref, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, ds.context_lens - 1)
         ds.context_lens -= 1          # attend the stored prior context
+        # with the split fixed (no work stealing) both entry points split
+        # every range the same way, so the bits must agree exactly
+        monkeypatch.setenv("PKV_DETERMINISTIC", "1")
+        ref = torch.empty((st.S, st.Hq, st.d), dtype=torch.float32, device="cuda")
+        paged_decode_attention(ref, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, ds.context_lens)
         out = torch.full_like(ref, float("nan"))
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
         rc = call_static(L, out, ds.q, ds, status)
         assert rc == 0, L.pkv_status_string(rc)
         torch.cuda.synchronize()
+        assert torch.equal(out, ref), "%s: fixed-split static decode differs from the workspace decode" % name
+        monkeypatch.delenv("PKV_DETERMINISTIC")
+        # the default (work-stealing) launch, twice in a row on the same
+        # scratch: equal up to the rounding of the split, and nothing is
+        # allocated -- neither through torch's allocator nor on the device
+        torch.cuda.synchronize()
+        alloc0 = torch.cuda.memory_allocated()
+        free0, _ = torch.cuda.mem_get_info()
+        for _ in range(2):
+            out.fill_(float("nan"))
+            rc = call_static(L, out, ds.q, ds, status)
+            assert rc == 0, L.pkv_status_string(rc)
+            torch.cuda.synchronize()
+            diff = (out - ref).abs().nan_to_num(1e9).max().item()
+            assert diff <= ATOL, "%s: static-scratch decode differs by %g" % (name, diff)
+        free1, _ = torch.cuda.mem_get_info()
+        assert torch.cuda.memory_allocated() == alloc0
+        assert free1 == free0, "%s: device free memory changed by %d bytes" % (name, free0 - free1)
         assert int(status.item()) == 0
-        diff = (out - ref).abs().max().item()
-        assert diff <= ATOL, "%s: static-scratch decode differs by %g" % (name, diff)
 
 
 def test_static_scratch_rejects_too_many_sequences(cuda_lib):
