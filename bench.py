@@ -3,8 +3,10 @@ workload (256 sequences, 32 query / 8 KV heads, head_dim 128, 16-token blocks,
 lognormal contexts with median 1024 clipped to 32..8192, bf16, 64k-block pool).
 
 A step = append of the 256 new tokens' K/V, then paged decode attention over
-every sequence's whole context, in one launch (the append fused into the
-split-KV decode kernel; the same step as two launches is timed beside it).
+every sequence's whole context, in one call: a small kernel that zeroes the
+call's control region of the workspace, then the split-KV decode kernel with
+the append fused in (the same step as separate append and decode calls is
+timed beside it).
 Prints ONE JSON line (rank 0).  `--impl reference` times the FP64 CPU oracle
 on a bounded sample of the same workload instead.
 
@@ -38,21 +40,33 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
     return kv + S * Hq * d * esize * 2 + int(((ctx + bs - 1) // bs).sum()) * 4 + 4 * S
 
 
-# DRAM traffic per algorithmic byte of the decode kernel with the append fused,
-# from an ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# 64-sequence case, valid for the decode source with this SHA-1; reported as
-# null once it changes.
-DECODE_TRAFFIC_RATIO = (326.97 + 3.24) / 325.566140
-DECODE_TRAFFIC_SHA1 = "925cb1a75289b5ed3eb47de04b7a8adf1c9bca23"
+# DRAM traffic of one full-size decode launch (the default 256-sequence step,
+# append fused): dram__bytes_read.sum + dram__bytes_write.sum from one ncu
+# capture of that launch, valid for the decode source with this SHA-1 and
+# reported as null once it changes (or for another workload).
+DECODE_TRAFFIC_BYTES = 1453946880 + 5271808
+DECODE_TRAFFIC_SHA1 = "fa48b5f6666f7bd61352c46c00b093ca33bf5088"
 
 
-def decode_traffic(dbytes):
+# launches per decode call: the control-region clear and the decode kernel
+LAUNCHES_PER_DECODE_CALL = 2
+
+
+def clear_bytes(S, Hkv):
+    """Bytes a decode call zeroes before its kernel: control words (256),
+    record registry (2048), per-range counters and list heads (4 B each,
+    each array 256-B aligned)."""
+    a = lambda x: (x + 255) // 256 * 256
+    return 256 + 2048 + 2 * a(4 * S * Hkv)
+
+
+def decode_traffic(default_workload):
     import hashlib
     src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "paged_kv_cache_tables_gb300", "csrc", "decode.cu")
     with open(src, "rb") as f:
         if hashlib.sha1(f.read()).hexdigest() != DECODE_TRAFFIC_SHA1:
             return None
-    return int(round(dbytes * DECODE_TRAFFIC_RATIO))
+    return DECODE_TRAFFIC_BYTES if default_workload else None
 
 
 def load_peaks():
@@ -935,8 +949,9 @@ def run_llama1b(args):
         "pct_of_8tbs": round(100 * value / 8000.0, 2),
         "roofline": {"bound": "hbm", "achieved": round(value, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(value / peak, 4), "traffic": None, "peak_source": peak_kind,
-                     "kernel": "paged_decode_kernel<bf16, 64, 1> with the append fused, one launch per step"},
-        "gpu_launches": K,
+                     "kernel": "paged_decode_kernel<bf16, 64, 1> with the append fused, one call (control-region "
+                               "clear + decode kernel) per step"},
+        "gpu_launches": LAUNCHES_PER_DECODE_CALL * K,
         "clocks": clk.summary(),
     }))
 
@@ -992,8 +1007,10 @@ def run_pkv(args):
     barrier(ws)
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), ws)
     ms_step = total_ms / K
-    # one launch per step and nothing else in the region: the kernel's
-    # average duration is the region's time over K (gaps included)
+    # one call per step and nothing else in the region: the call's two
+    # launches (control-region clear, then the decode kernel) average the
+    # region's time over K, gaps included -- the decode kernel's own time is
+    # at most this
     fused_ms = t_start.elapsed_time(t_end) / K
     if int(status.item()) != 0:
         raise RuntimeError("device status %d during the benchmark" % int(status.item()))
@@ -1049,21 +1066,22 @@ def run_pkv(args):
         "touched_bytes_per_step": int(step_bytes + (((st.context_lens + 15) // 16 * 16 - st.context_lens).sum())
                                       * 2 * Hkv * d * 2),
         "pct_of_8tbs": round(100 * value / 8000.0, 2),
-        "kernels_ms": {"paged_decode_append_attention": round(fused_ms, 4)},
+        "kernels_ms": {"paged_decode_append_attention (clear + decode kernels)": round(fused_ms, 4)},
         "two_launch_step": {"ms_per_step": round(two_ms, 4), "kv_append_ms": round(app_ms, 4),
                             "paged_decode_attention_ms": round(dec_ms, 4), "steps": K2,
                             "decode_gbs": round(dbytes / (dec_ms * 1e-3) / 1e9, 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": decode_traffic(step_bytes),
+                     "frac": round(achieved / peak, 4), "traffic": decode_traffic(not (args.seqs or args.pool)),
                      "peak_source": peak_kind,
                      "kernel": "paged_decode_kernel with the append fused (split-KV, in-kernel merge), "
-                               "bytes %d per launch" % step_bytes,
-                     "traffic_source": "ncu capture of the 64-sequence case (%.4f x algorithmic), scaled by "
-                                       "bytes" % DECODE_TRAFFIC_RATIO},
+                               "bytes %d per launch; timed together with the control-region clear launched "
+                               "before it (%d bytes zeroed)" % (step_bytes, clear_bytes(S, Hkv)),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum of one full-size "
+                                       "launch of this decode source (profiles/paged_decode_llama8b_launches.md)"},
         "e2e": None if e2e_value is None else {
             "value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": K,
+        "gpu_launches": LAUNCHES_PER_DECODE_CALL * K,
         "clocks": clk.summary(),
     }
     if not args.no_mixed:
