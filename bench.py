@@ -707,13 +707,15 @@ def trace_line(args, n, NB, policy="continuous", outputs="geometric", shared=Fal
     dev_s = res["stream_ms"] / 1e3
     # oracle check of the sampled layer-0 rows, and the oracle's own time on them
     import oracle
-    from oracle.trace_check import layer0_row
+    from oracle.trace_check import layer0_inputs
     worst, checked, t_or, keys = 0.0, 0, 0.0, 0
     for rows, vals in res["samples"]:
         for (row, rid, pos), got in zip(rows, vals.numpy()):
+            inputs = layer0_inputs(rid, pos, Hq, Hkv, d, keys=None if row_keys is None else
+                                   (lambda ps, r=rid: row_keys(np.full(len(ps), r), ps)))
+            # the oracle's attention alone is timed (not the regeneration of its inputs)
             t0 = time.perf_counter()
-            ref = layer0_row(rid, pos, Hq, Hkv, d, keys=None if row_keys is None else
-                             (lambda ps, r=rid: row_keys(np.full(len(ps), r), ps)))
+            ref = oracle.decode(*inputs, "bf16")[0]
             t_or += time.perf_counter() - t0
             keys += pos + 1
             err = np.abs(got.astype(np.float64) - ref)
@@ -878,10 +880,10 @@ def run_batching_bench(args):
 
 
 
-def run_llama1b(args):
+def llama1b_line(args, K, with_cpu=True):
     """The Llama-3.2-1B-shaped decode step: 64 sequences, contexts U{128..2048},
     32 query / 8 KV heads, head_dim 64, 16,384-block pool, append fused, one
-    launch per step.  A step streams about 143 MB of K/V, close to the 129 MB
+    call per step.  A step streams about 143 MB of K/V, close to the 129 MB
     L2, so R = 8 independent instances (own caches, tables, queries and new
     rows; seeds apart) are stepped in turn: a step's data was last touched
     eight steps (over 1.1 GB of traffic) earlier."""
@@ -914,10 +916,10 @@ def run_llama1b(args):
         pkv.paged_decode_append_attention(x["out"], x["q"], x["kn"], x["vn"], x["kc"], x["vc"], x["bt"], x["cl"],
                                           scale=scale, workspace=x["work"], dev_status=status, stream=stream)
 
-    for k in range(max(args.warmup, R)):
+    warm = max(args.warmup, R)
+    for k in range(warm):
         step(k)
     torch.cuda.synchronize()
-    K = args.steps
     with ClockSampler(0) as clk:
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -935,10 +937,9 @@ def run_llama1b(args):
     value = total_bytes / (ms * K * 1e-3) / 1e9
     peak, peak_kind = load_peaks()
     ctx_all = np.concatenate([x["st"].context_lens for x in inst])
-    print(json.dumps({
-        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": K,
-        "warmup": max(args.warmup, R), "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "steps": K, "warmup": warm,
+        "ms_per_step": round(ms, 4),
         "config": {"workload": "llama1b-decode", "seqs_per_gpu": st0.S, "q_heads": st0.Hq, "kv_heads": st0.Hkv,
                    "head_dim": st0.d, "block_size": 16, "pool_blocks": int(st0.k_cache.shape[0]),
                    "mean_context": round(float(ctx_all.mean()), 1), "instances": R,
@@ -953,7 +954,106 @@ def run_llama1b(args):
                                "clear + decode kernel) per step"},
         "gpu_launches": LAUNCHES_PER_DECODE_CALL * K,
         "clocks": clk.summary(),
-    }))
+    }
+    if with_cpu:
+        cb = cpu_oracle_run(st0, st0.S, min_seconds=min(args.cpu_budget, 4.0))
+        cb.pop("seconds")
+        line["cpu_baseline"] = cb
+    return line
+
+
+def run_llama1b(args):
+    line = llama1b_line(args, args.steps)
+    out = {"metric": METRIC, "value": line["value"], "unit": "GB/s", "n_gpus": 1, "steps": line["steps"],
+           "warmup": line["warmup"], "ms_per_step": line["ms_per_step"], "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"}
+    out.update({k: v for k, v in line.items() if k not in out})
+    print(json.dumps(out))
+
+
+def tiny_line(args, K=1000):
+    """The tiny correctness step (2 sequences, contexts 18 and 15 after the
+    append, 4/4 heads, head_dim 64, fp16): append fused into decode, K calls
+    back to back.  Launch-bound; reported for completeness, with the oracle's
+    time on the same step."""
+    import torch
+    import paged_kv_cache_tables_gb300 as pkv
+    from synth import make_step
+    import oracle
+    st = make_step("tiny")
+    dv = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.float16).cuda()
+    q, kn, vn, kc, vc = dv(st.q), dv(st.k_new), dv(st.v_new), dv(st.k_cache), dv(st.v_cache)
+    bt = torch.from_numpy(st.block_tables).cuda()
+    cl = torch.from_numpy(st.context_lens).cuda()
+    out = torch.empty((st.S, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    work = torch.empty(pkv.decode_workspace_size(st.S, st.Hq, st.Hkv, st.d), dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    step = lambda: pkv.paged_decode_append_attention(out, q, kn, vn, kc, vc, bt, cl, workspace=work,
+                                                     dev_status=status, stream=stream)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status %d in the tiny step" % int(status.item()))
+    ms = a.elapsed_time(b) / K
+    k_ref, v_ref = st.k_cache.copy(), st.v_cache.copy()
+    oracle.append(st.k_new, st.v_new, st.slot_mapping, k_ref, v_ref, st.bs)
+    t0 = time.perf_counter()
+    reps = 0
+    while reps == 0 or time.perf_counter() - t0 < 0.5:
+        ref = oracle.decode(st.q, k_ref, v_ref, st.block_tables, st.context_lens, st.dtype)
+        reps += 1
+    or_ms = (time.perf_counter() - t0) / reps * 1e3
+    err = float(np.abs(out.cpu().numpy().astype(np.float64) - ref).max())
+    nbytes = decode_bytes(st.context_lens, st.Hq, st.Hkv, st.d) + st.T * 2 * st.Hkv * st.d * 2 * 2
+    return {"workload": "tiny: 2 sequences, contexts 18 and 15 after the append, 4/4 heads, d 64, fp16, "
+                        "64-block pool", "steps": K, "ms_per_step": round(ms, 5),
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "note": "launch-bound (one call: control-region clear + decode kernel); a correctness config",
+            "max_abs_err_fp32_out": err, "gpu_launches": LAUNCHES_PER_DECODE_CALL * K,
+            "cpu_baseline": {"value": round(nbytes / (or_ms * 1e-3) / 1e9, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": "the whole step, %d passes, %.3f ms each" % (reps, or_ms)}}
+
+
+def trace_summary(args, n, NB, big_steps_only=True):
+    """The trace line condensed for the default bench line, with the oracle's
+    time on the sampled rows extrapolated to every attended key of the trace
+    (one host core) as its CPU baseline.  The roofline is taken over the steps
+    whose per-layer working set exceeds 4 x L2, or (big_steps_only False, for a
+    pool too small to hold such a step) over every step."""
+    t = trace_line(args, n, NB)
+    oc = t["oracle_check"]
+    keys_total = t["attended_tokens_per_s"] * t["wall_s"]
+    keep = ["workload", "engine_steps", "wall_s", "stream_s", "device_s", "output_tokens_per_s",
+            "attended_tokens_per_s", "kv_gbs", "kv_gbs_device", "kv_gbs_steps_over_4x_l2", "preemptions",
+            "preemption_rate", "avg_running_batch", "latency_steps_p50", "latency_steps_p99", "ttft_ms_mean",
+            "host_ms_per_step", "oracle_check", "clocks"]
+    out = {k: t[k] for k in keep}
+    peak, peak_kind = load_peaks()
+    if big_steps_only:
+        big = t["kv_gbs_steps_over_4x_l2"]["gbs"]
+        what = ("all launches of the steps whose per-layer working set exceeds 4 x L2 (append, prefill and decode "
+                "of every layer), KV bytes over their device time")
+    else:
+        big = t["kv_gbs_device"]
+        what = ("all launches of every step (append, prefill and decode of every layer), KV bytes over device "
+                "time; the pool caps a layer's working set near 3 x L2, so some bytes may come from L2")
+    out["roofline"] = {"bound": "hbm", "achieved": big, "peak": peak, "unit": "GB/s", "frac": round(big / peak, 4),
+                       "traffic": None, "peak_source": peak_kind, "kernel": what}
+    out["cpu_baseline"] = {"value": round(oc["oracle_keys_per_s"], 1), "unit": "attended tokens/s (per query head "
+                           "group, one layer)", "cores": 1, "kind": "oracle",
+                           "sample": "%d sampled layer-0 rows, %.2f s; the whole trace (%.3g attended keys x %d "
+                                     "layers) would take ~%.0f s on one core (extrapolated)"
+                                     % (oc["rows"], oc["oracle_s"], keys_total / args.trace_layers,
+                                        args.trace_layers, keys_total / max(oc["oracle_keys_per_s"], 1e-9))}
+    return out
 
 
 def run_pkv(args):
@@ -1086,6 +1186,13 @@ def run_pkv(args):
     }
     if not args.no_mixed:
         line["mixed_step"] = run_mixed(args)
+    if not args.no_more_configs and ws == 1:
+        # the other configurations of the workload family, each with its
+        # own roofline fraction and oracle baseline
+        line["llama1b_step"] = llama1b_line(args, min(K, 1000))
+        line["trace"] = trace_summary(args, args.trace_requests, args.trace_pool)
+        line["trace_small_pool"] = trace_summary(args, args.trace_requests, 6250, big_steps_only=False)
+        line["tiny_step"] = tiny_line(args)
     if not args.no_cpu_baseline and ws == 1:
         k = oracle_sample_size(st, args.cpu_budget)
         cb = cpu_oracle_run(st, k, min_seconds=args.cpu_budget)
@@ -1109,6 +1216,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-mixed", action="store_true", help="skip the mixed prefill + decode step")
+    ap.add_argument("--no-more-configs", action="store_true",
+                    help="skip the 1B-shaped step and the two traces in the default line")
     ap.add_argument("--mixed-steps", type=int, default=50)
     ap.add_argument("--mixed-chunks", type=int, default=0, help="override the prefill chunk count (profiling)")
     ap.add_argument("--mixed-prior", type=int, default=-1,

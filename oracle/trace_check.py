@@ -14,9 +14,11 @@ from synth.trace import kv_tag, q_tag, token_rows
 from . import decode
 
 
-def layer0_row(rid, pos, Hq, Hkv, d, dtype="bf16", keys=None):
-    """keys(positions) -> the row keys of the request's tokens (default: the
-    request id; a shared prompt head uses its group's key)."""
+def layer0_inputs(rid, pos, Hq, Hkv, d, dtype="bf16", keys=None):
+    """The oracle's inputs for one sampled row: (q, k_cache, v_cache,
+    block_table, context_len) of that row alone, its layer-0 K/V rebuilt from
+    the generator.  keys(positions) -> the row keys of the request's tokens
+    (default: the request id; a shared prompt head uses its group's key)."""
     n = pos + 1
     nb = -(-n // 16)
     kk = np.full(n, rid) if keys is None else keys(np.arange(n))
@@ -29,4 +31,9 @@ def layer0_row(rid, pos, Hq, Hkv, d, dtype="bf16", keys=None):
     vc = vc.reshape(nb, 16, Hkv, d).transpose(0, 2, 1, 3).copy()
     qk = np.array([rid]) if keys is None else keys(np.array([pos]))
     q = token_rows(qk, np.array([pos]), q_tag(0), Hq * d, dtype).reshape(1, Hq, d)
-    return decode(q, kc, vc, np.arange(nb, dtype=np.int32)[None], np.array([n], np.int32), dtype)[0]
+    return q, kc, vc, np.arange(nb, dtype=np.int32)[None], np.array([n], np.int32)
+
+
+def layer0_row(rid, pos, Hq, Hkv, d, dtype="bf16", keys=None):
+    """The FP64 oracle's output [Hq, d] for one sampled row."""
+    return decode(*layer0_inputs(rid, pos, Hq, Hkv, d, dtype, keys), dtype)[0]
