@@ -54,10 +54,10 @@ LAUNCHES_PER_DECODE_CALL = 2
 
 def clear_bytes(S, Hkv):
     """Bytes a decode call zeroes before its kernel: control words (256),
-    record registry (2048), per-range counters and list heads (4 B each,
-    each array 256-B aligned)."""
+    per-range counter words (8 B) and list heads (4 B), each array 256-B
+    aligned."""
     a = lambda x: (x + 255) // 256 * 256
-    return 256 + 2048 + 2 * a(4 * S * Hkv)
+    return 256 + a(8 * S * Hkv) + a(4 * S * Hkv)
 
 
 def decode_traffic(default_workload):

@@ -322,15 +322,15 @@ int pkv_mixed_split(int num_sms, const int32_t *cu_seqlens, int num_prefill, con
  * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS, and the smallest workspace the
  *   shape accepts must fit in PKV_STATIC_SCRATCH_BYTES.  On a GB300 (152
  *   SMs, 1216 warps) that smallest workspace is about
- *       8 * num_seqs * num_kv_heads + 8 * num_seqs + 12 KB
- *       + 2432 * 4 * (2G + G * head_dim + 8)  bytes,  G = num_q_heads / num_kv_heads,
- *   so the largest group (G = 16, head_dim 128: 20.3 MB of records) leaves
- *   room for num_seqs * num_kv_heads up to about 590,000 (every shape with
- *   num_seqs <= 16384 and num_kv_heads <= 32), and G = 4, head_dim 128
- *   (5.1 MB of records) up to about 2.4 million.  Anything larger returns
- *   PKV_ERR_WORKSPACE before anything is enqueued, and pkv_last_cuda_error()
- *   names the limit.  The rest of the array is room for rebalancing work
- *   between SMs.
+ *       44 * num_seqs * num_kv_heads + 8 * num_seqs + 10 KB
+ *       + 2432 * 4 * (2G + G * head_dim + 8)  bytes,  G = num_q_heads / num_kv_heads.
+ *   So with num_seqs = 16384 the largest num_kv_heads that fits is 27 for
+ *   head_dim 128 and G = 4 (452,000 (sequence, KV head) pairs), 20 for G = 8,
+ *   and 6 for G = 16 (whose records alone take 20.3 MB); with 256 sequences
+ *   every group size fits with several hundred KV heads.  Anything larger
+ *   returns PKV_ERR_WORKSPACE before anything is enqueued, and
+ *   pkv_last_cuda_error() names the limit.  The rest of the array is room for
+ *   rebalancing work between SMs.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.

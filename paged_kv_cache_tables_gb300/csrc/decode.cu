@@ -17,15 +17,16 @@
 //    swap on the same word, and streams that piece too.  Owner and thief can
 //    never both get a block.
 //  * A (sequence, KV head) range processed in more than one piece leaves one
-//    partial record (m, l, acc, first block, block count) per piece on a
-//    per-range list; a per-range counter of finished blocks tells the warp
-//    that finishes the range's last block to combine the records by
-//    log-sum-exp.  The counters, list heads and a small registry of the first
-//    records taken (which lets a merge in a small step find its records with
-//    one parallel scan instead of walking the list a load at a time) sit in a
-//    control region at the front of the workspace that a small kernel zeroes
-//    just before every call, so nothing read from the workspace depends on
-//    what the memory held before the call.
+//    partial record (m, l, acc) per piece, in records the warp owns, and
+//    registers it in the range's slot array (record, first block, block
+//    count; pieces past the fourth go on a per-range list instead).  A
+//    per-range counter word counts the pieces registered and the blocks
+//    finished; the warp that finishes the range's last block reads the slots
+//    in one round trip and combines the records by log-sum-exp, with the
+//    loads of several records in flight together.  The counters and list
+//    heads sit in a control region at the front of the workspace that a small
+//    kernel zeroes just before every call, so nothing read from the workspace
+//    depends on what the memory held before the call.
 //  * The kernel checks its own bookkeeping: a merge verifies that its pieces
 //    tile the range exactly (no gap, no overlap), and the last CTA to leave
 //    compares the blocks consumed by all warps with the planned total; either
@@ -63,21 +64,25 @@ constexpr int kStealMin = 10;       // unclaimed blocks a warp must hold to be r
 // (a chain of dependent loads) is worth.
 constexpr int kMaxPieces = 4;
 constexpr int kMinWarpBlocks = 20;
-// A merge scans the registry of the records taken by the call (a few loads
-// per lane, all in flight together) when there are at most this many;
-// otherwise it walks the range's list.
-constexpr int kScanRecords = 512;
+// Pieces of a range registered in its slot array; later pieces go on the
+// range's list.  A slot is one u64: record (bits 0-23), first block (24-43),
+// block count (44-63).
+constexpr int kSlots = 4;
+constexpr int kSlotRecBits = 24, kSlotBlkBits = 20;
 
 // Control words, zeroed before every call (u32 each).
 enum Ctl : int {
     kCtlReady = 0,      // CTAs that have published their warps' range words
-    kCtlSteals = 1,     // steals reserved
-    kCtlTaken = 2,      // partial records taken
     kCtlDrained = 3,    // 1 once a full scan found no warp worth robbing
     kCtlExited = 4,     // CTAs that have finished
     kCtlConsumed64 = 8, // u64 at words 8-9: blocks streamed by all warps (checked at exit)
     kCtlBytes = 256,
 };
+
+__device__ __forceinline__ unsigned long long slot_pack(uint32_t rec1, int j0, int n) {
+    return (unsigned long long)rec1 | ((unsigned long long)j0 << kSlotRecBits) |
+           ((unsigned long long)n << (kSlotRecBits + kSlotBlkBits));
+}
 
 struct DecodeParams {
     void *out;
@@ -86,13 +91,13 @@ struct DecodeParams {
     const int32_t *context_lens;
     // control region (zeroed before the call)
     uint32_t *ctl;                  // [kCtlBytes / 4]
-    uint32_t *reg;                  // [kScanRecords]: range + 1 of record i + 1 (0: not yet registered)
-    uint32_t *seg_done;             // [S * Hkv]: blocks of the range finished in recorded pieces
-    uint32_t *seg_list;             // [S * Hkv]: 1 + the range's last linked record (0: none)
+    unsigned long long *seg_cnt;    // [S * Hkv]: (pieces registered << 32) | blocks finished in recorded pieces
+    uint32_t *seg_list;             // [S * Hkv]: 1 + the range's last listed record (0: none)
     // written by the call before they are read
+    unsigned long long *seg_slots;  // [S * Hkv][kSlots]: the first pieces' slot words
     unsigned long long *ranges;     // [total_warps]: (end << 32) | begin, offsets from the warp's range start
     long long *prefix;              // [S + 1]: blocks before sequence s (written by CTA 0)
-    float *part;                    // [pool_cap][rec_floats] partial records
+    float *part;                    // [total_warps * rec_per_warp][rec_floats] partial records
     int *dev_status;
     int S, max_blocks, num_blocks, Hq, Hkv, G;
     float scale_log2;   // scale * log2(e): scores are kept in base-2 units
@@ -100,7 +105,8 @@ struct DecodeParams {
     int total_warps;
     int rec_floats;     // m[G], l[G], acc[G][D], padding, then a 16-byte trailer:
                         // next record, first block, block count, unused
-    int pool_cap, steal_cap;
+    int rec_per_warp;   // records each warp owns (its own range's two, two per steal)
+    int steal;          // 0: no work stealing (the split is fixed by the contexts alone)
     // fused append (null: none): row s of k_new / v_new [S][Hkv][D] is the
     // token at position context_lens[s] - 1 of sequence s
     const void *k_new, *v_new;
@@ -205,59 +211,35 @@ __device__ __forceinline__ int locate_seq(const DecodeParams &p, int64_t x, int 
     return lo;
 }
 
-// Log-sum-exp combination of the partial records of range (s, h), run by the
-// warp that finished the range's last block.  The records are taken in the
-// order of their first block (not the order they were linked), so a given
-// split always combines to the same bits, and the sorted pieces must tile
-// blocks [0, c_nb) exactly, else PKV_DEV_SPLIT is set.  Lane hh folds the
-// (max, sum) pairs of head hh; then every lane accumulates its D/32 output
-// columns of every head.
+// Log-sum-exp combination of the npieces partial records of range (s, h),
+// run by the warp that finished the range's last block.  Lane k takes piece
+// k: the first kSlots come from the range's slot array (one load each, all at
+// once), later ones from its list.  The pieces are taken in the order of
+// their first block (not the order they registered), so a given split always
+// combines to the same bits, and the sorted pieces must tile blocks [0, c_nb)
+// exactly, else PKV_DEV_SPLIT is set.  Lane hh folds the (max, sum) pairs of
+// head hh; then every lane accumulates its D/32 output columns of every head,
+// the loads of several records in flight together.
 template <typename T, int D, int NT>
-__device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, int c_nb, int lane, bool try_scan) {
+__device__ __forceinline__ void merge_range(const DecodeParams &p, int s, int h, int c_nb, int npieces, int lane) {
     constexpr int HP = 8 * NT, PER = D / 32;
+    constexpr uint32_t kFull = 0xffffffffu;
     const int G = p.G;
     const int tr = p.rec_floats - 4;   // trailer: next, first block, block count
     const uint32_t seg = (uint32_t)s * (uint32_t)p.Hkv + (uint32_t)h;
     auto rec_of = [&](uint32_t idx1) { return p.part + (size_t)(idx1 - 1) * p.rec_floats; };
-    int n = 0;
     uint32_t mine = 0u;
-    uint32_t rest = 0u;   // pieces past the 32nd (not produced by the usual splits) follow in list order
-    bool scanned = false;
-    if (try_scan) {
-        // every piece of this range registered its record before the count
-        // that made this warp the merger, so the records taken so far hold
-        // them all -- in a small step only: a step that gave every warp a
-        // share takes many records, and the count is a line every SM's
-        // atomics hit
-        const uint32_t taken = min(ld_relaxed_u32(p.ctl + kCtlTaken), (uint32_t)p.pool_cap);
-        if (taken <= (uint32_t)kScanRecords) {
-            for (uint32_t b0 = 0; b0 < taken; b0 += 8 * 32) {
-                uint32_t tg[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t i = b0 + u * 32 + lane;
-                    tg[u] = i < taken ? ld_relaxed_u32(p.reg + i) : 0u;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    unsigned m = __ballot_sync(0xffffffffu, tg[u] == seg + 1u);
-                    while (m != 0u) {
-                        const int src = __ffs(m) - 1;
-                        m &= m - 1;
-                        if (lane == n) mine = b0 + u * 32 + src + 1;
-                        ++n;
-                    }
-                }
-            }
-            scanned = n <= 32;
-            if (!scanned) {
-                n = 0;
-                mine = 0u;
-            }
-        }
+    int key = INT32_MAX, cnt = 0;
+    const int nslot = min(npieces, kSlots);
+    if (lane < nslot) {
+        const unsigned long long e = __ldcg(p.seg_slots + (size_t)seg * kSlots + lane);
+        mine = (uint32_t)(e & ((1u << kSlotRecBits) - 1u));
+        key = (int)((e >> kSlotRecBits) & ((1u << kSlotBlkBits) - 1u));
+        cnt = (int)(e >> (kSlotRecBits + kSlotBlkBits));
     }
-    if (!scanned) {
-        // lane k takes the k-th record of the list
+    int n = nslot;
+    uint32_t rest = 0u;   // pieces past the 32nd (not produced by the usual splits) follow in list order
+    if (npieces > kSlots) {
         uint32_t r = ld_acquire_u32(p.seg_list + seg);
         while (r != 0u && n < 32) {
             if (lane == n) mine = r;
@@ -265,22 +247,20 @@ __device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, 
             ++n;
         }
         rest = r;
-    }
-    // (first block, block count) of each lane's record, all loads at once
-    int key = INT32_MAX, cnt = 0;
-    if (lane < n) {
-        const float *rec = rec_of(mine);
-        key = __float_as_int(__ldcg(rec + tr + 1));
-        cnt = __float_as_int(__ldcg(rec + tr + 2));
+        if (lane >= nslot && lane < n) {
+            const float *rec = rec_of(mine);
+            key = __float_as_int(__ldcg(rec + tr + 1));
+            cnt = __float_as_int(__ldcg(rec + tr + 2));
+        }
     }
     // bitonic sort of the 32 (first block, record, count) triples, ascending
 #pragma unroll
     for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
         for (int j = k >> 1; j > 0; j >>= 1) {
-            const int ok = __shfl_xor_sync(0xffffffffu, key, j);
-            const uint32_t om = __shfl_xor_sync(0xffffffffu, mine, j);
-            const int oc = __shfl_xor_sync(0xffffffffu, cnt, j);
+            const int ok = __shfl_xor_sync(kFull, key, j);
+            const uint32_t om = __shfl_xor_sync(kFull, mine, j);
+            const int oc = __shfl_xor_sync(kFull, cnt, j);
             const bool up = (lane & k) == 0;
             const bool lower = (lane & j) == 0;
             const bool take = lower == up ? ok < key : ok > key;
@@ -293,7 +273,7 @@ __device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, 
     }
     // the pieces must tile [0, c_nb): sorted, each starts where the previous
     // one ended, the first at 0 and the last at the range's end
-    const int pkey = __shfl_up_sync(0xffffffffu, key, 1), pcnt = __shfl_up_sync(0xffffffffu, cnt, 1);
+    const int pkey = __shfl_up_sync(kFull, key, 1), pcnt = __shfl_up_sync(kFull, cnt, 1);
     bool bad = false;
     if (lane < n) {
         bad = cnt <= 0 || (lane == 0 ? key != 0 : (rest == 0u && key != pkey + pcnt));
@@ -301,18 +281,37 @@ __device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, 
     }
     int counted = cnt;   // with more than 32 pieces only the total is checked
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) counted += __shfl_xor_sync(0xffffffffu, counted, o);
-    auto record_k = [&](int k, uint32_t &walk) -> const float * {
-        if (k < n) return rec_of(__shfl_sync(0xffffffffu, mine, k));
+    for (int o = 16; o > 0; o >>= 1) counted += __shfl_xor_sync(kFull, counted, o);
+
+    // ---- (max, sum) per head: lane hh < G folds the records in order, the
+    // (m, l) loads of eight records in flight at a time
+    float M = -INFINITY, L = 0.f;
+    for (int k0 = 0; k0 < n; k0 += 8) {
+        float mv[8], lv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const uint32_t r = __shfl_sync(kFull, mine, (k0 + u) & 31);
+            mv[u] = -INFINITY;
+            lv[u] = 0.f;
+            if (k0 + u < n && lane < G) {
+                const float *rec = rec_of(r);
+                mv[u] = __ldcg(rec + lane);
+                lv[u] = __ldcg(rec + G + lane);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (k0 + u < n) {
+                const float Mn = fmaxf(M, mv[u]);
+                L = L * exp2_approx(M - Mn) + lv[u] * exp2_approx(mv[u] - Mn);
+                M = Mn;
+            }
+        }
+    }
+    for (uint32_t walk = rest; walk != 0u;) {
         const float *rec = rec_of(walk);
         walk = __float_as_uint(__ldcg(rec + tr));
         counted += __float_as_int(__ldcg(rec + tr + 2));
-        return rec;
-    };
-    float M = -INFINITY, L = 0.f;
-    uint32_t walk = rest;
-    for (int k = 0; k < n || walk != 0u; ++k) {
-        const float *rec = record_k(k, walk);
         if (lane < G) {
             const float mv = __ldcg(rec + lane), lv = __ldcg(rec + G + lane);
             const float Mn = fmaxf(M, mv);
@@ -321,18 +320,18 @@ __device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, 
         }
     }
     if (rest != 0u) bad |= counted != c_nb;
-    if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(p.dev_status, PKV_DEV_SPLIT);
+    if (__any_sync(kFull, bad) && lane == 0) set_status(p.dev_status, PKV_DEV_SPLIT);
     float Mh[HP], invL[HP], o[HP][PER];
 #pragma unroll
     for (int hh = 0; hh < HP; ++hh) {
-        Mh[hh] = __shfl_sync(0xffffffffu, M, hh);
-        invL[hh] = 1.f / __shfl_sync(0xffffffffu, L, hh);
+        Mh[hh] = __shfl_sync(kFull, M, hh);
+        invL[hh] = 1.f / __shfl_sync(kFull, L, hh);
 #pragma unroll
         for (int k = 0; k < PER; ++k) o[hh][k] = 0.f;
     }
-    walk = rest;
-    for (int k = 0; k < n || walk != 0u; ++k) {
-        const float *rec = record_k(k, walk);
+    // ---- accumulators, a record at a time (its G x D/32 loads per lane in
+    // flight together)
+    auto add_record = [&](const float *rec) {
 #pragma unroll
         for (int hh = 0; hh < HP; ++hh) {
             if (hh < G) {
@@ -342,6 +341,12 @@ __device__ __forceinline__ void merge_list(const DecodeParams &p, int s, int h, 
                 for (int k2 = 0; k2 < PER; ++k2) o[hh][k2] += f * __ldcg(racc + lane + 32 * k2);
             }
         }
+    };
+    for (int k = 0; k < n; ++k) add_record(rec_of(__shfl_sync(kFull, mine, k)));
+    for (uint32_t walk = rest; walk != 0u;) {
+        const float *rec = rec_of(walk);
+        walk = __float_as_uint(__ldcg(rec + tr));
+        add_record(rec);
     }
 #pragma unroll
     for (int hh = 0; hh < HP; ++hh) {
@@ -400,7 +405,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int64_t nw = (total + min_blocks - 1) / min_blocks;
     if (nw > p.total_warps) nw = p.total_warps;
     if (nw < 1) nw = 1;
-    const bool scan_merge = nw < p.total_warps;   // a small step: merges scan the few records
     if (tid < kDecodeWarps) plan_s[tid] = -1;
     __syncthreads();
     int64_t carry = 0;
@@ -465,7 +469,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const uint32_t ring_addr = smem_addr(wring);
 
     uint32_t slot_base = 0;     // ring slots used by earlier pieces of work (phases continue)
-    bool steal_reserved = false;
+    bool seen_ready = false;    // every CTA has published its range words
+    int rec_used = 0;           // records of this warp's own set taken so far
     uint32_t warp_blocks = 0;   // blocks this warp has streamed (checked against the plan at exit)
 
     // Work: first the warp's own range (claimed in batches), then stolen pieces.
@@ -610,15 +615,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     }
                     return;
                 }
-                // one piece of a range: leave (m, l, acc) on the range's list
-                uint32_t ri = 0;
-                if (lane == 0) ri = atomicAdd(p.ctl + kCtlTaken, 1u) + 1u;
-                ri = __shfl_sync(0xffffffffu, ri, 0);
-                if ((int64_t)ri > (int64_t)p.pool_cap) {
-                    // cannot happen: steals are budgeted so that the records fit
+                // one piece of a range: leave (m, l, acc) in a record of
+                // this warp's own set, register it, count its blocks
+                const uint32_t seg = (uint32_t)cs * (uint32_t)Hkv + (uint32_t)ch;
+                if (rec_used >= p.rec_per_warp) {
+                    // cannot happen: a warp steals only while two records are left
                     if (lane == 0) set_status(p.dev_status, PKV_DEV_SPLIT);
                     return;
                 }
+                const uint32_t ri = (uint32_t)(wg * p.rec_per_warp + rec_used) + 1u;
+                ++rec_used;
+                // the piece's number within the range first (a round trip that
+                // overlaps the record stores below)
+                unsigned long long before = 0;
+                if (lane == 0) before = atomicAdd(p.seg_cnt + seg, 1ull << 32);
                 float *rec = p.part + (size_t)(ri - 1) * p.rec_floats;
 #pragma unroll
                 for (int pn = 0; pn < NT; ++pn) {
@@ -642,32 +652,35 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                         }
                     }
                 }
-                // publish: every lane's record stores, then lane 0 links the
-                // record, registers it and adds the piece's blocks to the
-                // range's counter (a release; the warp that completes the
-                // count acquires)
-                __threadfence();
-                __syncwarp();
-                const uint32_t seg = (uint32_t)cs * (uint32_t)Hkv + (uint32_t)ch;
-                uint32_t done = 0;
                 if (lane == 0) {
-                    const uint32_t nxt = atomicExch(p.seg_list + seg, ri);
                     float *trailer = rec + p.rec_floats - 4;
-                    trailer[0] = __uint_as_float(nxt);
                     trailer[1] = __int_as_float(piece_j0);
                     trailer[2] = __int_as_float(piece_n);
-                    if (ri <= (uint32_t)kScanRecords) p.reg[ri - 1] = seg + 1u;
-                    __threadfence();
-                    done = atomicAdd(p.seg_done + seg, (uint32_t)piece_n) + (uint32_t)piece_n;
+                    const int k = (int)(before >> 32);
+                    if (k < kSlots) {
+                        p.seg_slots[(size_t)seg * kSlots + k] = slot_pack(ri, piece_j0, piece_n);
+                    } else {
+                        // past the slots: on the range's list
+                        trailer[0] = __uint_as_float(atomicExch(p.seg_list + seg, ri));
+                    }
+                }
+                // publish: every lane's stores, then lane 0 adds the piece's
+                // blocks to the range's count (a release; the warp that
+                // completes the count acquires)
+                __threadfence();
+                __syncwarp();
+                unsigned long long after = 0;
+                if (lane == 0) {
+                    after = atomicAdd(p.seg_cnt + seg, (unsigned long long)piece_n) + (unsigned long long)piece_n;
                     __threadfence();
                     // a count past the range's blocks means a block was
                     // streamed twice (a merge may already have run short)
-                    if (done > (uint32_t)c_nb) set_status(p.dev_status, PKV_DEV_SPLIT);
+                    if ((uint32_t)after > (uint32_t)c_nb) set_status(p.dev_status, PKV_DEV_SPLIT);
                 }
-                done = __shfl_sync(0xffffffffu, done, 0);
-                if (done == (uint32_t)c_nb) {
+                after = __shfl_sync(0xffffffffu, after, 0);
+                if ((uint32_t)after == (uint32_t)c_nb) {
                     __syncwarp();
-                    merge_list<T, D, NT>(p, cs, ch, c_nb, lane, scan_merge);
+                    merge_range<T, D, NT>(p, cs, ch, c_nb, (int)(after >> 32), lane);
                 }
             };
 
@@ -920,25 +933,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         // no share reaches kStealMin blocks (shares differ by at most one
         // block): no warp can ever be robbed in this call
         if ((total + nw - 1) / nw < kStealMin) break;
+        // a steal can leave two records: stop when fewer are left
+        if (!p.steal || rec_used + 2 > p.rec_per_warp) break;
         // nothing left to take: unclaimed work only shrinks, so once one full
         // scan found no warp worth robbing, none will be again in this call.
         // The drained word and the ready count are read side by side.
         const uint32_t drained = ld_relaxed_u32(p.ctl + kCtlDrained);
         uint32_t rdy = 0u;
-        if (lane == 0 && !steal_reserved) rdy = ld_acquire_u32(p.ctl + kCtlReady);
+        if (lane == 0 && !seen_ready) rdy = ld_acquire_u32(p.ctl + kCtlReady);
         if (drained != 0u) break;
-        if (lane == 0 && !steal_reserved) {
-            // every CTA has published its words, and the steal budget allows
-            // one more piece (each steal can leave two partial records)
-            if (rdy >= gridDim.x) {
-                const uint32_t r = atomicAdd(p.ctl + kCtlSteals, 1u) + 1u;
-                steal_reserved = (int64_t)r <= (int64_t)p.steal_cap;
-            }
-        }
-        // (the other lanes' reads of range words and prefixes below come
-        // after lane 0's acquire of the ready count)
+        // thieves rob no warp before every CTA has published its words; the
+        // other lanes' reads of range words and prefixes below come after
+        // lane 0's acquire of the ready count
+        if (lane == 0 && !seen_ready) seen_ready = rdy >= gridDim.x;
         __syncwarp();
-        if (!__shfl_sync(0xffffffffu, steal_reserved ? 1 : 0, 0)) break;
+        if (!__shfl_sync(0xffffffffu, seen_ready ? 1 : 0, 0)) break;
         bool got = false;
         for (int attempt = 0; attempt < 8 && !got; ++attempt) {
             // every lane reads its share of the range words, eight at a time
@@ -1000,7 +1009,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             }
         }
         if (!got) break;
-        steal_reserved = false;
         own = false;
         s0 = locate_seq(p, x0, lane);
         off0 = (int)(x0 - __ldcg(p.prefix + s0) * Hkv);
@@ -1054,10 +1062,10 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
 
 // ---- workspace ----------------------------------------------------------------
 // Control region, zeroed before every call:
-//   [control words 256 B][record registry kScanRecords x 4]
-//   [range counters S*Hkv x 4][range list heads S*Hkv x 4]
+//   [control words 256 B][range counter words S*Hkv x 8][range list heads S*Hkv x 4]
 // then, written by the call before it reads them:
-//   [range words, one per warp x 8][prefix (S+1) x 8][partial records]
+//   [range slot arrays S*Hkv x kSlots x 8][range words, one per warp x 8]
+//   [prefix (S+1) x 8][partial records, rec_per_warp per warp]
 // each part 256-B aligned.  A partial record holds G maxima, G sums,
 // G x head_dim accumulators and a trailer (link, first block, block count).
 
@@ -1066,7 +1074,7 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 static int record_floats(int G, int head_dim) { return ((2 * G + G * head_dim + 3) & ~3) + 4; }
 
 struct DecodeLayout {
-    size_t ctl, reg, seg_done, seg_list, clear_bytes, ranges, prefix, part, fixed;
+    size_t ctl, seg_cnt, seg_list, clear_bytes, seg_slots, ranges, prefix, part, fixed;
 };
 
 static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
@@ -1074,13 +1082,13 @@ static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
     size_t o = 0;
     L.ctl = o;
     o += kCtlBytes;
-    L.reg = o;
-    o += align256((size_t)kScanRecords * 4);
-    L.seg_done = o;
-    o += align256((size_t)S * Hkv * 4);
+    L.seg_cnt = o;
+    o += align256((size_t)S * Hkv * 8);
     L.seg_list = o;
     o += align256((size_t)S * Hkv * 4);
     L.clear_bytes = o;
+    L.seg_slots = o;
+    o += align256((size_t)S * Hkv * kSlots * 8);
     L.ranges = o;
     o += align256((size_t)total_warps * 8);
     L.prefix = o;
@@ -1090,10 +1098,12 @@ static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
     return L;
 }
 
-// records: two per warp for its own range (the pieces at its ends) plus two
+// records per warp: two for its own range (the pieces at its ends) plus two
 // per steal; the recommended size allows four steals per warp
-static size_t records_min(int total_warps) { return (size_t)2 * total_warps; }
-static size_t records_recommended(int total_warps) { return (size_t)10 * total_warps; }
+constexpr int kRecordsMin = 2;
+constexpr int kRecordsRecommended = 10;
+static size_t records_min(int total_warps) { return (size_t)kRecordsMin * total_warps; }
+static size_t records_recommended(int total_warps) { return (size_t)kRecordsRecommended * total_warps; }
 
 size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
@@ -1136,6 +1146,8 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     if ((int64_t)num_blocks * num_kv_heads * block_size >= (int64_t)1 << 31) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)num_seqs * max_blocks_per_seq >= (int64_t)1 << 31) return PKV_ERR_UNSUPPORTED;
+    // a range's first block and block count live in 20-bit fields of its slots
+    if (max_blocks_per_seq >= (1 << kSlotBlkBits)) return PKV_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PKV_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !workspace)
         return PKV_ERR_INVALID_ARG;
@@ -1160,7 +1172,10 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     const DecodeLayout lay = decode_layout(num_seqs, num_kv_heads, total_warps);
     const size_t rec_bytes = (size_t)record_floats(G, head_dim) * sizeof(float);
     if (workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) return PKV_ERR_WORKSPACE;
-    const size_t cap = (workspace_bytes - lay.fixed) / rec_bytes;
+    // records per warp (record numbers live in 24-bit slot fields)
+    size_t per_warp = (workspace_bytes - lay.fixed) / rec_bytes / total_warps;
+    const size_t max_per_warp = (((size_t)1 << kSlotRecBits) - 2) / total_warps;
+    if (per_warp > max_per_warp) per_warp = max_per_warp;
 
     CUtensorMap tk, tv;
     rc = encode_cache_map(&tk, k_cache, num_blocks, num_kv_heads, block_size, head_dim);
@@ -1175,9 +1190,9 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     prm.block_tables = block_tables;
     prm.context_lens = context_lens;
     prm.ctl = reinterpret_cast<uint32_t *>(ws + lay.ctl);
-    prm.reg = reinterpret_cast<uint32_t *>(ws + lay.reg);
-    prm.seg_done = reinterpret_cast<uint32_t *>(ws + lay.seg_done);
+    prm.seg_cnt = reinterpret_cast<unsigned long long *>(ws + lay.seg_cnt);
     prm.seg_list = reinterpret_cast<uint32_t *>(ws + lay.seg_list);
+    prm.seg_slots = reinterpret_cast<unsigned long long *>(ws + lay.seg_slots);
     prm.ranges = reinterpret_cast<unsigned long long *>(ws + lay.ranges);
     prm.prefix = reinterpret_cast<long long *>(ws + lay.prefix);
     prm.part = reinterpret_cast<float *>(ws + lay.part);
@@ -1192,12 +1207,11 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     prm.out_dtype = out_dtype;
     prm.total_warps = total_warps;
     prm.rec_floats = record_floats(G, head_dim);
-    prm.pool_cap = cap > (size_t)INT32_MAX ? INT32_MAX : (int)cap;
-    prm.steal_cap = (int)((prm.pool_cap - records_min(total_warps)) / 2);
+    prm.rec_per_warp = (int)per_warp;
     // PKV_DETERMINISTIC=1: no stealing, so the split of every range is fixed
     // by the contexts alone and the output bits repeat from call to call
     const char *det = std::getenv("PKV_DETERMINISTIC");
-    if (det && det[0] == '1') prm.steal_cap = 0;
+    prm.steal = (det && det[0] == '1') ? 0 : 1;
     prm.k_new = k_new;
     prm.v_new = v_new;
     prm.k_cache = const_cast<void *>(k_cache);

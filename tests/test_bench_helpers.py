@@ -40,9 +40,10 @@ def test_clock_summary_flags_throttle_reasons():
 
 
 def test_traffic_is_reported_only_for_the_captured_source(monkeypatch):
-    assert bench.decode_traffic(1000) in (None, int(round(1000 * bench.DECODE_TRAFFIC_RATIO)))
+    assert bench.decode_traffic(True) in (None, bench.DECODE_TRAFFIC_BYTES)
+    assert bench.decode_traffic(False) is None          # another workload: never the captured bytes
     monkeypatch.setattr(bench, "DECODE_TRAFFIC_SHA1", "0" * 40)
-    assert bench.decode_traffic(1000) is None
+    assert bench.decode_traffic(True) is None
 
 
 def test_step_config_describes_the_workload():
