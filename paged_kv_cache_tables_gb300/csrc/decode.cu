@@ -442,9 +442,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int64_t lo_w = wg < nw ? range_lo(wg, total, nw) : total;
     const int n_own = wg < nw ? (int)(range_lo(wg + 1, total, nw) - lo_w) : 0;
     if (lane == 0) p.ranges[wg] = rw_make(0, n_own);
-    __threadfence();
+    // publish: the barrier orders every thread's range word and prefix
+    // stores before thread 0's fence, which makes them visible at GPU scope
+    // before the ready count moves (only thread 0 waits for it)
     __syncthreads();
-    if (tid == 0) atomicAdd(p.ctl + kCtlReady, 1u);
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(p.ctl + kCtlReady, 1u);
+    }
 
     // ---- this warp's ring ----
     uint8_t *wring = ring + warp * STAGES * Sh::STAGE_BYTES;
