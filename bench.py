@@ -760,7 +760,7 @@ def run_trace_bench(args):
     print(json.dumps(trace_line(args, args.trace_requests, args.trace_pool)))
 
 
-def run_prefix_bench(args):
+def prefix_summary(args):
     """Prefix caching on a sharing-heavy trace: 1000 requests in 8 groups whose
     prompts share a head (lognormal, mean 1024 tokens, whole pages) followed by
     their own tail (lognormal, mean 128), outputs geometric with mean 256; the
@@ -771,7 +771,7 @@ def run_prefix_bench(args):
     keep = ["engine_steps", "wall_s", "output_tokens", "output_tokens_per_s", "prefill_tokens", "prefix_hit_blocks",
             "avg_running_batch", "ttft_steps_mean", "ttft_ms_mean", "latency_steps_p50", "latency_steps_p99",
             "preemptions", "oracle_check", "clocks"]
-    print(json.dumps({
+    return {
         "metric": "prefix caching: output tokens/s, prefill tokens and mean time to first token",
         "workload": "%d requests in 8 groups sharing a prompt head (lognormal mean 1024, whole pages) + own tail "
                     "(lognormal mean 128), outputs geometric mean 256, Poisson(20)/step, max batch 256, budget 8192, "
@@ -780,7 +780,11 @@ def run_prefix_bench(args):
         "throughput_ratio": round(on["output_tokens_per_s"] / off["output_tokens_per_s"], 3),
         "prefill_token_ratio": round(off["prefill_tokens"] / max(1, on["prefill_tokens"]), 3),
         "ttft_ratio_no_cache_over_cache": round(off["ttft_ms_mean"] / on["ttft_ms_mean"], 3),
-    }))
+    }
+
+
+def run_prefix_bench(args):
+    print(json.dumps(prefix_summary(args)))
 
 
 def swap_copy_rates(NB=8192, n=4096, reps=5):
@@ -828,16 +832,12 @@ def swap_copy_rates(NB=8192, n=4096, reps=5):
     return res
 
 
-def run_preempt_bench(args):
+def preempt_summary(args):
     """Preemption by recompute against preemption by swap on the trace with a
     pool small enough to preempt: the same requests, engine and kernels; only
     what happens to a victim's blocks differs (freed and recomputed, or copied
     to pinned host memory and back)."""
     import torch
-    if args.copy_rates_only:
-        torch.cuda.set_device(0)
-        print(json.dumps({"swap_copy_gbs": swap_copy_rates()}))
-        return
     NB = args.trace_pool if args.trace_pool != 200000 else 6250
     swap = args.swap_blocks or 2 * NB
     n = args.trace_requests
@@ -848,7 +848,7 @@ def run_preempt_bench(args):
     keep = ["engine_steps", "wall_s", "output_tokens", "output_tokens_per_s", "prefill_tokens", "preemptions",
             "swapped_out_blocks", "swapped_in_blocks", "swap_bytes", "avg_running_batch", "ttft_ms_mean",
             "latency_steps_p50", "latency_steps_p99", "oracle_check", "clocks"]
-    print(json.dumps({
+    return {
         "metric": "preemption by recompute vs by swap: output tokens/s, prefill tokens and swapped bytes",
         "workload": "%d requests as in the trace, pool %d blocks, %d layers (8B shape) over %d caches; swap space "
                     "%d blocks per cache array in pinned host memory" % (n, NB, args.trace_layers,
@@ -856,10 +856,19 @@ def run_preempt_bench(args):
         "recompute": {k: rec[k] for k in keep}, "swap": {k: sw[k] for k in keep},
         "throughput_ratio_swap_over_recompute": round(sw["output_tokens_per_s"] / rec["output_tokens_per_s"], 3),
         "swap_copy_gbs": rates,
-    }))
+    }
 
 
-def run_batching_bench(args):
+def run_preempt_bench(args):
+    import torch
+    if args.copy_rates_only:
+        torch.cuda.set_device(0)
+        print(json.dumps({"swap_copy_gbs": swap_copy_rates()}))
+        return
+    print(json.dumps(preempt_summary(args)))
+
+
+def batching_summary(args):
     """Static against continuous batching on one synthetic trace: 500 requests
     with lognormal output lengths, the rest as in the trace workload.  Both runs
     use the same engine, kernels and pool; only the admission policy differs."""
@@ -868,7 +877,7 @@ def run_batching_bench(args):
     co = trace_line(args, n, args.trace_pool, policy="continuous", outputs="lognormal")
     keep = ["engine_steps", "wall_s", "output_tokens", "output_tokens_per_s", "avg_running_batch", "ttft_steps_mean",
             "ttft_ms_mean", "latency_steps_p50", "latency_steps_p99", "preemptions", "oracle_check", "clocks"]
-    print(json.dumps({
+    return {
         "metric": "static vs continuous batching: output tokens/s and mean time to first token",
         "workload": "%d requests, Poisson(20)/step, prompt lognormal mean 512, output lognormal mean 256 (sigma 1), "
                     "max batch 256, budget 8192, chunk 512, pool %d blocks, %d layers (8B shape)"
@@ -876,7 +885,11 @@ def run_batching_bench(args):
         "static": {k: st[k] for k in keep}, "continuous": {k: co[k] for k in keep},
         "throughput_ratio": round(co["output_tokens_per_s"] / st["output_tokens_per_s"], 3),
         "ttft_ratio_static_over_continuous": round(st["ttft_ms_mean"] / co["ttft_ms_mean"], 3),
-    }))
+    }
+
+
+def run_batching_bench(args):
+    print(json.dumps(batching_summary(args)))
 
 
 
@@ -1193,6 +1206,11 @@ def run_pkv(args):
         line["trace"] = trace_summary(args, args.trace_requests, args.trace_pool)
         line["trace_small_pool"] = trace_summary(args, args.trace_requests, 6250, big_steps_only=False)
         line["tiny_step"] = tiny_line(args)
+        # the NEXT rows on the same engine: static against continuous
+        # batching, prefix caching, preemption by swap against recompute
+        # (the pages' batching gains are context, not targets)
+        line["next"] = {"static_vs_continuous": batching_summary(args), "prefix_caching": prefix_summary(args),
+                        "swap_vs_recompute": preempt_summary(args)}
     if not args.no_cpu_baseline and ws == 1:
         k = oracle_sample_size(st, args.cpu_budget)
         cb = cpu_oracle_run(st, k, min_seconds=args.cpu_budget)
