@@ -100,3 +100,21 @@ def oracle_decode_all(q, k_cache, v_cache, block_tables, context_lens, dtype, sc
     with ThreadPoolExecutor(max_workers=threads) as ex:
         list(ex.map(run, [(cuts[i], cuts[i + 1]) for i in range(len(cuts) - 1) if cuts[i + 1] > cuts[i]]))
     return out
+
+
+def oracle_prefill_all(q, cu_seqlens, k_cache, v_cache, block_tables, context_lens, dtype, scale=None):
+    """oracle.prefill over every chunk of a step, one plain oracle call per
+    chunk, run side by side on host threads (longest first)."""
+    n = len(cu_seqlens) - 1
+    out = np.empty((int(cu_seqlens[n]),) + q.shape[1:], np.float64)
+    threads = max(1, min(len(os.sched_getaffinity(0)), 16, n))
+
+    def run(c):
+        lo, hi = int(cu_seqlens[c]), int(cu_seqlens[c + 1])
+        out[lo:hi] = oracle.prefill(q[lo:hi], np.array([0, hi - lo], np.int32), k_cache, v_cache,
+                                    block_tables[c:c + 1], context_lens[c:c + 1], dtype, scale=scale)
+
+    work = sorted(range(n), key=lambda c: -int(context_lens[c]) * int(cu_seqlens[c + 1] - cu_seqlens[c]))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, work))
+    return out

@@ -4,7 +4,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import DeviceStep, assert_close, dev, dev_bits, out_to_f64
+from gpu_helpers import (DeviceStep, assert_close, dev, dev_bits, oracle_decode_all, oracle_prefill_all,
+                         out_to_f64)
 from paged_kv_cache_tables_gb300 import kv_append, paged_decode_attention, paged_prefill_attention
 from synth import build_step, make_step, rne_bits
 
@@ -100,23 +101,24 @@ def test_prefill_with_one_query_row_equals_decode(cuda_lib):
     np.testing.assert_allclose(pre.cpu().numpy(), dec.cpu().numpy(), rtol=0, atol=2e-5)
 
 
-def sampled_prefill_reference(st, kc, vc, rows):
-    """Oracle rows of the prefill part via attention over [0, position]."""
-    q_p, cu_p, bt_p, cl_p = st.prefill_part()
-    ref = []
-    for c, i in rows:
-        q_len = int(cu_p[c + 1] - cu_p[c])
-        pos = int(cl_p[c]) - q_len + i
-        m, l, acc = oracle.decode_range(q_p[int(cu_p[c]) + i], kc, vc, bt_p[c], 0, pos + 1, st.dtype)
-        ref.append(acc / l[:, None])
-    return np.stack(ref)
-
-
-def test_mixed_step_full_size_sampled(cuda_lib):
-    """The mixed step: append 4344 tokens, prefill 8 chunks of 512, decode 248
-    sequences -- in the launch configuration of the benchmark -- checked on
-    sampled rows of both parts."""
+@pytest.fixture(scope="module")
+def mixed_reference():
+    """The mixed step after its append, with the oracle's output for every
+    prefill row and every decode row (computed once for the module)."""
     st = make_step("mixed")
+    kc, vc = oracle_after_append(st)
+    q_p, cu_p, bt_p, cl_p = st.prefill_part()
+    ref_pre = oracle_prefill_all(q_p, cu_p, kc, vc, bt_p, cl_p, st.dtype)
+    q_d, bt_d, cl_d = st.decode_part()
+    ref_dec = oracle_decode_all(q_d, kc, vc, bt_d, cl_d, st.dtype)
+    return st, ref_pre, ref_dec
+
+
+def test_mixed_step_full_size_every_row(cuda_lib, mixed_reference):
+    """The mixed step: append 4344 tokens, prefill 8 chunks of 512, decode 248
+    sequences -- in the launch configuration of the benchmark -- every row of
+    both parts against the oracle."""
+    st, ref_pre, ref_dec = mixed_reference
     ds = DeviceStep(st)
     kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
     p = st.n_prefill
@@ -124,23 +126,18 @@ def test_mixed_step_full_size_sampled(cuda_lib):
     pre = torch.empty((t1, st.Hq, st.d), dtype=torch.float32, device="cuda")
     paged_prefill_attention(pre, ds.q[:t1], ds.cu_seqlens[:p + 1], 512, ds.k_cache, ds.v_cache,
                             ds.block_tables[:p], ds.context_lens[:p], dev_status=ds.status)
+    pre16 = torch.empty((t1, st.Hq, st.d), dtype=ds.q.dtype, device="cuda")
+    paged_prefill_attention(pre16, ds.q[:t1], ds.cu_seqlens[:p + 1], 512, ds.k_cache, ds.v_cache,
+                            ds.block_tables[:p], ds.context_lens[:p], dev_status=ds.status)
     dec = torch.empty((st.S - p, st.Hq, st.d), dtype=torch.float32, device="cuda")
     paged_decode_attention(dec, ds.q[t1:], ds.k_cache, ds.v_cache, ds.block_tables[p:], ds.context_lens[p:],
                            dev_status=ds.status)
     torch.cuda.synchronize()
     assert int(ds.status.item()) == 0
-    kc, vc = oracle_after_append(st)
-    rng = np.random.default_rng(0)
-    rows = [(c, i) for c in range(p) for i in [0, 1, 255, 511, int(rng.integers(2, 511))]]
-    ref = sampled_prefill_reference(st, kc, vc, rows)
-    got = np.stack([out_to_f64(pre[int(st.cu_seqlens[c]) + i]) for c, i in rows])
-    e1 = assert_close(got, ref, "fp32", what="mixed prefill rows")
-    pick = [0, 5, 100, 247]
-    q_d, bt_d, cl_d = st.decode_part()
-    refd = oracle.decode(q_d[pick], kc, vc, bt_d[pick], cl_d[pick], st.dtype)
-    e2 = assert_close(out_to_f64(dec)[pick], refd, "fp32", what="mixed decode rows")
-    assert np.all(np.isfinite(pre.cpu().numpy()))
-    print("mixed sampled max-abs prefill %.3g decode %.3g" % (e1, e2))
+    e1 = assert_close(out_to_f64(pre), ref_pre, "fp32", what="mixed prefill, fp32 out")
+    e16 = assert_close(out_to_f64(pre16), ref_pre, st.dtype, what="mixed prefill, bf16 out")
+    e2 = assert_close(out_to_f64(dec), ref_dec, "fp32", what="mixed decode")
+    print("mixed step, every row: max-abs prefill fp32 %.3g bf16 %.3g, decode fp32 %.3g" % (e1, e16, e2))
 
 
 def test_prefill_flags_a_chunk_longer_than_its_context(cuda_lib):
@@ -157,13 +154,13 @@ def test_prefill_flags_a_chunk_longer_than_its_context(cuda_lib):
 
 
 @pytest.mark.parametrize("decode_sms", [0, 24, 130])
-def test_mixed_entry_side_by_side_matches_oracle(cuda_lib, decode_sms):
+def test_mixed_entry_side_by_side_matches_oracle(cuda_lib, mixed_reference, decode_sms):
     """pkv_paged_mixed_attention on the mixed step (prefill and decode kernels
     on split SMs, the split picked from host metadata or forced): the prefill
-    rows are the bits of the plain prefill call, and sampled rows of both parts
-    match the oracle."""
+    rows are the bits of the plain prefill call, and every row of both parts
+    matches the oracle."""
     from paged_kv_cache_tables_gb300 import paged_mixed_attention
-    st = make_step("mixed")
+    st, ref_pre, ref_dec = mixed_reference
     ds = DeviceStep(st)
     kv_append(ds.k_new, ds.v_new, ds.slot_mapping, ds.k_cache, ds.v_cache, dev_status=ds.status)
     p = st.n_prefill
@@ -179,12 +176,5 @@ def test_mixed_entry_side_by_side_matches_oracle(cuda_lib, decode_sms):
     assert int(ds.status.item()) == 0
     assert torch.equal(out[:t1], pre)
     assert np.all(np.isfinite(out.cpu().numpy()))
-    kc, vc = oracle_after_append(st)
-    rows = [(c, i) for c in range(p) for i in (0, 300, 511)]
-    ref = sampled_prefill_reference(st, kc, vc, rows)
-    got = np.stack([out_to_f64(out[int(st.cu_seqlens[c]) + i]) for c, i in rows])
-    assert_close(got, ref, "fp32", what="mixed entry prefill rows")
-    pick = [0, 7, 123, 247]
-    q_d, bt_d, cl_d = st.decode_part()
-    refd = oracle.decode(q_d[pick], kc, vc, bt_d[pick], cl_d[pick], st.dtype)
-    assert_close(out_to_f64(out[t1:])[pick], refd, "fp32", what="mixed entry decode rows")
+    assert_close(out_to_f64(out[:t1]), ref_pre, "fp32", what="mixed entry prefill rows")
+    assert_close(out_to_f64(out[t1:]), ref_dec, "fp32", what="mixed entry decode rows")
