@@ -112,9 +112,11 @@ class PagedEngine:
                     raise B.PkvError("swap in", rc)
         self.swap_bytes += (n_out + n_in) * blk * 2 * self.R
 
-    def step(self, fill, on_layer_done=None):
+    def step(self, fill, on_layer_done=None, time_layers=False):
         """One engine step.  Returns None when nothing was scheduled, else a
-        dict with the step's metadata (numpy) and device views."""
+        dict with the step's metadata (numpy) and device views.  With
+        time_layers, events around each layer's attention call let the caller
+        separate the attention's device time from the rows' generation."""
         torch = self.torch
         t0 = time.perf_counter()
         m = self.sched.step_raw()
@@ -196,9 +198,13 @@ class PagedEngine:
         vc = [t.data_ptr() for t in self.v_cache]
         NB, Hq, Hkv, d = self.NB, self.Hq, self.Hkv, self.d
         self.host_ms += (time.perf_counter() - t0) * 1e3 - waited
+        layer_events = []
         for layer in range(self.L):
             cid = layer % self.R
             fill(layer, cid, q, k, v, trids, tpos)
+            if time_layers:
+                layer_events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                layer_events[-1][0].record(self.stream)
             # the layer's append and attention in one call: prefill chunks
             # (their rows appended by slot) beside the decodes on split SMs,
             # each decode's row appended inside the decode kernel
@@ -207,19 +213,25 @@ class PagedEngine:
                                                     nwork, hcu, hctx, 0, pst, pstream)
             if rc != B.PKV_OK:
                 raise B.PkvError("engine step, layer %d" % layer, rc)
+            if time_layers:
+                layer_events[-1][1].record(self.stream)
             if on_layer_done is not None:
                 on_layer_done(layer, info, out)
         ev[1].record(self.stream)
         info["events"] = ev
+        info["layer_events"] = layer_events
         return info
 
 
 def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pick=None, max_steps=1000000,
-              tokens=None):
+              tokens=None, time_layers_every=0):
     """Drive `engine` through a request trace: request i is added at engine
     step arrival[i]; steps run until every request has finished.  On every
     `sample_every`-th engine step, pick(info) names (output row, rid,
     position) samples whose layer-0 outputs are copied back for checking.
+    Every `time_layers_every`-th step also times its attention calls alone
+    (events around each; they break the overlap of a layer's launches with
+    the row generation before them, so only a sample of steps is timed).
     Returns per-step records, finish steps, timings and the sampled rows."""
     torch = engine.torch
     n = len(arrival)
@@ -248,7 +260,8 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
             engine.add(i, int(prompt[i]), int(max_tokens), int(eos[i]), tokens=None if tokens is None else tokens[i])
             nxt += 1
         state["sample"] = bool(sample_every) and pick is not None and len(steps) % sample_every == 0
-        info = engine.step(fill, on_layer_done=on_layer)
+        timed = bool(time_layers_every) and len(steps) % time_layers_every == 0
+        info = engine.step(fill, on_layer_done=on_layer, time_layers=timed)
         if info is not None:
             for rid in info["finished"]:
                 finish_step[int(rid)] = step
@@ -259,13 +272,17 @@ def run_trace(engine, arrival, prompt, eos, max_tokens, fill, sample_every=0, pi
                 if rid not in first_token and c >= prompt[rid]:
                     first_token[rid] = step
             steps.append({"step": step, "S": info["S"], "T": info["T"], "P": info["P"],
-                          "context_lens": info["context_lens"], "q_lens": info["q_lens"], "events": info["events"]})
+                          "context_lens": info["context_lens"], "q_lens": info["q_lens"], "events": info["events"],
+                          "layer_events": info["layer_events"]})
         if nxt >= n and len(finish_step) == n:
             break
     ev1.record(engine.stream)
     torch.cuda.synchronize()
-    for s in steps:   # device time of each step's layer launches
+    for s in steps:   # device time of each step's layer launches (and of their attention calls alone)
         e = s.pop("events")
         s["device_ms"] = e[0].elapsed_time(e[1])
+        le = s.pop("layer_events")
+        if le:
+            s["attention_ms"] = sum(a.elapsed_time(b) for a, b in le)
     return {"steps": steps, "finish_step": finish_step, "first_token_step": first_token, "wall_s": time.perf_counter() - t_wall,
             "stream_ms": ev0.elapsed_time(ev1), "samples": samples}
