@@ -386,6 +386,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     // per-sequence block offsets that thieves search ----
     int64_t local = 0;
     int local_max = 0;
+    if (tid < kDecodeWarps) plan_s[tid] = -1;   // (the scan's barriers order this before the plan)
     for (int s = tid; s < p.S; s += blockDim.x) {
         const int nb = blocks_of(p.context_lens, s, p.max_blocks, p.dev_status, nullptr);
         local += nb;
@@ -394,7 +395,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     local_max = __reduce_max_sync(0xffffffffu, local_max);
     if (lane == 0) sh_max[warp] = local_max;
     int64_t total_nblk;
-    block_scan(local, sh_scan, &total_nblk);
+    const int64_t incl0 = block_scan(local, sh_scan, &total_nblk);
     const int64_t total = total_nblk * Hkv;
     // warps that get a share: all of them, unless the step is too small to
     // give each at least min_blocks blocks (the scan's barriers published sh_max)
@@ -405,14 +406,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int64_t nw = (total + min_blocks - 1) / min_blocks;
     if (nw > p.total_warps) nw = p.total_warps;
     if (nw < 1) nw = 1;
-    if (tid < kDecodeWarps) plan_s[tid] = -1;
-    __syncthreads();
-    int64_t carry = 0;
-    for (int base = 0; base < p.S; base += blockDim.x) {
-        const int s = base + tid;
-        const int nb = s < p.S ? blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) : 0;
-        int64_t tile_total;
-        const int64_t excl = carry + block_scan(nb, sh_scan, &tile_total) - nb;
+    // sequence s holds flat triples [excl * Hkv, (excl + nb) * Hkv): note it as
+    // the start of this CTA's warps whose first triple falls there
+    auto place = [&](int s, int nb, int64_t excl) {
         if (blockIdx.x == 0 && s < p.S) p.prefix[s] = excl;
         if (nb > 0) {
 #pragma unroll
@@ -423,10 +419,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     plan_s[w] = s;
                     plan_off[w] = (int)(lo - excl * Hkv);
                 }
-
             }
         }
-        carry += tile_total;
+    };
+    if (p.S <= (int)blockDim.x) {
+        // one sequence per thread: the first scan already gave its offset
+        if (tid < p.S) place(tid, (int)local, incl0 - local);
+    } else {
+        int64_t carry = 0;
+        for (int base = 0; base < p.S; base += blockDim.x) {
+            const int s = base + tid;
+            const int nb = s < p.S ? blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) : 0;
+            int64_t tile_total;
+            const int64_t excl = carry + block_scan(nb, sh_scan, &tile_total) - nb;
+            place(s, nb, excl);
+            carry += tile_total;
+        }
     }
     if (blockIdx.x == 0 && tid == 0) p.prefix[p.S] = total_nblk;
 
@@ -584,6 +592,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             float m_run[NT], l_run[NT];
             bool seg_fresh = true;
             int piece_j0 = cj, piece_n = 0;
+            // a piece sure to leave a record (it starts inside its range, or
+            // the work ends before the range does) takes its number within
+            // the range when it starts, so the round trip overlaps its blocks
+            bool early_no = false;
+            unsigned long long early_word = 0;   // lane 0: the counter word before this piece's number
 
             // closes the piece of (cs, ch) that ends with block cj of this warp
             auto finish_piece = [&]() {
@@ -630,10 +643,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 }
                 const uint32_t ri = (uint32_t)(wg * p.rec_per_warp + rec_used) + 1u;
                 ++rec_used;
-                // the piece's number within the range first (a round trip that
-                // overlaps the record stores below)
-                unsigned long long before = 0;
-                if (lane == 0) before = atomicAdd(p.seg_cnt + seg, 1ull << 32);
+                // the piece's number within the range: taken when the piece
+                // started, or now (a round trip that overlaps the record
+                // stores below)
+                unsigned long long before = early_word;
+                if (!early_no && lane == 0) before = atomicAdd(p.seg_cnt + seg, 1ull << 32);
                 float *rec = p.part + (size_t)(ri - 1) * p.rec_floats;
 #pragma unroll
                 for (int pn = 0; pn < NT; ++pn) {
@@ -734,6 +748,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     seg_fresh = false;
                     piece_j0 = cj;
                     piece_n = 0;
+                    early_no = cj > 0 || len - i < c_nb - cj;
+                    if (early_no && lane == 0)
+                        early_word = atomicAdd(p.seg_cnt + (size_t)cs * Hkv + ch, 1ull << 32);
                 }
 
                 const uint32_t slot = slot_base + i;
