@@ -68,6 +68,9 @@ constexpr int kMinWarpBlocks = 20;
 // range's list.  A slot is one u64: record (bits 0-23), first block (24-43),
 // block count (44-63).
 constexpr int kSlots = 4;
+// Merges a warp owes, kept in shared memory and run after its work (at most
+// this many; more are merged at once)
+constexpr int kDefer = 8;
 constexpr int kSlotRecBits = 24, kSlotBlkBits = 20;
 
 // Control words, zeroed before every call (u32 each).
@@ -126,7 +129,8 @@ struct DecodeShape {
     static constexpr int ROW_BYTES = D * 2;
     static constexpr int SIDE_BYTES = 2 * ROW_BYTES + 16;
     static constexpr int SIDE_TOTAL = kDecodeWarps * STAGES * SIDE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + SIDE_TOTAL + kDecodeWarps * STAGES * 8 + 256;
+    static constexpr int DEFER_BYTES = kDecodeWarps * kDefer * 16;
+    static constexpr int SMEM_BYTES = 1024 + RING_BYTES + SIDE_TOTAL + kDecodeWarps * STAGES * 8 + 256 + DEFER_BYTES;
 };
 
 __device__ __forceinline__ int blocks_of(const int32_t *context_lens, int s, int max_blocks, int *dev_status,
@@ -220,7 +224,7 @@ __device__ __forceinline__ int locate_seq(const DecodeParams &p, int64_t x, int 
 // exactly, else PKV_DEV_SPLIT is set.  Lane hh folds the (max, sum) pairs of
 // head hh; then every lane accumulates its D/32 output columns of every head,
 // the loads of several records in flight together.
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool kBatch>
 __device__ __forceinline__ void merge_range(const DecodeParams &p, int s, int h, int c_nb, int npieces, int lane) {
     constexpr int HP = 8 * NT, PER = D / 32;
     constexpr uint32_t kFull = 0xffffffffu;
@@ -342,7 +346,39 @@ __device__ __forceinline__ void merge_range(const DecodeParams &p, int s, int h,
             }
         }
     };
-    for (int k = 0; k < n; ++k) add_record(rec_of(__shfl_sync(kFull, mine, k)));
+    if constexpr (kBatch) {
+        // two records' loads in flight together (outside the streaming loop
+        // there are registers to spare)
+        for (int k0 = 0; k0 < n; k0 += 2) {
+            const bool two = k0 + 1 < n;
+            const float *rec0 = rec_of(__shfl_sync(kFull, mine, k0 & 31));
+            const float *rec1 = two ? rec_of(__shfl_sync(kFull, mine, (k0 + 1) & 31)) : rec0;
+            float a0[HP][PER], a1[HP][PER], f0[HP], f1[HP];
+#pragma unroll
+            for (int hh = 0; hh < HP; ++hh) {
+                if (hh < G) {
+                    f0[hh] = __ldcg(rec0 + hh);
+                    f1[hh] = __ldcg(rec1 + hh);
+#pragma unroll
+                    for (int k2 = 0; k2 < PER; ++k2) {
+                        a0[hh][k2] = __ldcg(rec0 + 2 * G + hh * D + lane + 32 * k2);
+                        a1[hh][k2] = __ldcg(rec1 + 2 * G + hh * D + lane + 32 * k2);
+                    }
+                }
+            }
+#pragma unroll
+            for (int hh = 0; hh < HP; ++hh) {
+                if (hh < G) {
+                    const float g0 = exp2_approx(f0[hh] - Mh[hh]) * invL[hh];
+                    const float g1 = two ? exp2_approx(f1[hh] - Mh[hh]) * invL[hh] : 0.f;
+#pragma unroll
+                    for (int k2 = 0; k2 < PER; ++k2) o[hh][k2] += g0 * a0[hh][k2] + g1 * a1[hh][k2];
+                }
+            }
+        }
+    } else {
+        for (int k = 0; k < n; ++k) add_record(rec_of(__shfl_sync(kFull, mine, k)));
+    }
     for (uint32_t walk = rest; walk != 0u;) {
         const float *rec = rec_of(walk);
         walk = __float_as_uint(__ldcg(rec + tr));
@@ -373,6 +409,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int *plan_s = reinterpret_cast<int *>(sh_scan + kDecodeWarps);   // segment holding each warp's first block
     int *plan_off = plan_s + kDecodeWarps;
     int *sh_max = plan_off + kDecodeWarps;                           // per-warp longest sequence, in blocks
+    int4 *defer = reinterpret_cast<int4 *>(reinterpret_cast<uint8_t *>(sh_scan) + 256);   // merges owed, per warp
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
@@ -485,6 +522,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     bool seen_ready = false;    // every CTA has published its range words
     int rec_used = 0;           // records of this warp's own set taken so far
     uint32_t warp_blocks = 0;   // blocks this warp has streamed (checked against the plan at exit)
+    int4 *wdefer = defer + warp * kDefer;
+    int n_defer = 0;            // merges this warp owes (run after its work)
 
     // Work: first the warp's own range (claimed in batches), then stolen pieces.
     int64_t x0 = lo_w;          // flat start of the current work
@@ -698,8 +737,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 }
                 after = __shfl_sync(0xffffffffu, after, 0);
                 if ((uint32_t)after == (uint32_t)c_nb) {
-                    __syncwarp();
-                    merge_range<T, D, NT>(p, cs, ch, c_nb, (int)(after >> 32), lane);
+                    // this piece completed the range: merge it after the
+                    // warp's work, so the warp keeps streaming now (groups of
+                    // more than 8 heads, or a full list, merge at once)
+                    if (NT == 1 && n_defer < kDefer) {
+                        if (lane == 0) wdefer[n_defer] = make_int4(cs, ch, c_nb, (int)(after >> 32));
+                        ++n_defer;
+                    } else {
+                        __syncwarp();
+                        merge_range<T, D, NT, false>(p, cs, ch, c_nb, (int)(after >> 32), lane);
+                    }
                 }
             };
 
@@ -1034,6 +1081,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         own = false;
         s0 = locate_seq(p, x0, lane);
         off0 = (int)(x0 - __ldcg(p.prefix + s0) * Hkv);
+    }
+
+    // ---- the merges this warp owes ----
+    __syncwarp();
+    for (int k = 0; k < n_defer; ++k) {
+        const int4 e = wdefer[k];
+        merge_range<T, D, NT, true>(p, e.x, e.y, e.z, e.w, lane);
     }
 
     // ---- exit: every block of the plan must have been streamed exactly once
