@@ -21,9 +21,10 @@
 //    registers it in the range's slot array (record, first block, block
 //    count; pieces past the fourth go on a per-range list instead).  A
 //    per-range counter word counts the pieces registered and the blocks
-//    finished; the warp that finishes the range's last block reads the slots
-//    in one round trip and combines the records by log-sum-exp, with the
-//    loads of several records in flight together.  The counters and list
+//    finished; the warp that finishes the range's last block notes the range
+//    and, after its own work, reads the slots in one round trip and combines
+//    the records by log-sum-exp, with the loads of several records in flight
+//    together.  The counters and list
 //    heads sit in a control region at the front of the workspace that a small
 //    kernel zeroes just before every call, so nothing read from the workspace
 //    depends on what the memory held before the call.
