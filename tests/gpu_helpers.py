@@ -15,6 +15,21 @@ import torch
 import oracle
 
 ATOL = 2e-3
+# Two splits of the same decode agree to fp32 rounding plus the rounding of
+# the softmax weights P, which each split forms against its own running
+# maximum as a 16-bit value and its 16-bit residual (about 16 significant
+# bits): |a - b| <= SPLIT_ATOL + SPLIT_RTOL * |b|.  A range merged with a
+# piece missing or doubled is off by 1e-3 or more.
+SPLIT_ATOL = 2e-6
+SPLIT_RTOL = 2.0 ** -15
+
+
+def split_excess(a, b):
+    """How far two decode outputs (torch tensors) of different splits exceed
+    the split tolerance: max of |a - b| - (SPLIT_ATOL + SPLIT_RTOL |b|), NaN
+    counted as a large excess.  <= 0 means they agree."""
+    d = (a - b).abs() - (SPLIT_ATOL + SPLIT_RTOL * b.abs())
+    return float(d.nan_to_num(1e9).max())
 TORCH_DT = {"fp16": torch.float16, "bf16": torch.bfloat16}
 MANT_BITS = {"fp16": 10, "bf16": 7}
 
