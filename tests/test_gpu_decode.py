@@ -232,7 +232,9 @@ def test_decode_sequence_alone_equals_sequence_in_batch(cuda_lib):
     full = run_decode(ds, ds.q, ds.block_tables, ds.context_lens - 1, "fp32")
     for s in [0, 17, 63]:
         alone = run_decode(ds, ds.q[s:s + 1], ds.block_tables[s:s + 1], ds.context_lens[s:s + 1] - 1, "fp32")
-        np.testing.assert_allclose(out_to_f64(alone[0]), out_to_f64(full[s]), rtol=0, atol=1e-5)
+        # a sequence alone and in a batch is split differently: fp32 rounding
+        # plus the rounding of P against each split's running maxima
+        np.testing.assert_allclose(out_to_f64(alone[0]), out_to_f64(full[s]), rtol=SPLIT_RTOL, atol=1e-5)
 
 
 def test_decode_flags_bad_block_ids_and_contexts_without_faulting(cuda_lib):
