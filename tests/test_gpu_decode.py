@@ -287,3 +287,50 @@ def test_workspace_size_is_independent_of_contexts(cuda_lib):
     assert decode_workspace_size(256, 8, 8, 128) < a < decode_workspace_size(256, 64, 8, 128) < \
         decode_workspace_size(256, 128, 8, 128)
     assert decode_workspace_size(256, 32, 8, 64) < a
+
+
+def test_decode_with_the_smallest_accepted_workspace(cuda_lib):
+    """The call accepts a workspace down to two partial records per warp; a
+    warp then steals only when its own share left no piece.  The smallest
+    accepted size is found by bisection (a smaller workspace is rejected
+    before anything is enqueued); it is the fixed part plus two records per
+    warp, eight fewer per warp than the recommended size.  The 8B-shaped step
+    run on it still matches the oracle on every sequence."""
+    from paged_kv_cache_tables_gb300 import PkvError
+    st = make_step("llama8b")
+    ds = DeviceStep(st)
+    cl = ds.context_lens - 1
+    out = torch.empty((st.S, st.Hq, st.d), dtype=torch.float32, device="cuda")
+    big = decode_workspace_size(st.S, st.Hq, st.Hkv, st.d)
+    pool = torch.empty(big, dtype=torch.uint8, device="cuda")
+
+    def accepted(n):
+        try:
+            paged_decode_attention(out, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, cl, workspace=pool[:n],
+                                   dev_status=ds.status)
+            return True
+        except PkvError as e:
+            assert e.status == -3      # PKV_ERR_WORKSPACE, nothing enqueued
+            return False
+
+    lo, hi = 16, big                   # accepted(hi), not accepted(lo)
+    assert accepted(hi) and not accepted(lo)
+    while hi - lo > 16:
+        mid = (lo + hi) // 2 // 16 * 16
+        if accepted(mid):
+            hi = mid
+        else:
+            lo = mid
+    assert not accepted(hi - 1)
+    G = st.Hq // st.Hkv
+    rec_bytes = 4 * (((2 * G + G * st.d + 3) & ~3) + 4)
+    n_warps = 8 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert big - hi == 8 * n_warps * rec_bytes
+    out.fill_(float("nan"))
+    paged_decode_attention(out, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, cl, workspace=pool[:hi],
+                           dev_status=ds.status)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) == 0
+    ref = oracle_decode_all(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens - 1, st.dtype)
+    err = assert_close(out_to_f64(out), ref, "fp32", what="smallest workspace (%d bytes)" % hi)
+    print("smallest accepted workspace %d bytes (recommended %d), max-abs %.3g" % (hi, big, err))
