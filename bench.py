@@ -44,8 +44,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # append fused): dram__bytes_read.sum + dram__bytes_write.sum from one ncu
 # capture of that launch, valid for the decode source with this SHA-1 and
 # reported as null once it changes (or for another workload).
-DECODE_TRAFFIC_BYTES = 1454913024 + 5327872
-DECODE_TRAFFIC_SHA1 = "d144d6066d37b7cfff9cfd8d1180712638af2ccd"
+DECODE_TRAFFIC_BYTES = 1454519040 + 4899072
+DECODE_TRAFFIC_SHA1 = "1b9949a84613094f1b970c22e62458d3ff87f828"
 
 
 # launches per decode call: the control-region clear and the decode kernel

@@ -415,9 +415,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
 
-    // inputs may come from the previous kernel on the stream (the append, or
-    // the clear of the control region)
-    pdl_wait_primary();
+    // Launched early behind the clear of the control region, which starts
+    // only once everything before it on the stream is complete.  So the plan
+    // below may read the inputs and write the workspace past the control
+    // region and the rows of empty sequences before waiting; the control
+    // region is touched only after the wait.
     pdl_launch_dependents();
 
     // ---- plan: total blocks, this CTA's warp starts; CTA 0 publishes the
@@ -488,6 +490,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int64_t lo_w = wg < nw ? range_lo(wg, total, nw) : total;
     const int n_own = wg < nw ? (int)(range_lo(wg + 1, total, nw) - lo_w) : 0;
     if (lane == 0) p.ranges[wg] = rw_make(0, n_own);
+    // the clear of the control region is complete from here on
+    pdl_wait_primary();
     // publish: the barrier orders every thread's range word and prefix
     // stores before thread 0's fence, which makes them visible at GPU scope
     // before the ready count moves (only thread 0 waits for it)
