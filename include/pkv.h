@@ -11,6 +11,11 @@
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   Every device entry point only enqueues work on that stream and returns;
  *   results are ready when the stream reaches that point.
+ * - Kernels are launched with programmatic dependent launch: one may start
+ *   while the kernel before it on the stream is still running, and waits for
+ *   that kernel to finish before it touches anything the kernel may write.
+ *   The one exception is context_lens in the decode entry points (see
+ *   pkv_paged_decode_attention).
  * - Return value: PKV_OK (0) or a negative PKV_ERR_* code.  Arguments are
  *   validated on the host before any launch; on an error nothing is enqueued.
  *   PKV_ERR_CUDA means a CUDA call failed; pkv_last_cuda_error() names it.
@@ -165,6 +170,13 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  *                  same call.  Owned by the caller; must not be used by another
  *                  call that may run concurrently.
  *   dev_status     device int or NULL (see conventions)
+ * When num_seqs <= 256 the decode kernel reads context_lens to plan its work
+ * before it waits for the work enqueued ahead of the call.  By then that work
+ * has ended, or has signalled its dependents through programmatic dependent
+ * launch.  So context_lens must not be written by a kernel just before the
+ * call that signals its dependents before that write (the library's own
+ * kernels never write it).  Everything else is read and written only after
+ * the wait.
  * One persistent kernel: every warp starts on an equal share of the
  * (sequence, KV head, block) list, and warps that finish early take over the
  * far half of busier warps' unclaimed blocks.  A (sequence, KV head) range

@@ -415,12 +415,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
 
-    // Launched early behind the clear of the control region, which starts
-    // only once everything before it on the stream is complete.  So the plan
-    // below may read the inputs and write the workspace past the control
-    // region and the rows of empty sequences before waiting; the control
-    // region is touched only after the wait.
+    // The kernel may start while the clear of the control region still
+    // waits for the kernel before it on the stream (which may be the last
+    // call, still using this workspace).  A one-pass plan (a sequence per
+    // thread) reads only context_lens and writes only shared memory before
+    // it waits; a longer plan waits first, since it writes the prefix array
+    // as it goes.
     pdl_launch_dependents();
+    const bool one_pass = p.S <= (int)blockDim.x;
+    if (!one_pass) pdl_wait_primary();
 
     // ---- plan: total blocks, this CTA's warp starts; CTA 0 publishes the
     // per-sequence block offsets that thieves search ----
@@ -449,7 +452,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     // sequence s holds flat triples [excl * Hkv, (excl + nb) * Hkv): note it as
     // the start of this CTA's warps whose first triple falls there
     auto place = [&](int s, int nb, int64_t excl) {
-        if (blockIdx.x == 0 && s < p.S) p.prefix[s] = excl;
+        if (blockIdx.x == 0 && s < p.S && !one_pass) p.prefix[s] = excl;
         if (nb > 0) {
 #pragma unroll
             for (int w = 0; w < kDecodeWarps; ++w) {
@@ -476,6 +479,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             carry += tile_total;
         }
     }
+    if (one_pass) {
+        pdl_wait_primary();
+        if (blockIdx.x == 0 && tid < p.S) p.prefix[tid] = incl0 - local;
+    }
     if (blockIdx.x == 0 && tid == 0) p.prefix[p.S] = total_nblk;
 
     // sequences with an empty context get all-zero rows
@@ -490,8 +497,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int64_t lo_w = wg < nw ? range_lo(wg, total, nw) : total;
     const int n_own = wg < nw ? (int)(range_lo(wg + 1, total, nw) - lo_w) : 0;
     if (lane == 0) p.ranges[wg] = rw_make(0, n_own);
-    // the clear of the control region is complete from here on
-    pdl_wait_primary();
     // publish: the barrier orders every thread's range word and prefix
     // stores before thread 0's fence, which makes them visible at GPU scope
     // before the ready count moves (only thread 0 waits for it)
@@ -1112,8 +1117,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 // It waits for the previous kernel on the stream (which may be the previous
 // call, still using the region) and lets the decode kernel launch at once.
 __global__ void __launch_bounds__(256) decode_clear_kernel(uint4 *ctl, int n16) {
-    pdl_wait_primary();
     pdl_launch_dependents();
+    pdl_wait_primary();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += gridDim.x * blockDim.x)
         ctl[i] = make_uint4(0u, 0u, 0u, 0u);
 }
