@@ -334,3 +334,35 @@ def test_decode_with_the_smallest_accepted_workspace(cuda_lib):
     ref = oracle_decode_all(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens - 1, st.dtype)
     err = assert_close(out_to_f64(out), ref, "fp32", what="smallest workspace (%d bytes)" % hi)
     print("smallest accepted workspace %d bytes (recommended %d), max-abs %.3g" % (hi, big, err))
+
+
+def test_decode_back_to_back_calls_of_different_shapes_share_a_workspace(cuda_lib):
+    """Decode calls of two different steps (the 1B shape with 64 sequences,
+    the 8B shape with 96) alternate on one workspace and one stream, twelve
+    times each, with no synchronisation between them.  Each call may start
+    and plan while the previous one (another shape, same workspace) still
+    runs.  Every call's context lengths are computed by the kernel just
+    before it.  Every output matches its oracle on every sequence, and the
+    status word stays clean."""
+    sa = make_step("llama1b", S=64)
+    sb = make_step("llama8b", seed=7, S=96, NB=16384)
+    da, db = DeviceStep(sa), DeviceStep(sb)
+    size = max(decode_workspace_size(s.S, s.Hq, s.Hkv, s.d) for s in (sa, sb))
+    ws = torch.empty(size, dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for k in range(12):
+        for st, ds in ((sa, da), (sb, db)):
+            out = torch.full((st.S, st.Hq, st.d), float("nan"), dtype=torch.float32, device="cuda")
+            cl = ds.context_lens - 1          # written by the kernel right before the call
+            paged_decode_attention(out, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, cl, workspace=ws,
+                                   dev_status=status)
+            outs.append((st, out))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    refs = {id(st): oracle_decode_all(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens - 1, st.dtype)
+            for st in (sa, sb)}
+    worst = 0.0
+    for k, (st, out) in enumerate(outs):
+        worst = max(worst, assert_close(out_to_f64(out), refs[id(st)], "fp32", what="call %d (%s)" % (k, st.name)))
+    print("24 alternating calls on one workspace: max-abs %.3g" % worst)
