@@ -185,7 +185,12 @@ size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads
  * Which blocks are taken over depends on timing, so the last bits of the
  * output may differ from call to call; with the environment variable
  * PKV_DETERMINISTIC=1 (read at every call) nothing is taken over and equal
- * inputs give equal bits.
+ * inputs give equal bits.  With head_dim 64, groups of at most 4 query heads
+ * and an even num_kv_heads, a unit of work can be a block of two adjacent KV
+ * heads (one 4 KB run of K and one of V in the cache), with ranges per
+ * (sequence, KV-head pair).  The call takes that form for steps of at least
+ * 256 such ranges (512 when max_blocks_per_seq > 128) whose layout fits the
+ * workspace; pkv_decode_workspace_size covers both forms.
  */
 int pkv_paged_decode_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                                const int32_t *block_tables, int max_blocks_per_seq,
@@ -334,8 +339,11 @@ int pkv_mixed_split(int num_sms, const int32_t *cu_seqlens, int num_prefill, con
  * - Limits: num_seqs <= PKV_STATIC_MAX_SEQS, and the smallest workspace the
  *   shape accepts must fit in PKV_STATIC_SCRATCH_BYTES.  On a GB300 (152
  *   SMs, 1216 warps) that smallest workspace is about
- *       44 * num_seqs * num_kv_heads + 8 * num_seqs + 10 KB
- *       + 2432 * 4 * (2G + G * head_dim + 8)  bytes,  G = num_q_heads / num_kv_heads.
+ *       44 * num_seqs * U + 8 * num_seqs + 10 KB
+ *       + 2432 * 4 * (2G + G * head_dim + 8)  bytes,  G = num_q_heads / U,
+ *   with U = num_kv_heads; when head_dim is 64, the group has at most 4
+ *   query heads and num_kv_heads is even, also with U = num_kv_heads / 2
+ *   (two adjacent KV heads as one unit), whichever is less.
  *   So with num_seqs = 16384 the largest num_kv_heads that fits is 27 for
  *   head_dim 128 and G = 4 (452,000 (sequence, KV head) pairs), 20 for G = 8,
  *   and 6 for G = 16 (whose records alone take 20.3 MB); with 256 sequences

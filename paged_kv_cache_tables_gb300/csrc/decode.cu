@@ -395,11 +395,22 @@ __device__ __forceinline__ void merge_range(const DecodeParams &p, int s, int h,
     }
 }
 
-template <typename T, int D, int NT>
+// PAIR (head_dim 64 only): one unit of work is a block of two adjacent KV
+// heads, whose tiles lie next to each other in the cache (4 KB of K and 4 KB
+// of V instead of 2 KB each), held in the registers and ring of the
+// head_dim-128 form: the first KV head's 64 dimensions in the first 64-column
+// half, the second's in the other.  p.Hkv and p.G then count KV-head pairs
+// and the 2G query heads of a pair; the query rows of the first head are zero
+// against the second half of K and the other way round, so the product S
+// holds each head's own scores, and of O^T += V^T P^T a row only uses the
+// half of its own KV head.  D is the register width (128), DO the head_dim.
+template <typename T, int D, int NT, bool PAIR>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     paged_decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv) {
+    static_assert(!PAIR || (D == 128 && NT == 1), "paired heads use the 128-wide single-tile form");
     using Sh = DecodeShape<D, NT>;
+    constexpr int DO = PAIR ? 64 : D;   // head_dim of q, out, the caches' rows and the records
     constexpr int STAGES = Sh::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -414,6 +425,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = p.Hkv, G = p.G;
+    // query row r of a unit is a real head, and (paired) register group x
+    // (an mt or kk index) belongs to r's own KV head
+    auto own_half = [&](int r, int x) { return r < G && (!PAIR || ((2 * r >= G) == (x >= D / 32))); };
 
     // The kernel may start while the clear of the control region still
     // waits for the kernel before it on the stream (which may be the last
@@ -488,7 +502,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     // sequences with an empty context get all-zero rows
     for (int s = blockIdx.x; s < p.S; s += gridDim.x) {
         if (blocks_of(p.context_lens, s, p.max_blocks, nullptr, nullptr) != 0) continue;
-        for (int e = tid; e < p.Hq * D; e += blockDim.x) store_out<T>(p.out, p.out_dtype, (int64_t)s * p.Hq * D + e, 0.f);
+        for (int e = tid; e < p.Hq * DO; e += blockDim.x) store_out<T>(p.out, p.out_dtype, (int64_t)s * p.Hq * DO + e, 0.f);
     }
 
     // every warp publishes its range word; the CTA then counts itself ready
@@ -569,10 +583,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             };
             auto issue = [&](uint32_t slot, int blk) {
                 if (lane == 0) {
-                    int row = (blk * Hkv + ph) * 16;
+                    // cache row of the tile (its first KV head's, when paired)
+                    int row = (blk * Hkv + ph) * 16 * (PAIR ? 2 : 1);
                     if (blk < 0 || blk >= p.num_blocks) {
                         set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                        row = p.num_blocks * Hkv * 16;   // past the end: the load fills zeros
+                        row = p.num_blocks * Hkv * 16 * (PAIR ? 2 : 1);   // past the end: the load fills zeros
                     }
                     const int stage = (int)(slot % STAGES);
                     uint64_t *bar = &wbar[stage];
@@ -584,8 +599,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     uint8_t *vdst = kdst + Sh::TILE_BYTES;
 #pragma unroll
                     for (int hf = 0; hf < Sh::HALVES; ++hf) {
-                        tma_load_2d(kdst + hf * Sh::HALF_BYTES, &tk, hf * 64, row, bar, policy);
-                        tma_load_2d(vdst + hf * Sh::HALF_BYTES, &tv, hf * 64, row, bar, policy);
+                        // a half is 64 columns of the tile, or (paired) the next KV head's 16 rows
+                        const int x = PAIR ? 0 : hf * 64, y = PAIR ? row + 16 * hf : row;
+                        tma_load_2d(kdst + hf * Sh::HALF_BYTES, &tk, x, y, bar, policy);
+                        tma_load_2d(vdst + hf * Sh::HALF_BYTES, &tv, x, y, bar, policy);
                     }
                     if (with_row) {
                         uint8_t *sd = wside + stage * Sh::SIDE_BYTES;
@@ -667,14 +684,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                         const int ha = pn * 8 + 2 * t4, hb = ha + 1;
 #pragma unroll
                         for (int mt = 0; mt < D / 16; ++mt) {
-                            const int d0 = mt * 16 + g;
-                            if (ha < G) {
-                                const int64_t o = ((int64_t)cs * p.Hq + head0 + ha) * D;
+                            const int d0 = (PAIR ? (mt & 3) : mt) * 16 + g;
+                            if (own_half(ha, mt)) {
+                                const int64_t o = ((int64_t)cs * p.Hq + head0 + ha) * DO;
                                 store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][0] * inv_lo);
                                 store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][2] * inv_lo);
                             }
-                            if (hb < G) {
-                                const int64_t o = ((int64_t)cs * p.Hq + head0 + hb) * D;
+                            if (own_half(hb, mt)) {
+                                const int64_t o = ((int64_t)cs * p.Hq + head0 + hb) * DO;
                                 store_out<T>(p.out, p.out_dtype, o + d0, acc[mt][pn][1] * inv_hi);
                                 store_out<T>(p.out, p.out_dtype, o + d0 + 8, acc[mt][pn][3] * inv_hi);
                             }
@@ -709,14 +726,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     const int ha = pn * 8 + 2 * t4, hb = ha + 1;
 #pragma unroll
                     for (int mt = 0; mt < D / 16; ++mt) {
-                        const int d0 = mt * 16 + g;
-                        if (ha < G) {
-                            racc[ha * D + d0] = acc[mt][pn][0];
-                            racc[ha * D + d0 + 8] = acc[mt][pn][2];
+                        const int d0 = (PAIR ? (mt & 3) : mt) * 16 + g;
+                        if (own_half(ha, mt)) {
+                            racc[ha * DO + d0] = acc[mt][pn][0];
+                            racc[ha * DO + d0 + 8] = acc[mt][pn][2];
                         }
-                        if (hb < G) {
-                            racc[hb * D + d0] = acc[mt][pn][1];
-                            racc[hb * D + d0 + 8] = acc[mt][pn][3];
+                        if (own_half(hb, mt)) {
+                            racc[hb * DO + d0] = acc[mt][pn][1];
+                            racc[hb * DO + d0 + 8] = acc[mt][pn][3];
                         }
                     }
                 }
@@ -755,7 +772,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                         ++n_defer;
                     } else {
                         __syncwarp();
-                        merge_range<T, D, NT, false>(p, cs, ch, c_nb, (int)(after >> 32), lane);
+                        merge_range<T, DO, NT, false>(p, cs, ch, c_nb, (int)(after >> 32), lane);
                     }
                 }
             };
@@ -777,18 +794,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                 if (seg_fresh) {
                     // query fragments of (cs, ch): rows = heads of the group (padded to 16)
                     const uint32_t *qbase = reinterpret_cast<const uint32_t *>(
-                        static_cast<const T *>(p.q) + ((int64_t)cs * p.Hq + (int64_t)ch * G) * D);
+                        static_cast<const T *>(p.q) + ((int64_t)cs * p.Hq + (int64_t)ch * G) * DO);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const int c0 = (kk * 16 + 2 * t4) >> 1;
-                        qa[kk][0] = g < G ? __ldg(qbase + g * (D / 2) + c0) : 0u;
-                        qa[kk][2] = g < G ? __ldg(qbase + g * (D / 2) + c0 + 4) : 0u;
+                        // paired: a query row meets only its own KV head's half of K
+                        const int c0 = ((PAIR ? (kk & 3) : kk) * 16 + 2 * t4) >> 1;
+                        const bool use = own_half(g, kk);
+                        qa[kk][0] = use ? __ldg(qbase + g * (DO / 2) + c0) : 0u;
+                        qa[kk][2] = use ? __ldg(qbase + g * (DO / 2) + c0 + 4) : 0u;
                         if constexpr (NT == 1) {   // group of at most 8 heads: rows 8..15 are padding
                             qa[kk][1] = 0u;
                             qa[kk][3] = 0u;
                         } else {
-                            qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0) : 0u;
-                            qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (D / 2) + c0 + 4) : 0u;
+                            qa[kk][1] = g + 8 < G ? __ldg(qbase + (g + 8) * (DO / 2) + c0) : 0u;
+                            qa[kk][3] = g + 8 < G ? __ldg(qbase + (g + 8) * (DO / 2) + c0 + 4) : 0u;
                         }
                     }
 #pragma unroll
@@ -833,8 +852,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                         const int blk = *reinterpret_cast<const int *>(sd + 2 * Sh::ROW_BYTES);
                         if (blk >= 0 && blk < p.num_blocks) {
                             uint8_t *cache = static_cast<uint8_t *>(which ? p.v_cache : p.k_cache);
-                            *reinterpret_cast<uint4 *>(cache + (((size_t)blk * Hkv + ch) * 16 + r) * Sh::ROW_BYTES +
-                                                       c * 16) = val;
+                            // paired: chunks 0-7 are the first KV head's row, 8-15 the second's
+                            const size_t crow = PAIR ? ((size_t)blk * 2 * Hkv + 2 * ch + (c >> 3)) * 16 + r
+                                                     : ((size_t)blk * Hkv + ch) * 16 + r;
+                            const int ccol = PAIR ? (c & 7) : c;
+                            *reinterpret_cast<uint4 *>(cache + crow * (DO * 2) + ccol * 16) = val;
                         }
                     }
                     __syncwarp();
@@ -1097,7 +1119,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     __syncwarp();
     for (int k = 0; k < n_defer; ++k) {
         const int4 e = wdefer[k];
-        merge_range<T, D, NT, true>(p, e.x, e.y, e.z, e.w, lane);
+        merge_range<T, DO, NT, true>(p, e.x, e.y, e.z, e.w, lane);
     }
 
     // ---- exit: every block of the plan must have been streamed exactly once
@@ -1123,13 +1145,13 @@ __global__ void __launch_bounds__(256) decode_clear_kernel(uint4 *ctl, int n16) 
         ctl[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <typename T, int D, int NT>
+template <typename T, int D, int NT, bool PAIR = false>
 static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensorMap &tv, int grid,
                          size_t clear_bytes, cudaStream_t stream) {
     using Sh = DecodeShape<D, NT>;
     static unsigned long long attr_set = 0;   // per instantiation and device
     if (!done_on_device(&attr_set)) {
-        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, NT>,
+        cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<T, D, NT, PAIR>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
         if (e != cudaSuccess) return cuda_fail(e);
         mark_done_on_device(&attr_set);
@@ -1140,7 +1162,7 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
     cudaError_t e = launch_pdl(decode_clear_kernel, dim3(cgrid), dim3(256), 0, stream,
                                reinterpret_cast<uint4 *>(prm.ctl), n16);
     if (e == cudaSuccess)
-        e = launch_pdl(paged_decode_kernel<T, D, NT>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES, stream,
+        e = launch_pdl(paged_decode_kernel<T, D, NT, PAIR>, dim3(grid), dim3(kDecodeWarps * 32), Sh::SMEM_BYTES, stream,
                        prm, tk, tv);
     if (e == cudaSuccess) e = cudaGetLastError();
     return e == cudaSuccess ? PKV_OK : cuda_fail(e);
@@ -1191,14 +1213,42 @@ constexpr int kRecordsRecommended = 10;
 static size_t records_min(int total_warps) { return (size_t)kRecordsMin * total_warps; }
 static size_t records_recommended(int total_warps) { return (size_t)kRecordsRecommended * total_warps; }
 
+// head_dim 64 with groups of at most 4 query heads and an even number of KV
+// heads can run two adjacent KV heads as one unit (the kernel's PAIR form):
+// the kernel then sees num_kv_heads / 2 units of 2G query heads each.  A unit
+// then streams twice the bytes at twice the arithmetic, which pays while the
+// warps have long shares (the step is bound by bandwidth), and costs in a
+// small step, where each warp's few units are a chain of round trips.  So it
+// is used from 256 sequence x KV-pair ranges on, or from 512 when the block
+// tables are wider than 128 blocks: contexts past 2,048 tokens, whose long
+// ranges a small step cuts into many pieces.
+static bool pair_eligible(int num_q_heads, int num_kv_heads, int head_dim) {
+    return head_dim == 64 && num_kv_heads % 2 == 0 && num_q_heads / num_kv_heads <= 4;
+}
+
+static bool pair_wanted(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int max_blocks_per_seq) {
+    if (!pair_eligible(num_q_heads, num_kv_heads, head_dim)) return false;
+    const int64_t ranges = (int64_t)num_seqs * (num_kv_heads / 2);
+    return ranges >= (max_blocks_per_seq > 128 ? 512 : 256);
+}
+
+static size_t workspace_bytes_for(int num_seqs, int num_q_heads, int units, int head_dim, int nw, size_t records) {
+    return decode_layout(num_seqs, units, nw).fixed +
+           records * (size_t)record_floats(num_q_heads / units, head_dim) * sizeof(float);
+}
+
+// The smallest workspace a call accepts (the paired form falls back to the
+// single-head one when its own layout does not fit).
 size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim) {
     if (num_seqs < 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return 0;
     int sms = 0;
     if (current_sm_count(&sms) != PKV_OK) return 0;
     const int nw = sms * kDecodeWarps;
-    const int G = num_q_heads / num_kv_heads;
-    return decode_layout(num_seqs, num_kv_heads, nw).fixed +
-           records_min(nw) * (size_t)record_floats(G, head_dim) * sizeof(float);
+    size_t need = workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads, head_dim, nw, records_min(nw));
+    if (pair_eligible(num_q_heads, num_kv_heads, head_dim))
+        need = std::min(need, workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads / 2, head_dim, nw,
+                                                  records_min(nw)));
+    return need;
 }
 
 }  // namespace pkv
@@ -1209,9 +1259,12 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
     int sms = 0;
     if (current_sm_count(&sms) != PKV_OK) return 0;
     const int nw = sms * kDecodeWarps;
-    const int G = num_q_heads / num_kv_heads;
-    return decode_layout(num_seqs, num_kv_heads, nw).fixed +
-           records_recommended(nw) * (size_t)record_floats(G, head_dim) * sizeof(float);
+    // large enough for either form
+    size_t need = workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads, head_dim, nw, records_recommended(nw));
+    if (pair_eligible(num_q_heads, num_kv_heads, head_dim))
+        need = std::max(need, workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads / 2, head_dim, nw,
+                                                  records_recommended(nw)));
+    return need;
 }
 
 namespace pkv {
@@ -1246,17 +1299,33 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     int sms = 0;
     int rc = current_sm_count(&sms);
     if (rc != PKV_OK) return rc;
-    // enough warps for the largest possible total, at most one CTA per SM
-    const int64_t upper = (int64_t)num_seqs * num_kv_heads * max_blocks_per_seq;
-    int grid = (int)((upper + kDecodeWarps - 1) / kDecodeWarps);
-    if (grid > sms) grid = sms;
-    if (max_sms > 0 && grid > max_sms) grid = max_sms;
-    if (grid < 1) grid = 1;
-    const int total_warps = grid * kDecodeWarps;
+    // the kernel's units: KV heads, or pairs of adjacent KV heads
+    bool pair = pair_wanted(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+    int units = 0, Gu = 0, total_warps = 0, grid = 0;
+    int64_t upper = 0;
+    DecodeLayout lay;
+    size_t rec_bytes = 0;
+    for (;;) {
+        units = pair ? num_kv_heads / 2 : num_kv_heads;
+        Gu = num_q_heads / units;
+        // enough warps for the largest possible total, at most one CTA per SM
+        upper = (int64_t)num_seqs * units * max_blocks_per_seq;
+        grid = (int)((upper + kDecodeWarps - 1) / kDecodeWarps);
+        if (grid > sms) grid = sms;
+        if (max_sms > 0 && grid > max_sms) grid = max_sms;
+        if (grid < 1) grid = 1;
+        total_warps = grid * kDecodeWarps;
+        lay = decode_layout(num_seqs, units, total_warps);
+        rec_bytes = (size_t)record_floats(Gu, head_dim) * sizeof(float);
+        // the paired form falls back to single heads when its layout does not fit
+        if (pair && workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) {
+            pair = false;
+            continue;
+        }
+        break;
+    }
     // range offsets are 32-bit fields
     if (upper / total_warps + 1 >= ((int64_t)1 << 30)) return PKV_ERR_UNSUPPORTED;
-    const DecodeLayout lay = decode_layout(num_seqs, num_kv_heads, total_warps);
-    const size_t rec_bytes = (size_t)record_floats(G, head_dim) * sizeof(float);
     if (workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) return PKV_ERR_WORKSPACE;
     // records per warp (record numbers live in 24-bit slot fields)
     size_t per_warp = (workspace_bytes - lay.fixed) / rec_bytes / total_warps;
@@ -1287,12 +1356,12 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     prm.max_blocks = max_blocks_per_seq;
     prm.num_blocks = num_blocks;
     prm.Hq = num_q_heads;
-    prm.Hkv = num_kv_heads;
-    prm.G = G;
+    prm.Hkv = units;
+    prm.G = Gu;
     prm.scale_log2 = scale * 1.4426950408889634f;
     prm.out_dtype = out_dtype;
     prm.total_warps = total_warps;
-    prm.rec_floats = record_floats(G, head_dim);
+    prm.rec_floats = record_floats(Gu, head_dim);
     prm.rec_per_warp = (int)per_warp;
     // PKV_DETERMINISTIC=1: no stealing, so the split of every range is fixed
     // by the contexts alone and the output bits repeat from call to call
@@ -1304,6 +1373,9 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     prm.v_cache = const_cast<void *>(v_cache);
     cudaStream_t st = stream;
     const bool wide = G > 8;
+    if (pair)
+        return dtype == PKV_DTYPE_BF16 ? launch_decode<__nv_bfloat16, 128, 1, true>(prm, tk, tv, grid, lay.clear_bytes, st)
+                                       : launch_decode<__half, 128, 1, true>(prm, tk, tv, grid, lay.clear_bytes, st);
     if (dtype == PKV_DTYPE_BF16) {
         if (head_dim == 128)
             return wide ? launch_decode<__nv_bfloat16, 128, 2>(prm, tk, tv, grid, lay.clear_bytes, st)

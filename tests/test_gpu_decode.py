@@ -286,7 +286,9 @@ def test_workspace_size_is_independent_of_contexts(cuda_lib):
     # partial records hold exactly the G heads of a group
     assert decode_workspace_size(256, 8, 8, 128) < a < decode_workspace_size(256, 64, 8, 128) < \
         decode_workspace_size(256, 128, 8, 128)
-    assert decode_workspace_size(256, 32, 8, 64) < a
+    # head_dim 64: records of the 2G heads of a KV-head pair while G <= 4
+    assert 0 < decode_workspace_size(256, 8, 8, 64) < decode_workspace_size(256, 32, 8, 64) < \
+        decode_workspace_size(256, 128, 8, 64)
 
 
 def test_decode_with_the_smallest_accepted_workspace(cuda_lib):
@@ -366,3 +368,49 @@ def test_decode_back_to_back_calls_of_different_shapes_share_a_workspace(cuda_li
     for k, (st, out) in enumerate(outs):
         worst = max(worst, assert_close(out_to_f64(out), refs[id(st)], "fp32", what="call %d (%s)" % (k, st.name)))
     print("24 alternating calls on one workspace: max-abs %.3g" % worst)
+
+
+@pytest.mark.parametrize("Hq,Hkv,dtype,S,ctx_hi", [
+    (8, 8, "fp16", 256, 2048),     # G = 1: units of 2 query heads
+    (16, 8, "bf16", 256, 2048),    # G = 2
+    (32, 8, "bf16", 128, 8192),    # G = 4, wide tables: paired from 512 ranges on
+    (32, 4, "fp16", 160, 2048),    # two KV-head pairs
+])
+def test_decode_head_dim_64_in_kv_head_pairs(cuda_lib, Hq, Hkv, dtype, S, ctx_hi):
+    """Steps large enough for head_dim 64 to run two adjacent KV heads as
+    one unit, against the oracle on every sequence (fp32 and 16-bit
+    outputs); then the same step with a workspace too small for the paired
+    layout but large enough for single heads, which must fall back and give
+    the same attention."""
+    rng = np.random.default_rng(Hq * 7 + Hkv)
+    ctx = rng.integers(1, ctx_hi, size=S, endpoint=True)
+    st = custom_step(ctx, Hq, Hkv, 64, dtype, seed=Hq + S)
+    ds = DeviceStep(st)
+    ref = oracle_decode_all(st.q, st.k_cache, st.v_cache, st.block_tables, st.context_lens, st.dtype)
+    out32 = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, "fp32")
+    out16 = run_decode(ds, ds.q, ds.block_tables, ds.context_lens, dtype)
+    assert int(ds.status.item()) == 0
+    e32 = assert_close(out_to_f64(out32), ref, "fp32", what="paired fp32")
+    e16 = assert_close(out_to_f64(out16), ref, dtype, what="paired %s" % dtype)
+    # the smallest accepted workspace: the single-head layout (smaller here)
+    big = decode_workspace_size(st.S, st.Hq, st.Hkv, st.d)
+    pool = torch.empty(big, dtype=torch.uint8, device="cuda")
+    from paged_kv_cache_tables_gb300 import PkvError
+    lo, hi = 16, big
+    while hi - lo > 16:
+        mid = (lo + hi) // 2 // 16 * 16
+        try:
+            paged_decode_attention(out32, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, ds.context_lens,
+                                   workspace=pool[:mid], dev_status=ds.status)
+            hi = mid
+        except PkvError as e:
+            assert e.status == -3
+            lo = mid
+    out32.fill_(float("nan"))
+    paged_decode_attention(out32, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, ds.context_lens,
+                           workspace=pool[:hi], dev_status=ds.status)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) == 0
+    e_small = assert_close(out_to_f64(out32), ref, "fp32", what="fallback fp32")
+    print("Hq %d Hkv %d %s S %d: fp32 %.3g, 16-bit %.3g; smallest workspace %d of %d: %.3g"
+          % (Hq, Hkv, dtype, S, e32, e16, hi, big, e_small))
