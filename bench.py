@@ -44,8 +44,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # append fused): dram__bytes_read.sum + dram__bytes_write.sum from one ncu
 # capture of that launch, valid for the decode source with this SHA-1 and
 # reported as null once it changes (or for another workload).
-DECODE_TRAFFIC_BYTES = 1453978112 + 4895744
-DECODE_TRAFFIC_SHA1 = "ac2ef6d2e5087ab0f8e11797990a9d4ddda3a325"
+DECODE_TRAFFIC_BYTES = 1454492416 + 5152256
+DECODE_TRAFFIC_SHA1 = "9d7097ff2fea4f3d72b534aead57f5a04087a00e"
 
 
 # launches per decode call: the control-region clear and the decode kernel
