@@ -135,8 +135,10 @@ int pkv_copy_blocks(void *dst, int64_t dst_blocks, const void *src, int64_t src_
  * Bytes of device workspace pkv_paged_decode_attention should be given on the
  * current device for these head counts and head_dim (independent of the
  * contexts).  The call also accepts less, down to two partial records per
- * warp of its grid (it then rebalances work between SMs less); below that it
- * returns PKV_ERR_WORKSPACE.  Returns 0 if no device is current.
+ * warp of its grid and four piece slots per (sequence, KV head) range (it
+ * then rebalances work between SMs less, and a step of at most 1024 ranges
+ * finds a range's pieces past the fourth through a list instead of 32 slots);
+ * below that it returns PKV_ERR_WORKSPACE.  Returns 0 if no device is current.
  */
 size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim);
 

@@ -67,8 +67,14 @@ constexpr int kMaxPieces = 4;
 constexpr int kMinWarpBlocks = 20;
 // Pieces of a range registered in its slot array; later pieces go on the
 // range's list.  A slot is one u64: record (bits 0-23), first block (24-43),
-// block count (44-63).
+// block count (44-63).  A step of at most kManySlotsRanges ranges -- where
+// long contexts are cut into many pieces -- gives each range kSlotsMax slots
+// when the workspace holds them (a merge then finds up to 32 pieces with one
+// load per lane); larger steps, whose ranges have few pieces, and the
+// smallest accepted workspace use kSlots.
 constexpr int kSlots = 4;
+constexpr int kSlotsMax = 32;
+constexpr int64_t kManySlotsRanges = 1024;
 // Merges a warp owes, kept in shared memory and run after its work (at most
 // this many; more are merged at once)
 constexpr int kDefer = 8;
@@ -98,7 +104,7 @@ struct DecodeParams {
     unsigned long long *seg_cnt;    // [S * Hkv]: (pieces registered << 32) | blocks finished in recorded pieces
     uint32_t *seg_list;             // [S * Hkv]: 1 + the range's last listed record (0: none)
     // written by the call before they are read
-    unsigned long long *seg_slots;  // [S * Hkv][kSlots]: the first pieces' slot words
+    unsigned long long *seg_slots;  // [S * Hkv][n_slots]: the first pieces' slot words
     unsigned long long *ranges;     // [total_warps]: (end << 32) | begin, offsets from the warp's range start
     long long *prefix;              // [S + 1]: blocks before sequence s (written by CTA 0)
     float *part;                    // [total_warps * rec_per_warp][rec_floats] partial records
@@ -111,6 +117,7 @@ struct DecodeParams {
                         // next record, first block, block count, unused
     int rec_per_warp;   // records each warp owns (its own range's two, two per steal)
     int steal;          // 0: no work stealing (the split is fixed by the contexts alone)
+    int n_slots;        // slots per range: kSlots or kSlotsMax
     // fused append (null: none): row s of k_new / v_new [S][Hkv][D] is the
     // token at position context_lens[s] - 1 of sequence s
     const void *k_new, *v_new;
@@ -218,7 +225,7 @@ __device__ __forceinline__ int locate_seq(const DecodeParams &p, int64_t x, int 
 
 // Log-sum-exp combination of the npieces partial records of range (s, h),
 // run by the warp that finished the range's last block.  Lane k takes piece
-// k: the first kSlots come from the range's slot array (one load each, all at
+// k: the first n_slots come from the range's slot array (one load each, all at
 // once), later ones from its list.  The pieces are taken in the order of
 // their first block (not the order they registered), so a given split always
 // combines to the same bits, and the sorted pieces must tile blocks [0, c_nb)
@@ -235,16 +242,16 @@ __device__ __forceinline__ void merge_range(const DecodeParams &p, int s, int h,
     auto rec_of = [&](uint32_t idx1) { return p.part + (size_t)(idx1 - 1) * p.rec_floats; };
     uint32_t mine = 0u;
     int key = INT32_MAX, cnt = 0;
-    const int nslot = min(npieces, kSlots);
+    const int nslot = min(npieces, p.n_slots);
     if (lane < nslot) {
-        const unsigned long long e = __ldcg(p.seg_slots + (size_t)seg * kSlots + lane);
+        const unsigned long long e = __ldcg(p.seg_slots + (size_t)seg * p.n_slots + lane);
         mine = (uint32_t)(e & ((1u << kSlotRecBits) - 1u));
         key = (int)((e >> kSlotRecBits) & ((1u << kSlotBlkBits) - 1u));
         cnt = (int)(e >> (kSlotRecBits + kSlotBlkBits));
     }
     int n = nslot;
     uint32_t rest = 0u;   // pieces past the 32nd (not produced by the usual splits) follow in list order
-    if (npieces > kSlots) {
+    if (npieces > p.n_slots) {
         uint32_t r = ld_acquire_u32(p.seg_list + seg);
         while (r != 0u && n < 32) {
             if (lane == n) mine = r;
@@ -742,8 +749,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                     trailer[1] = __int_as_float(piece_j0);
                     trailer[2] = __int_as_float(piece_n);
                     const int k = (int)(before >> 32);
-                    if (k < kSlots) {
-                        p.seg_slots[(size_t)seg * kSlots + k] = slot_pack(ri, piece_j0, piece_n);
+                    if (k < p.n_slots) {
+                        p.seg_slots[(size_t)seg * p.n_slots + k] = slot_pack(ri, piece_j0, piece_n);
                     } else {
                         // past the slots: on the range's list
                         trailer[0] = __uint_as_float(atomicExch(p.seg_list + seg, ri));
@@ -1172,7 +1179,7 @@ static int launch_decode(DecodeParams prm, const CUtensorMap &tk, const CUtensor
 // Control region, zeroed before every call:
 //   [control words 256 B][range counter words S*Hkv x 8][range list heads S*Hkv x 4]
 // then, written by the call before it reads them:
-//   [range slot arrays S*Hkv x kSlots x 8][range words, one per warp x 8]
+//   [range slot arrays S*Hkv x n_slots x 8][range words, one per warp x 8]
 //   [prefix (S+1) x 8][partial records, rec_per_warp per warp]
 // each part 256-B aligned.  A partial record holds G maxima, G sums,
 // G x head_dim accumulators and a trailer (link, first block, block count).
@@ -1185,7 +1192,7 @@ struct DecodeLayout {
     size_t ctl, seg_cnt, seg_list, clear_bytes, seg_slots, ranges, prefix, part, fixed;
 };
 
-static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
+static DecodeLayout decode_layout(int S, int Hkv, int total_warps, int n_slots) {
     DecodeLayout L;
     size_t o = 0;
     L.ctl = o;
@@ -1196,7 +1203,7 @@ static DecodeLayout decode_layout(int S, int Hkv, int total_warps) {
     o += align256((size_t)S * Hkv * 4);
     L.clear_bytes = o;
     L.seg_slots = o;
-    o += align256((size_t)S * Hkv * kSlots * 8);
+    o += align256((size_t)S * Hkv * n_slots * 8);
     L.ranges = o;
     o += align256((size_t)total_warps * 8);
     L.prefix = o;
@@ -1232,8 +1239,13 @@ static bool pair_wanted(int num_seqs, int num_q_heads, int num_kv_heads, int hea
     return ranges >= (max_blocks_per_seq > 128 ? 512 : 256);
 }
 
-static size_t workspace_bytes_for(int num_seqs, int num_q_heads, int units, int head_dim, int nw, size_t records) {
-    return decode_layout(num_seqs, units, nw).fixed +
+static int slots_for(int num_seqs, int units) {
+    return (int64_t)num_seqs * units <= kManySlotsRanges ? kSlotsMax : kSlots;
+}
+
+static size_t workspace_bytes_for(int num_seqs, int num_q_heads, int units, int head_dim, int nw, size_t records,
+                                  int n_slots) {
+    return decode_layout(num_seqs, units, nw, n_slots).fixed +
            records * (size_t)record_floats(num_q_heads / units, head_dim) * sizeof(float);
 }
 
@@ -1244,10 +1256,10 @@ size_t decode_workspace_min(int num_seqs, int num_q_heads, int num_kv_heads, int
     int sms = 0;
     if (current_sm_count(&sms) != PKV_OK) return 0;
     const int nw = sms * kDecodeWarps;
-    size_t need = workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads, head_dim, nw, records_min(nw));
+    size_t need = workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads, head_dim, nw, records_min(nw), kSlots);
     if (pair_eligible(num_q_heads, num_kv_heads, head_dim))
         need = std::min(need, workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads / 2, head_dim, nw,
-                                                  records_min(nw)));
+                                                  records_min(nw), kSlots));
     return need;
 }
 
@@ -1260,10 +1272,11 @@ extern "C" size_t pkv_decode_workspace_size(int num_seqs, int num_q_heads, int n
     if (current_sm_count(&sms) != PKV_OK) return 0;
     const int nw = sms * kDecodeWarps;
     // large enough for either form
-    size_t need = workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads, head_dim, nw, records_recommended(nw));
+    size_t need = workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads, head_dim, nw, records_recommended(nw),
+                                      slots_for(num_seqs, num_kv_heads));
     if (pair_eligible(num_q_heads, num_kv_heads, head_dim))
         need = std::max(need, workspace_bytes_for(num_seqs, num_q_heads, num_kv_heads / 2, head_dim, nw,
-                                                  records_recommended(nw)));
+                                                  records_recommended(nw), slots_for(num_seqs, num_kv_heads / 2)));
     return need;
 }
 
@@ -1315,7 +1328,7 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
         if (max_sms > 0 && grid > max_sms) grid = max_sms;
         if (grid < 1) grid = 1;
         total_warps = grid * kDecodeWarps;
-        lay = decode_layout(num_seqs, units, total_warps);
+        lay = decode_layout(num_seqs, units, total_warps, kSlots);
         rec_bytes = (size_t)record_floats(Gu, head_dim) * sizeof(float);
         // the paired form falls back to single heads when its layout does not fit
         if (pair && workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) {
@@ -1327,6 +1340,16 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     // range offsets are 32-bit fields
     if (upper / total_warps + 1 >= ((int64_t)1 << 30)) return PKV_ERR_UNSUPPORTED;
     if (workspace_bytes < lay.fixed + records_min(total_warps) * rec_bytes) return PKV_ERR_WORKSPACE;
+    // the full slot arrays for a step of few ranges, when they leave the
+    // recommended records room
+    int n_slots = kSlots;
+    if (slots_for(num_seqs, units) == kSlotsMax) {
+        const DecodeLayout big = decode_layout(num_seqs, units, total_warps, kSlotsMax);
+        if (workspace_bytes >= big.fixed + records_recommended(total_warps) * rec_bytes) {
+            lay = big;
+            n_slots = kSlotsMax;
+        }
+    }
     // records per warp (record numbers live in 24-bit slot fields)
     size_t per_warp = (workspace_bytes - lay.fixed) / rec_bytes / total_warps;
     const size_t max_per_warp = (((size_t)1 << kSlotRecBits) - 2) / total_warps;
@@ -1367,6 +1390,7 @@ int decode_attention(void *out, const void *q, const void *k_cache, const void *
     // by the contexts alone and the output bits repeat from call to call
     const char *det = std::getenv("PKV_DETERMINISTIC");
     prm.steal = (det && det[0] == '1') ? 0 : 1;
+    prm.n_slots = n_slots;
     prm.k_new = k_new;
     prm.v_new = v_new;
     prm.k_cache = const_cast<void *>(k_cache);

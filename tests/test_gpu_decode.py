@@ -292,12 +292,13 @@ def test_workspace_size_is_independent_of_contexts(cuda_lib):
 
 
 def test_decode_with_the_smallest_accepted_workspace(cuda_lib):
-    """The call accepts a workspace down to two partial records per warp; a
-    warp then steals only when its own share left no piece.  The smallest
-    accepted size is found by bisection (a smaller workspace is rejected
-    before anything is enqueued); it is the fixed part plus two records per
-    warp, eight fewer per warp than the recommended size.  The 8B-shaped step
-    run on it still matches the oracle on every sequence."""
+    """The call accepts a workspace down to two partial records per warp and
+    four slots per range; a warp then steals only when its own share left no
+    piece.  The smallest accepted size is found by bisection (a smaller
+    workspace is rejected before anything is enqueued); it is eight records
+    per warp (and, in a step of few ranges, 28 slots per range) short of the
+    recommended size.  The 8B-shaped step run on it still matches the oracle
+    on every sequence."""
     from paged_kv_cache_tables_gb300 import PkvError
     st = make_step("llama8b")
     ds = DeviceStep(st)
@@ -327,7 +328,11 @@ def test_decode_with_the_smallest_accepted_workspace(cuda_lib):
     G = st.Hq // st.Hkv
     rec_bytes = 4 * (((2 * G + G * st.d + 3) & ~3) + 4)
     n_warps = 8 * torch.cuda.get_device_properties(0).multi_processor_count
-    assert big - hi == 8 * n_warps * rec_bytes
+    a256 = lambda x: (x + 255) // 256 * 256
+    # the recommended size adds eight records per warp, and 28 more slots per
+    # range in a step of at most 1024 ranges
+    slots = 32 if st.S * st.Hkv <= 1024 else 4
+    assert big - hi == 8 * n_warps * rec_bytes + a256(st.S * st.Hkv * slots * 8) - a256(st.S * st.Hkv * 4 * 8)
     out.fill_(float("nan"))
     paged_decode_attention(out, ds.q, ds.k_cache, ds.v_cache, ds.block_tables, cl, workspace=pool[:hi],
                            dev_status=ds.status)
