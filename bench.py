@@ -44,8 +44,8 @@ def decode_bytes(ctx, Hq, Hkv, d, esize=2, bs=16):
 # append fused): dram__bytes_read.sum + dram__bytes_write.sum from one ncu
 # capture of that launch, valid for the decode source with this SHA-1 and
 # reported as null once it changes (or for another workload).
-DECODE_TRAFFIC_BYTES = 1454626304 + 4870656
-DECODE_TRAFFIC_SHA1 = "7917bf16399a4b295439472f4b9cc5333cb1de0a"
+DECODE_TRAFFIC_BYTES = 1454636544 + 4925696
+DECODE_TRAFFIC_SHA1 = "9d5df3620f33531e1f5fc04ecfd5f2408b0c6255"
 
 
 # launches per decode call: the control-region clear and the decode kernel

@@ -452,7 +452,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     int local_max = 0;
     if (tid < kDecodeWarps) plan_s[tid] = -1;   // (the scan's barriers order this before the plan)
     for (int s = tid; s < p.S; s += blockDim.x) {
-        const int nb = blocks_of(p.context_lens, s, p.max_blocks, p.dev_status, nullptr);
+        // (a bad context is reported after the wait when the plan runs before it)
+        const int nb = blocks_of(p.context_lens, s, p.max_blocks, one_pass ? nullptr : p.dev_status, nullptr);
         local += nb;
         local_max = max(local_max, nb);
     }
@@ -502,7 +503,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
     if (one_pass) {
         pdl_wait_primary();
-        if (blockIdx.x == 0 && tid < p.S) p.prefix[tid] = incl0 - local;
+        if (blockIdx.x == 0 && tid < p.S) {
+            p.prefix[tid] = incl0 - local;
+            blocks_of(p.context_lens, tid, p.max_blocks, p.dev_status, nullptr);
+        }
     }
     if (blockIdx.x == 0 && tid == 0) p.prefix[p.S] = total_nblk;
 
@@ -590,12 +594,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             };
             auto issue = [&](uint32_t slot, int blk) {
                 if (lane == 0) {
-                    // cache row of the tile (its first KV head's, when paired)
-                    int row = (blk * Hkv + ph) * 16 * (PAIR ? 2 : 1);
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                        row = p.num_blocks * Hkv * 16 * (PAIR ? 2 : 1);   // past the end: the load fills zeros
-                    }
+                    // cache row of the tile (its first KV head's, when paired);
+                    // past the end for a bad block id: the load fills zeros
+                    const bool bad_blk = blk < 0 || blk >= p.num_blocks;
+                    if (bad_blk) set_status(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                    const int row = ((bad_blk ? p.num_blocks : blk) * Hkv + (bad_blk ? 0 : ph)) * 16 * (PAIR ? 2 : 1);
                     const int stage = (int)(slot % STAGES);
                     uint64_t *bar = &wbar[stage];
                     // the last block of a range also brings the range's new
